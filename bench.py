@@ -1,0 +1,398 @@
+"""Benchmark of the fused GDN decode step on GB300.
+
+One step is one call of the whole decode path (conv, SiLU, norms, gates, the
+gated delta rule, the gated RMSNorm) over one batch of synthetic input: by
+default the batched-decode workload of 64 sequences x 36 layers x 1 token with
+state ~N(0, 0.05). The metric is GDN state updates per second
+(sequence x layer x valid token) together with the achieved HBM bandwidth
+against the measured GB300 copy peak.
+
+Timed regions use CUDA events on the launching stream, bracketed by a barrier
+and a device synchronise. The state (7.3 GB at the default workload) is far
+larger than the 129 MB L2, so no step finds its inputs in L2.
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
+the same workload, on this machine's host cores.
+
+Multi-GPU: ``torchrun --nproc-per-node N bench.py --gpus N`` runs one process
+per GPU; each rank takes its own 64 sequences of a 64*N-sequence batch (weak
+scaling, no collective on the data path) and the slowest rank's time counts.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+# The oracle legs run single-threaded numpy: pin BLAS pools to one thread before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_b64_l36_t1"
+METRIC = "GDN state-updates/sec (seq*layer*token) and achieved HBM GB/s vs GB300 peak"
+UNIT = "state-updates/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_decode_step_kernel_traffic.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")
+
+
+# ------------------------------------------------------------------ args --
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------- distributed ----
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def shard_rows(rank: int, per_rank: int) -> tuple:
+    """Rank r owns sequences [r * per_rank, (r + 1) * per_rank) of the global batch."""
+    return rank * per_rank, (rank + 1) * per_rank
+
+
+# ------------------------------------------------------------- counting --
+def valid_tokens(w: W.Workload, lens) -> int:
+    """Valid (sequence, layer, token) updates of one step."""
+    if lens is None:
+        return w.B * w.L * w.T
+    return int(np.sum(lens)) * w.L
+
+
+def algorithmic_bytes(w: W.Workload, lens) -> dict:
+    """Bytes one step must move at least: each state tile and conv history read and
+    written once, each valid token's inputs read and its y written once, each layer's
+    weights read once."""
+    B, L, T = w.B, w.L, w.T
+    tok = valid_tokens(w, lens)  # sequence x layer x valid token
+    state = B * L * 48 * 128 * 128 * 4 * 2
+    conv = B * L * 10240 * 3 * 4 * 2
+    per_token = (10240 + 6144 + 48 + 48 + 6144) * 4
+    weights = L * (10240 * 4 + 48 + 48 + 128) * 4
+    if lens is not None:  # untouched sequences (length 0) move no state; lengths here are >= 1
+        pass
+    return {"state": state, "total": state + conv + tok * per_token + weights}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def committed_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    text = open(TRAFFIC_FILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    return float(m.group(1)) if h.group(1) == src else None
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.remove(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r[0] for r in rows]
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------- cpu legs ----
+def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None):
+    """Times the oracle on (sequence, layer) slices of the workload until the budget
+    is spent. Returns (updates done, oracle seconds, slices)."""
+    import oracle
+
+    lens = W.seq_lens(w)
+    done, spent, slices = 0, 0.0, 0
+    order = [(b, l) for l in range(w.L) for b in range(w.B)]
+    rng = np.random.default_rng(7)
+    rng.shuffle(order)
+    for b, l in order:
+        if spent >= seconds or (max_slices is not None and slices >= max_slices):
+            break
+        sl = W.sequence_slice(w, b, l)
+        wt = W.layer_weights(w, l)
+        n = w.T if lens is None else int(lens[b])
+        t0 = time.perf_counter()
+        oracle.gdn_decode_slice(sl, wt, n)
+        spent += time.perf_counter() - t0
+        done += n
+        slices += 1
+    return done, spent, slices
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))  # the whole run stays near two minutes
+    per_step = min(per_step, 6.0)
+    for _ in range(args.warmup):
+        oracle_sample(w, min(per_step, 1.0))
+    done_total, spent_total, slices_total = 0, 0.0, 0
+    for _ in range(args.steps):
+        d, s, n = oracle_sample(w, per_step)
+        done_total += d
+        spent_total += s
+        slices_total += n
+    value = done_total / spent_total
+    sample = (f"{slices_total} (sequence, layer) slices of {w.name} over {args.steps} steps "
+              f"(~{per_step:.1f} s of oracle time each), fp64 numpy, one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * spent_total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "T": w.T, "head_dim": 128, "v_heads": 48},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- gpu arm ----
+def run_gdn(args, w_global, world, rank, local):
+    import gated_deltanet_linear_step_gb300 as g
+
+    g.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    per_rank = W.WORKLOADS[args.workload].B
+    rows = shard_rows(rank, per_rank)
+    w = w_global.scaled(B=per_rank) if world > 1 else w_global
+    t = W.device_inputs(w_global, dev, threads=16, batch_rows=rows)
+    lens_all = W.seq_lens(w_global)
+    lens = None if lens_all is None else lens_all[rows[0]:rows[1]]
+    y = torch.empty(t["z"].shape, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if t["seq_len"] is None:
+            g.gdn_decode_step(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
+                              t["ssm_norm"], t["conv_state"], t["state"], y)
+        else:
+            g.gdn_decode_step_varlen(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
+                                     t["ssm_norm"], t["conv_state"], t["state"], y, t["seq_len"])
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s, e in ev:
+            s.record(stream)
+            step()
+            e.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in ev]
+    assert g.gdn_read_device_error(device=dev) == 0, "the kernel reported a device error"
+
+    updates_rank = valid_tokens(w, lens) * args.steps
+    total_updates = sum_over_ranks(updates_rank, world, dev)
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+    value = total_updates / (max_ms / 1000.0)
+
+    # end to end through the public API: pinned host inputs -> device -> step -> y back to the host
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.empty(t[k].shape, dtype=t[k].dtype, pin_memory=True) for k in ("qkv", "z", "alpha", "beta")}
+        for k in host:
+            host[k].copy_(t[k])
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        bi = sum(v.numel() * v.element_size() for v in host.values())
+        bo = y_host.numel() * y_host.element_size()
+
+        def e2e_step():
+            for k in host:
+                t[k].copy_(host[k], non_blocking=True)
+            step()
+            y_host.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        e2e = {"value": total_updates / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": bi,
+               "d2h_bytes_per_step": bo}
+
+    # roofline of the (only) kernel
+    bytes_alg = algorithmic_bytes(w, lens)
+    mean_launch_s = float(np.mean(launch_ms)) / 1000.0
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_alg["total"] / mean_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": committed_traffic(), "peak_kind": peak_kind,
+                "state_only_gbs": bytes_alg["state"] / mean_launch_s / 1e9,
+                "algorithmic_bytes_per_launch": bytes_alg["total"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        done, spent, slices = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": done / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{slices} random (sequence, layer) slices of {w.name}, {done} updates, "
+                         f"{spent:.1f} s, fp64 numpy on one host thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w_global.name, "B": w_global.B, "L": w.L, "T": w.T, "B_per_gpu": w.B,
+                       "head_dim": 128, "k_heads": 16, "v_heads": 48, "conv_channels": 10240,
+                       "l2": "state working set far larger than the 129 MB L2; updated in place every step",
+                       "parallelism": f"dp{world} (sequences sharded, no collective)"},
+            "clocks": clocks.summary(), "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline,
+            "cpu_baseline": cpu,
+            "launch_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
+                          "max": float(np.max(launch_ms))},
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    base = W.WORKLOADS[args.workload]
+    w_global = base.scaled(B=base.B * world) if world > 1 else base
+    if args.impl == "reference":
+        run_reference(args, base, world, rank)
+    else:
+        run_gdn(args, w_global, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+"""Thin ctypes binding of ``libgdn.so`` (C ABI in ``include/gdn.h``).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernel behind the C ABI. Functions take contiguous CUDA torch tensors, derive
+B, L and T from ``qkv``'s shape, check every other tensor's shape, and pass
+raw device pointers plus the stream (the current torch stream of the
+tensors' device unless one is given). A non-OK status raises ``GdnError``
+with the library's message. There is no fallback: without the built library
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+HEAD_DIM = 128
+K_HEADS = 16
+V_HEADS = 48
+CONV_CHANNELS = 10240
+VALUE_DIM = 6144
+D_CONV = 4
+
+FLAG_NO_STATE_WRITE = 0x1
+FLAG_NO_Y = 0x2
+FLAG_SILU_GATE = 0x4
+
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_ALIAS",
+          5: "GDN_ERR_CUDA", 6: "GDN_ERR_FLAGS"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads ``libgdn.so`` once; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        step_args = [_P] * 11 + [_I, _I, _I, _P]
+        lib.gdn_decode_step.argtypes = step_args
+        lib.gdn_decode_step_varlen.argtypes = [_P] * 12 + [_I, _I, _I, _P]
+        lib.gdn_verify_window.argtypes = [_P] * 12 + [_I, _I, _I, _P]
+        lib.gdn_verify_commit.argtypes = [_P] * 9 + [_I, _I, _I, _P]
+        lib.gdn_decode_step_ex.argtypes = [_P] * 12 + [_I, _I, _I, ctypes.c_uint32, _P]
+        for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
+                   "gdn_decode_step_ex", "gdn_get_geometry", "gdn_read_device_error"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+        lib.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.gdn_last_error.argtypes = []
+        lib.gdn_last_error.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def gdn_last_error() -> str:
+    return load_library().gdn_last_error().decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise GdnError(status, gdn_last_error())
+
+
+def _ptr(t, name, shape, dtype=torch.float32, device=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be on {device or 'a CUDA device'}, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _shapes(qkv):
+    if not isinstance(qkv, torch.Tensor) or qkv.dim() != 4 or qkv.shape[3] != CONV_CHANNELS:
+        raise ValueError(f"qkv must be a [B][L][T][{CONV_CHANNELS}] tensor")
+    B, L, T = (int(s) for s in qkv.shape[:3])
+    return B, L, T
+
+
+def _step_ptrs(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, need_y=True):
+    B, L, T = _shapes(qkv)
+    dev = qkv.device
+    return (B, L, T, dev, [
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev, optional=not need_y),
+        _ptr(alpha, "alpha", (B, L, T, V_HEADS), device=dev),
+        _ptr(beta, "beta", (B, L, T, V_HEADS), device=dev),
+        _ptr(dt, "dt", (L, V_HEADS), device=dev),
+        _ptr(ssm_a, "ssm_a", (L, V_HEADS), device=dev),
+        _ptr(conv_w, "conv_w", (L, CONV_CHANNELS, D_CONV), device=dev),
+        _ptr(ssm_norm, "ssm_norm", (L, HEAD_DIM), device=dev, optional=not need_y),
+        _ptr(conv_state, "conv_state", (B, L, CONV_CHANNELS, D_CONV - 1), device=dev),
+        _ptr(state, "state", (B, L, V_HEADS, HEAD_DIM, HEAD_DIM), device=dev),
+        _ptr(y, "y", (B, L, T, VALUE_DIM), device=dev, optional=not need_y),
+    ])
+
+
+def gdn_decode_step(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, stream=None):
+    """One decode call over T tokens; updates ``conv_state`` and ``state`` in place and writes ``y``."""
+    lib = load_library()
+    B, L, T, dev, p = _step_ptrs(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y)
+    with torch.cuda.device(dev):
+        _check(lib.gdn_decode_step(*p, B, L, T, _stream_handle(stream, dev)))
+
+
+def gdn_decode_step_varlen(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len,
+                           stream=None):
+    """``gdn_decode_step`` applying only the first ``seq_len[b]`` tokens of sequence b (int32 [B] on the device)."""
+    lib = load_library()
+    B, L, T, dev, p = _step_ptrs(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y)
+    sl = _ptr(seq_len, "seq_len", (B,), dtype=torch.int32, device=dev, optional=True)
+    with torch.cuda.device(dev):
+        _check(lib.gdn_decode_step_varlen(*p, sl, B, L, T, _stream_handle(stream, dev)))
+
+
+def gdn_verify_window(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len=None,
+                      stream=None):
+    """Phase 1 of a verify window: y for the draft tokens; ``state`` and ``conv_state`` are only read."""
+    lib = load_library()
+    B, L, T, dev, p = _step_ptrs(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y)
+    sl = _ptr(seq_len, "seq_len", (B,), dtype=torch.int32, device=dev, optional=True)
+    with torch.cuda.device(dev):
+        _check(lib.gdn_verify_window(*p, sl, B, L, T, _stream_handle(stream, dev)))
+
+
+def gdn_verify_commit(qkv, alpha, beta, dt, ssm_a, conv_w, conv_state, state, n_keep, stream=None):
+    """Phase 2: advance ``state`` and ``conv_state`` by ``n_keep[b]`` accepted tokens (int32 [B] on the device)."""
+    lib = load_library()
+    B, L, T = _shapes(qkv)
+    dev = qkv.device
+    p = [
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(alpha, "alpha", (B, L, T, V_HEADS), device=dev),
+        _ptr(beta, "beta", (B, L, T, V_HEADS), device=dev),
+        _ptr(dt, "dt", (L, V_HEADS), device=dev),
+        _ptr(ssm_a, "ssm_a", (L, V_HEADS), device=dev),
+        _ptr(conv_w, "conv_w", (L, CONV_CHANNELS, D_CONV), device=dev),
+        _ptr(conv_state, "conv_state", (B, L, CONV_CHANNELS, D_CONV - 1), device=dev),
+        _ptr(state, "state", (B, L, V_HEADS, HEAD_DIM, HEAD_DIM), device=dev),
+        _ptr(n_keep, "n_keep", (B,), dtype=torch.int32, device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_verify_commit(*p, B, L, T, _stream_handle(stream, dev)))
+
+
+def gdn_decode_step_ex(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len=None,
+                       flags=0, stream=None):
+    """``gdn_decode_step_varlen`` with ``FLAG_*`` bits (no state write, no y, SiLU output gate)."""
+    lib = load_library()
+    need_y = not (flags & FLAG_NO_Y)
+    B, L, T, dev, p = _step_ptrs(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y,
+                                 need_y=need_y)
+    sl = _ptr(seq_len, "seq_len", (B,), dtype=torch.int32, device=dev, optional=True)
+    with torch.cuda.device(dev):
+        _check(lib.gdn_decode_step_ex(*p, sl, B, L, T, int(flags), _stream_handle(stream, dev)))
+
+
+def gdn_get_geometry() -> dict:
+    out = (ctypes.c_int32 * 8)()
+    _check(load_library().gdn_get_geometry(out))
+    keys = ("head_dim", "k_heads", "v_heads", "conv_channels", "value_dim", "d_conv", "max_t", "cta_threads")
+    return dict(zip(keys, list(out)))
+
+
+def gdn_read_device_error(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the kernel's device error word."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    out = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        _check(load_library().gdn_read_device_error(_stream_handle(stream, dev), ctypes.byref(out)))
+    return int(out.value)

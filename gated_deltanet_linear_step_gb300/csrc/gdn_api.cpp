@@ -1,0 +1,199 @@
+// gdn_api.cpp - the C ABI declared in include/gdn.h: argument checks, error
+// messages, and the hand-off to the fused kernel in gdn_step.cu.
+
+#include "gdn.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "gdn_launch.h"
+
+static_assert(GDN_HEAD_DIM == gdn::kHeadDim, "geometry mismatch");
+static_assert(GDN_K_HEADS == gdn::kKHeads, "geometry mismatch");
+static_assert(GDN_V_HEADS == gdn::kVHeads, "geometry mismatch");
+static_assert(GDN_CONV_CHANNELS == gdn::kConvChannels, "geometry mismatch");
+static_assert(GDN_VALUE_DIM == gdn::kValueDim, "geometry mismatch");
+static_assert(GDN_D_CONV == gdn::kDConv, "geometry mismatch");
+static_assert(GDN_MAX_T == gdn::kMaxT, "geometry mismatch");
+static_assert(GDN_FLAG_NO_STATE_WRITE == gdn::kNoStateWrite && GDN_FLAG_NO_Y == gdn::kNoY &&
+                  GDN_FLAG_SILU_GATE == gdn::kSiluGate,
+              "flag mismatch");
+
+namespace {
+
+thread_local std::string t_last_error;
+
+gdn_status fail(gdn_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+struct Span {
+    const char* name;
+    const void* p;
+    unsigned long long bytes;
+    bool output;
+};
+
+bool overlaps(const Span& a, const Span& b) {
+    if (a.p == nullptr || b.p == nullptr || a.bytes == 0 || b.bytes == 0) return false;
+    const unsigned long long a0 = reinterpret_cast<unsigned long long>(a.p);
+    const unsigned long long b0 = reinterpret_cast<unsigned long long>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Checks and launches one decode-step call. `state_ro`/`conv_ro` mark the
+// states as read only (no alias rule for them as outputs).
+gdn_status run(const float* qkv, const float* z, const float* alpha, const float* beta, const float* dt,
+               const float* ssm_a, const float* conv_w, const float* ssm_norm, float* conv_state, float* state,
+               float* y, const int32_t* seq_len, int B, int L, int T, uint32_t flags, void* stream,
+               const char* fn) {
+    t_last_error.clear();
+    const uint32_t known = gdn::kNoStateWrite | gdn::kNoY | gdn::kSiluGate;
+    if (flags & ~known) return fail(GDN_ERR_FLAGS, "%s: unknown flag bits 0x%x", fn, flags & ~known);
+    const bool want_y = (flags & gdn::kNoY) == 0;
+    const bool write_state = (flags & gdn::kNoStateWrite) == 0;
+
+    const struct {
+        const char* name;
+        const void* p;
+        bool required;
+    } ptrs[] = {{"qkv", qkv, true},       {"z", z, want_y},           {"alpha", alpha, true},
+                {"beta", beta, true},     {"dt", dt, true},           {"ssm_a", ssm_a, true},
+                {"conv_w", conv_w, true}, {"ssm_norm", ssm_norm, want_y}, {"conv_state", conv_state, true},
+                {"state", state, true},   {"y", y, want_y}};
+    for (const auto& q : ptrs) {
+        if (q.required && q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if (q.p != nullptr && (reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (seq_len != nullptr && (reinterpret_cast<unsigned long long>(seq_len) & 3ull) != 0)
+        return fail(GDN_ERR_ALIGN, "%s: seq_len is not 4-byte aligned", fn);
+    if (B < 1 || L < 1) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d must be >= 1", fn, B, L);
+    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
+
+    // Byte sizes in 64-bit; B * L tiles of 3 MB must stay addressable.
+    const unsigned long long b = static_cast<unsigned long long>(B), l = static_cast<unsigned long long>(L),
+                             t = static_cast<unsigned long long>(T);
+    if (b * l > (1ull << 40) / (48ull * 65536ull))
+        return fail(GDN_ERR_SHAPE, "%s: B*L=%llu is too large", fn, b * l);
+    const unsigned long long blt = b * l * t;
+    const Span spans[] = {
+        {"qkv", qkv, blt * gdn::kConvChannels * 4, false},
+        {"z", z, want_y ? blt * gdn::kValueDim * 4 : 0, false},
+        {"alpha", alpha, blt * gdn::kVHeads * 4, false},
+        {"beta", beta, blt * gdn::kVHeads * 4, false},
+        {"dt", dt, l * gdn::kVHeads * 4, false},
+        {"ssm_a", ssm_a, l * gdn::kVHeads * 4, false},
+        {"conv_w", conv_w, l * gdn::kConvChannels * gdn::kDConv * 4, false},
+        {"ssm_norm", ssm_norm, want_y ? l * gdn::kHeadDim * 4 : 0, false},
+        {"seq_len", seq_len, seq_len ? b * 4 : 0, false},
+        {"conv_state", conv_state, b * l * gdn::kConvChannels * (gdn::kDConv - 1) * 4, write_state},
+        {"state", state, b * l * gdn::kVHeads * 65536ull, write_state},
+        {"y", y, want_y ? blt * gdn::kValueDim * 4 : 0, want_y},
+    };
+    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
+    for (int i = 0; i < n; ++i) {
+        if (!spans[i].output) continue;
+        for (int k = 0; k < n; ++k)
+            if (k != i && overlaps(spans[i], spans[k]))
+                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
+    }
+
+    gdn::StepArgs a;
+    a.qkv = qkv;
+    a.z = z;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.dt = dt;
+    a.ssm_a = ssm_a;
+    a.conv_w = conv_w;
+    a.ssm_norm = ssm_norm;
+    a.conv_state = conv_state;
+    a.state = state;
+    a.y = y;
+    a.seq_len = seq_len;
+    a.B = B;
+    a.L = L;
+    a.T = T;
+    a.flags = flags;
+    const cudaError_t e = gdn::launch_decode_step(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decode_step(const float* qkv, const float* z, const float* alpha, const float* beta,
+                           const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                           float* conv_state, float* state, float* y, int B, int L, int T, void* stream) {
+    return run(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, nullptr, B, L, T, 0u,
+               stream, "gdn_decode_step");
+}
+
+gdn_status gdn_decode_step_varlen(const float* qkv, const float* z, const float* alpha, const float* beta,
+                                  const float* dt, const float* ssm_a, const float* conv_w,
+                                  const float* ssm_norm, float* conv_state, float* state, float* y,
+                                  const int32_t* seq_len, int B, int L, int T, void* stream) {
+    return run(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len, B, L, T, 0u,
+               stream, "gdn_decode_step_varlen");
+}
+
+gdn_status gdn_verify_window(const float* qkv, const float* z, const float* alpha, const float* beta,
+                             const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                             const float* conv_state, const float* state, float* y, const int32_t* seq_len,
+                             int B, int L, int T, void* stream) {
+    // The kernel only reads state and conv_state under kNoStateWrite.
+    return run(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, const_cast<float*>(conv_state),
+               const_cast<float*>(state), y, seq_len, B, L, T, gdn::kNoStateWrite, stream, "gdn_verify_window");
+}
+
+gdn_status gdn_verify_commit(const float* qkv, const float* alpha, const float* beta, const float* dt,
+                             const float* ssm_a, const float* conv_w, float* conv_state, float* state,
+                             const int32_t* n_keep, int B, int L, int T, void* stream) {
+    if (n_keep == nullptr) return fail(GDN_ERR_NULL, "gdn_verify_commit: n_keep is NULL");
+    return run(qkv, nullptr, alpha, beta, dt, ssm_a, conv_w, nullptr, conv_state, state, nullptr, n_keep, B, L, T,
+               gdn::kNoY, stream, "gdn_verify_commit");
+}
+
+gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alpha, const float* beta,
+                              const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                              float* conv_state, float* state, float* y, const int32_t* seq_len, int B, int L,
+                              int T, uint32_t flags, void* stream) {
+    return run(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len, B, L, T, flags,
+               stream, "gdn_decode_step_ex");
+}
+
+const char* gdn_last_error(void) { return t_last_error.c_str(); }
+
+gdn_status gdn_get_geometry(int32_t out[8]) {
+    if (out == nullptr) return fail(GDN_ERR_NULL, "gdn_get_geometry: out is NULL");
+    out[0] = gdn::kHeadDim;
+    out[1] = gdn::kKHeads;
+    out[2] = gdn::kVHeads;
+    out[3] = gdn::kConvChannels;
+    out[4] = gdn::kValueDim;
+    out[5] = gdn::kDConv;
+    out[6] = gdn::kMaxT;
+    out[7] = gdn::kThreads;
+    return GDN_OK;
+}
+
+gdn_status gdn_read_device_error(void* stream, uint32_t* out) {
+    t_last_error.clear();
+    if (out == nullptr) return fail(GDN_ERR_NULL, "gdn_read_device_error: out is NULL");
+    const cudaError_t e = gdn::read_device_error(static_cast<cudaStream_t>(stream), out);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "gdn_read_device_error: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+}  // extern "C"

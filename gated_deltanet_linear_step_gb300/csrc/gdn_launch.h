@@ -1,0 +1,52 @@
+// Internal interface between the C ABI (gdn_api.cpp) and the CUDA kernels (gdn_step.cu).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace gdn {
+
+// Compiled geometry (header comment of Winery-Strata include/strata/core/layer.hpp;
+// q|k|v views of gdn_layer step 4 on src/core/layer.cpp).
+constexpr int kHeadDim = 128;
+constexpr int kKHeads = 16;
+constexpr int kVHeads = 48;
+constexpr int kGroup = kVHeads / kKHeads;  // v heads per k head
+constexpr int kConvChannels = 10240;
+constexpr int kValueDim = kVHeads * kHeadDim;
+constexpr int kDConv = 4;
+constexpr int kKOffset = kKHeads * kHeadDim;      // 2048
+constexpr int kVOffset = 2 * kKHeads * kHeadDim;  // 4096
+constexpr int kMaxT = 1024;
+constexpr int kThreads = kGroup * kHeadDim;       // 384: one thread per state column of 3 tiles
+
+// Kernel behaviour bits (match GDN_FLAG_* in gdn.h).
+constexpr uint32_t kNoStateWrite = 0x1u;
+constexpr uint32_t kNoY = 0x2u;
+constexpr uint32_t kSiluGate = 0x4u;
+
+struct StepArgs {
+    const float* qkv;
+    const float* z;
+    const float* alpha;
+    const float* beta;
+    const float* dt;
+    const float* ssm_a;
+    const float* conv_w;
+    const float* ssm_norm;
+    float* conv_state;
+    float* state;
+    float* y;
+    const int32_t* seq_len;
+    int B, L, T;
+    uint32_t flags;
+};
+
+// Launches the fused decode-step kernel on `stream`. Returns the launch status.
+cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream);
+
+// Synchronises `stream`, then reads and clears the device error word.
+cudaError_t read_device_error(cudaStream_t stream, uint32_t* out);
+
+}  // namespace gdn

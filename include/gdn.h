@@ -1,0 +1,166 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) Gated DeltaNet decode-step library.
+ *
+ * One call runs the whole decode step of a GDN layer's recurrent mixer for B
+ * sequences x L layers x T tokens, fused into a single CUDA kernel:
+ *
+ *   causal depthwise conv (d_conv = 4) against the rolling conv_state
+ *   -> SiLU over all 10240 conv channels, before the q|k|v split
+ *   -> L2 norm of each 128-wide q and k head (eps 1e-6); v untouched
+ *   -> q scaled by 1/sqrt(128) after its norm
+ *   -> beta = sigmoid(beta_raw); decay = exp(softplus(alpha_raw + dt) * ssm_a)
+ *   -> per v head h (reading q/k head h/3), on its 128x128 fp32 state S:
+ *        S *= decay; kv = S^T k; d = (v - kv) * beta; S += k d^T; o = S^T q
+ *   -> y = rms_norm(o per head, ssm_norm, eps 1e-6) * sigmoid(z)
+ *
+ * This order is the one listed in the header comment of the Winery-Strata
+ * page include/strata/core/layer.hpp and composed by gdn_layer (steps 3 to 7)
+ * on the page src/core/layer.cpp. The multi-token window and its commit follow
+ * Verifier::record_window and the commit graph on the page src/core/verify.cpp.
+ *
+ * Conventions for every entry point below.
+ *  - Geometry is compiled in: head dim S = 128, 16 q/k heads, 48 v heads,
+ *    10240 conv channels (q at [0, 2048), k at [2048, 4096), v at
+ *    [4096, 10240)), value dim 6144, d_conv = 4.
+ *  - Every tensor is fp32 (seq_len is int32), contiguous, row-major, indices
+ *    listed outermost first, in DEVICE-accessible memory, 16-byte aligned.
+ *    The caller owns all memory; the library allocates nothing and keeps no
+ *    per-call state.
+ *  - state is [B][L][48][128 (i, k index)][128 (j, v index)]: element
+ *    S[i][j] multiplies k[i] in kv = S^T k. conv_state is [B][L][10240][3],
+ *    oldest input first. conv_w is [L][10240][4]: tap 0 multiplies the oldest
+ *    history entry, tap 3 the current input.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and may be captured in a CUDA graph. Arguments are
+ *    checked on the host before anything is launched; on a non-OK status
+ *    nothing was launched and gdn_last_error() describes why. Errors raised
+ *    while the kernel runs surface at the caller's next synchronisation.
+ *  - Outputs may not overlap any other buffer of the call (GDN_ERR_ALIAS).
+ *    Inputs may overlap each other.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_HEAD_DIM 128
+#define GDN_K_HEADS 16
+#define GDN_V_HEADS 48
+#define GDN_CONV_CHANNELS 10240
+#define GDN_VALUE_DIM 6144
+#define GDN_D_CONV 4
+#define GDN_MAX_T 1024
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,   /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,  /* B, L or T out of range, or a size overflows */
+    GDN_ERR_ALIGN = 3,  /* a pointer is not 16-byte aligned (seq_len: 4-byte) */
+    GDN_ERR_ALIAS = 4,  /* an output overlaps another buffer of the call */
+    GDN_ERR_CUDA = 5,   /* the CUDA runtime refused a query or the launch */
+    GDN_ERR_FLAGS = 6   /* unknown bits in a flags word */
+} gdn_status;
+
+/* Flags of gdn_decode_step_ex. */
+#define GDN_FLAG_NO_STATE_WRITE 0x1u /* leave state and conv_state untouched */
+#define GDN_FLAG_NO_Y 0x2u           /* write no y (y may be NULL) */
+#define GDN_FLAG_SILU_GATE 0x4u      /* y = rms_norm(o) * w * SiLU(z): the earlier model variant's gate */
+
+/*
+ * gdn_decode_step - one decode call: T tokens applied in order per (sequence, layer).
+ *
+ *   qkv        [B][L][T][10240]  projected q|k|v per token (input)
+ *   z          [B][L][T][6144]   output-gate projection per token (input)
+ *   alpha      [B][L][T][48]     raw alpha per v head (input)
+ *   beta       [B][L][T][48]     raw beta per v head (input)
+ *   dt         [L][48]           ssm_dt bias per layer (input)
+ *   ssm_a      [L][48]           ssm_a per layer, expected < 0 (input)
+ *   conv_w     [L][10240][4]     depthwise conv weight per layer (input)
+ *   ssm_norm   [L][128]          RMSNorm weight per layer, shared by its heads (input)
+ *   conv_state [B][L][10240][3]  rolling conv history (in/out, advanced by T tokens)
+ *   state      [B][L][48][128][128] recurrent state (in/out, advanced by T tokens)
+ *   y          [B][L][T][6144]   gated RMSNorm output per token (output)
+ *   B, L >= 1; 1 <= T <= GDN_MAX_T.
+ *
+ * The state tiles stay on chip across the T tokens and are written back once.
+ */
+gdn_status gdn_decode_step(const float* qkv, const float* z, const float* alpha, const float* beta,
+                           const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                           float* conv_state, float* state, float* y, int B, int L, int T, void* stream);
+
+/*
+ * gdn_decode_step_varlen - gdn_decode_step with a valid length per sequence.
+ *
+ *   seq_len [B] int32 in DEVICE memory (4-byte aligned), or NULL for all T.
+ *
+ * Sequence b applies its first seq_len[b] tokens. Its state and conv_state
+ * end as after those tokens; y rows of tokens at or past seq_len[b] are not
+ * written (they keep whatever the caller put there). Values are clamped to
+ * [0, T]; 0 leaves the sequence untouched. This is the ragged form of the
+ * verify window's commit on the page src/core/verify.cpp.
+ */
+gdn_status gdn_decode_step_varlen(const float* qkv, const float* z, const float* alpha, const float* beta,
+                                  const float* dt, const float* ssm_a, const float* conv_w,
+                                  const float* ssm_norm, float* conv_state, float* state, float* y,
+                                  const int32_t* seq_len, int B, int L, int T, void* stream);
+
+/*
+ * gdn_verify_window - phase 1 of a speculative verify window: y for the T
+ * draft tokens of every sequence, computed from the untouched state, which is
+ * NOT written (Verifier::record_window's recurrence with no commit target, on
+ * the page src/core/verify.cpp). state and conv_state are read only. seq_len
+ * (may be NULL) limits the tokens per sequence as in gdn_decode_step_varlen.
+ */
+gdn_status gdn_verify_window(const float* qkv, const float* z, const float* alpha, const float* beta,
+                             const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                             const float* conv_state, const float* state, float* y, const int32_t* seq_len,
+                             int B, int L, int T, void* stream);
+
+/*
+ * gdn_verify_commit - phase 2: advance state and conv_state by the n_keep[b]
+ * accepted tokens of each sequence, re-running the recurrence from the
+ * untouched state over the same window inputs (the commit graph of
+ * Verifier::commit on the page src/core/verify.cpp). No y is written.
+ *
+ *   n_keep [B] int32 in DEVICE memory; values are clamped to [0, T].
+ */
+gdn_status gdn_verify_commit(const float* qkv, const float* alpha, const float* beta, const float* dt,
+                             const float* ssm_a, const float* conv_w, float* conv_state, float* state,
+                             const int32_t* n_keep, int B, int L, int T, void* stream);
+
+/*
+ * gdn_decode_step_ex - gdn_decode_step_varlen with GDN_FLAG_* bits. With
+ * GDN_FLAG_NO_Y, y and z may be NULL; with GDN_FLAG_NO_STATE_WRITE the state
+ * and conv_state are read only. Unknown bits give GDN_ERR_FLAGS.
+ */
+gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alpha, const float* beta,
+                              const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
+                              float* conv_state, float* state, float* y, const int32_t* seq_len, int B, int L,
+                              int T, uint32_t flags, void* stream);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char* gdn_last_error(void);
+
+/*
+ * The compiled geometry: out[0..7] = head dim, k heads, v heads, conv channels,
+ * value dim, d_conv, max T, CTA threads. Always GDN_OK for a non-NULL out.
+ */
+gdn_status gdn_get_geometry(int32_t out[8]);
+
+/*
+ * Reads and clears the kernel's device error word on the current device,
+ * after synchronising `stream`. 0 means no kernel reported an error; bit 0
+ * means a wait for a state tile gave up after its time limit (the kernel then
+ * stopped early and its outputs are not valid).
+ */
+gdn_status gdn_read_device_error(void* stream, uint32_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

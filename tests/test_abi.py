@@ -1,0 +1,145 @@
+"""The C-ABI library loads, exports every entry point its header declares, and
+rejects bad arguments on the host before anything is launched.
+
+These run on the CPU: the library is built here by nvcc, and every call below
+fails argument checking before any CUDA call. The pointers are fake integers,
+so on a machine with a GPU the calls are skipped rather than risk a launch.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+LIB = os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "libgdn.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from gated_deltanet_linear_step_gb300 import _build
+
+        _build.build()
+    import gated_deltanet_linear_step_gb300 as g
+
+    return g.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
+               "gdn_decode_step_ex", "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    missing = [fn for fn in declared_functions() if fn not in exported]
+    assert not missing, missing
+    for fn in declared_functions():
+        assert hasattr(lib, fn)
+
+
+def test_geometry_matches_pages(lib):
+    import gated_deltanet_linear_step_gb300 as g
+
+    geo = g.gdn_get_geometry()
+    vals = {}
+    with open(os.path.join(ROOT, "tests", "golden", "geometry.txt")) as f:
+        for line in f:
+            if not line.startswith("#") and line.strip():
+                k, v = line.split()[:2]
+                vals[k] = float(v)
+    assert geo["head_dim"] == vals["head_dim"]
+    assert geo["k_heads"] == vals["k_heads"]
+    assert geo["v_heads"] == vals["v_heads"]
+    assert geo["conv_channels"] == vals["conv_channels"]
+    assert geo["d_conv"] == vals["d_conv"]
+    assert geo["value_dim"] == 6144
+
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+
+B, L, T = 2, 3, 4
+SIZES = {  # bytes of each argument of gdn_decode_step for (B, L, T) = (2, 3, 4)
+    "qkv": B * L * T * 10240 * 4, "z": B * L * T * 6144 * 4, "alpha": B * L * T * 48 * 4,
+    "beta": B * L * T * 48 * 4, "dt": L * 48 * 4, "ssm_a": L * 48 * 4, "conv_w": L * 10240 * 16,
+    "ssm_norm": L * 128 * 4, "conv_state": B * L * 10240 * 12, "state": B * L * 48 * 65536, "y": B * L * T * 6144 * 4,
+}
+ORDER = list(SIZES)
+
+
+def fake_ptrs():
+    """Disjoint, 256-aligned fake addresses for every argument."""
+    base, out = 1 << 40, {}
+    for k in ORDER:
+        out[k] = base
+        base += (SIZES[k] + 4095) // 4096 * 4096 + 4096
+    return out
+
+
+def call(lib, p, b=B, l=L, t=T):
+    return lib.gdn_decode_step(*[p[k] for k in ORDER], b, l, t, None)
+
+
+@no_gpu
+def test_null_pointer_rejected(lib):
+    for k in ORDER:
+        p = fake_ptrs()
+        p[k] = None
+        assert call(lib, p) == 1, k
+        assert k in lib.gdn_last_error().decode()
+
+
+@no_gpu
+def test_misaligned_pointer_rejected(lib):
+    for k in ORDER:
+        p = fake_ptrs()
+        p[k] += 4
+        assert call(lib, p) == 3, k
+
+
+@no_gpu
+def test_bad_shapes_rejected(lib):
+    p = fake_ptrs()
+    for b, l, t in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1, 1, 1025), (-1, 2, 2)]:
+        assert call(lib, p, b, l, t) == 2, (b, l, t)
+
+
+@no_gpu
+def test_output_aliasing_rejected(lib):
+    for out in ("y", "state", "conv_state"):
+        for other in ORDER:
+            if other == out:
+                continue
+            p = fake_ptrs()
+            p[out] = p[other] + 16 * ((min(SIZES[other], SIZES[out]) // 2) // 16)
+            assert call(lib, p) == 4, (out, other)
+            assert "overlaps" in lib.gdn_last_error().decode()
+
+
+@no_gpu
+def test_flags_and_window_rules(lib):
+    p = fake_ptrs()
+    args = [p[k] for k in ORDER]
+    assert lib.gdn_decode_step_ex(*args, None, B, L, T, 0x8, None) == 6
+    # the verify window reads the states: y may not overlap them
+    w = dict(p)
+    w["y"] = w["state"]
+    assert lib.gdn_verify_window(*[w[k] for k in ORDER], None, B, L, T, None) == 4
+    # the commit needs n_keep
+    assert lib.gdn_verify_commit(p["qkv"], p["alpha"], p["beta"], p["dt"], p["ssm_a"], p["conv_w"],
+                                 p["conv_state"], p["state"], None, B, L, T, None) == 1
+    # misaligned seq_len
+    assert lib.gdn_decode_step_varlen(*args, (1 << 39) + 2, B, L, T, None) == 3

@@ -1,0 +1,252 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small cases are compared element by element on every output; they span
+several tiles, several 8-token chunks and ragged tails. The five workloads at
+full size run in the launch configuration ``bench.py`` times and are compared
+on sampled (sequence, layer) slices, which the oracle regenerates from the
+seed on its own; conv_state is checked bit-exactly on every slice. Tolerances
+are in ``tests/parity_util.py``: 1e-4 normwise relative on y and on the state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g(cuda_device):
+    import gated_deltanet_linear_step_gb300 as g
+
+    g.load_library()
+    yield g
+    torch.cuda.synchronize()
+    assert g.gdn_read_device_error() == 0
+
+
+SMALL = [
+    ("decode_b1_l1_t1", {}),
+    ("decode_b64_l36_t1", dict(B=3, L=2)),
+    ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=2, L=2)),
+    ("verify_b16_l36_t8_ragged", dict(B=6, L=2)),
+    ("decode_b1_l36_t64_zero_state", dict(L=2)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=2)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=3)),
+    ("decode_b64_l36_t1", dict(B=1, L=2, T=9)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=17)),
+    ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=20)),
+]
+
+
+@pytest.mark.parametrize("name,scale", SMALL, ids=[f"{n}-{s}" for n, s in SMALL])
+def test_small_cases_match_oracle_elementwise(g, name, scale):
+    w = W.WORKLOADS[name].scaled(**scale)
+    h = W.host_inputs(w, threads=8)
+    t = U.to_device(h, torch.device("cuda:0"))
+    y = U.run_step(g, t)
+    torch.cuda.synchronize()
+    ry, rs, rc = U.oracle_full(h)
+    assert U.y_errors(y.cpu().numpy(), ry) <= U.TOL
+    assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
+
+
+def test_silu_gate_variant_matches_oracle(g):
+    w = W.WORKLOADS["verify_b16_l36_t8_ragged"].scaled(B=3, L=2)
+    h = W.host_inputs(w, threads=8)
+    t = U.to_device(h, torch.device("cuda:0"))
+    y = U.run_step(g, t, flags=g.FLAG_SILU_GATE)
+    torch.cuda.synchronize()
+    ry, rs, rc = U.oracle_full(h, gate="silu")
+    assert U.y_errors(y.cpu().numpy(), ry) <= U.TOL
+    assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
+
+
+FULL = {
+    "decode_b1_l1_t1": [(0, 0)],
+    "decode_b1_l36_t64_zero_state": [(0, 0), (0, 17), (0, 35)],
+    "decode_b64_l36_t1": [(0, 0), (63, 35), (31, 17), (5, 30), (40, 1), (17, 22)],
+    "decode_b128_l36_t1_beta_hi_decay_hi": [(0, 0), (127, 35), (64, 18), (3, 33), (99, 7)],
+    "verify_b16_l36_t8_ragged": "by_length",
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workloads_on_sampled_slices(g, name):
+    w = W.WORKLOADS[name]
+    dev = torch.device("cuda:0")
+    t = W.device_inputs(w, dev, threads=16)
+    cs_before = t["conv_state"].cpu().numpy()
+    qkv = t["qkv"].cpu().numpy()
+    y = torch.full(t["z"].shape, float("nan"), device=dev)
+    U.run_step(g, t, y=y)
+    torch.cuda.synchronize()
+    lens = W.seq_lens(w)
+    samples = FULL[name]
+    if samples == "by_length":
+        # one sequence per distinct length, at two layers each
+        firsts = {int(n): b for b, n in reversed(list(enumerate(lens)))}
+        samples = [(b, l) for b in sorted(firsts.values()) for l in (0, 29)]
+    for b, l in samples:
+        ry, rs, rc = U.oracle_slice(w, b, l)
+        assert U.y_errors(y[b, l].cpu().numpy(), ry) <= U.TOL, (b, l)
+        assert U.state_errors(t["state"][b, l].cpu().numpy(), rs) <= U.TOL, (b, l)
+        assert np.array_equal(t["conv_state"][b, l].cpu().numpy(), rc), (b, l)
+    # every slice: conv_state is the last three inputs of [old history, valid tokens]
+    cs = t["conv_state"].cpu().numpy()
+    for b in range(w.B):
+        n = w.T if lens is None else int(lens[b])
+        hist = np.concatenate([cs_before[b], np.moveaxis(qkv[b, :, :n], 1, 2)], axis=2)
+        assert np.array_equal(cs[b], hist[..., -3:]), b
+    assert torch.isfinite(t["state"]).all()
+
+
+def _small(scale=dict(B=3, L=2, T=9), name="verify_b16_l36_t8_ragged"):
+    w = W.WORKLOADS[name].scaled(**scale)
+    return w, W.host_inputs(w, threads=8)
+
+
+def test_t_tokens_in_one_call_equal_t_single_calls_bitwise(g):
+    w, h = _small(name="decode_b64_l36_t1")
+    dev = torch.device("cuda:0")
+    a = U.to_device(h, dev)
+    ya = U.run_step(g, a)
+    b = U.to_device(h, dev)
+    ys = []
+    for tt in range(w.T):
+        one = dict(b)
+        for k in ("qkv", "z", "alpha", "beta"):
+            one[k] = b[k][:, :, tt:tt + 1].contiguous()
+        ys.append(U.run_step(g, one))
+    torch.cuda.synchronize()
+    assert torch.equal(ya, torch.cat(ys, dim=2))
+    assert torch.equal(a["state"], b["state"]) and torch.equal(a["conv_state"], b["conv_state"])
+
+
+def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g):
+    w, h = _small()
+    dev = torch.device("cuda:0")
+    lens = torch.tensor([0, 3, 9], dtype=torch.int32, device=dev)
+    a = U.to_device(h, dev)
+    a["seq_len"] = lens
+    sentinel = torch.full(a["z"].shape, 12345.0, device=dev)
+    ya = U.run_step(g, a, y=sentinel.clone())
+    torch.cuda.synchronize()
+    # sequence 0: nothing written
+    assert torch.equal(ya[0], sentinel[0])
+    assert torch.equal(a["state"][0], torch.from_numpy(h["state"][0]).to(dev))
+    assert torch.equal(a["conv_state"][0], torch.from_numpy(h["conv_state"][0]).to(dev))
+    # sequence 1: the prefix call with T = 3
+    p = U.to_device(h, dev)
+    p = {k: (v[1:2] if v is not None and k not in ("dt", "ssm_a", "conv_w", "ssm_norm") else v) for k, v in p.items()}
+    for k in ("qkv", "z", "alpha", "beta"):
+        p[k] = p[k][:, :, :3].contiguous()
+    p["seq_len"] = None
+    yp = U.run_step(g, p)
+    torch.cuda.synchronize()
+    assert torch.equal(ya[1, :, :3], yp[0]) and torch.equal(ya[1, :, 3:], sentinel[1, :, 3:])
+    assert torch.equal(a["state"][1], p["state"][0]) and torch.equal(a["conv_state"][1], p["conv_state"][0])
+    # lengths past T are clamped to T
+    c = U.to_device(h, dev)
+    c["seq_len"] = torch.tensor([100, 9, 9], dtype=torch.int32, device=dev)
+    yc = U.run_step(g, c)
+    full = U.to_device(h, dev)
+    yf = U.run_step(g, full, seq_len=None)
+    torch.cuda.synchronize()
+    assert torch.equal(yc, yf) and torch.equal(c["state"], full["state"])
+    assert torch.equal(yc[2], ya[2]) and torch.equal(c["state"][2], a["state"][2])
+
+
+def test_deterministic_and_batch_permutation_equivariant(g):
+    w, h = _small(dict(B=4, L=2, T=3), name="decode_b64_l36_t1")
+    dev = torch.device("cuda:0")
+    a = U.to_device(h, dev)
+    ya = U.run_step(g, a)
+    b = U.to_device(h, dev)
+    yb = U.run_step(g, b)
+    perm = [2, 0, 3, 1]
+    hp = {k: (v[perm] if v is not None and v.shape[0] == 4 and k not in ("dt", "ssm_a", "conv_w", "ssm_norm")
+              else v) for k, v in h.items()}
+    c = U.to_device(hp, dev)
+    yc = U.run_step(g, c)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb) and torch.equal(a["state"], b["state"])
+    assert torch.equal(yc, ya[perm]) and torch.equal(c["state"], a["state"][perm])
+    assert torch.equal(c["conv_state"], a["conv_state"][perm])
+
+
+def test_verify_window_then_commit(g):
+    w, h = _small(dict(B=3, L=2, T=6))
+    dev = torch.device("cuda:0")
+    win = U.to_device(h, dev)
+    y = torch.full(win["z"].shape, float("nan"), device=dev)
+    g.gdn_verify_window(win["qkv"], win["z"], win["alpha"], win["beta"], win["dt"], win["ssm_a"], win["conv_w"],
+                        win["ssm_norm"], win["conv_state"], win["state"], y)
+    ref = U.to_device(h, dev)
+    yref = U.run_step(g, ref, seq_len=None)
+    torch.cuda.synchronize()
+    # phase 1: the same y as a full decode, with both states untouched
+    assert torch.equal(y, yref)
+    assert torch.equal(win["state"], torch.from_numpy(h["state"]).to(dev))
+    assert torch.equal(win["conv_state"], torch.from_numpy(h["conv_state"]).to(dev))
+    # phase 2: keep 2, 6 and 0 tokens
+    n_keep = torch.tensor([2, 6, 0], dtype=torch.int32, device=dev)
+    g.gdn_verify_commit(win["qkv"], win["alpha"], win["beta"], win["dt"], win["ssm_a"], win["conv_w"],
+                        win["conv_state"], win["state"], n_keep)
+    exp = U.to_device(h, dev)
+    U.run_step(g, exp, seq_len=n_keep)
+    torch.cuda.synchronize()
+    assert torch.equal(win["state"], exp["state"]) and torch.equal(win["conv_state"], exp["conv_state"])
+    _, rs, rc = U.oracle_full(dict(h, seq_len=n_keep.cpu().numpy()))
+    assert U.state_errors(win["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(win["conv_state"].cpu().numpy(), rc)
+
+
+def test_outputs_have_untouched_guard_regions(g):
+    w, h = _small(dict(B=1, L=1, T=3), name="decode_b64_l36_t1")
+    dev = torch.device("cuda:0")
+    t = U.to_device(h, dev)
+    pad = 64  # floats = 256 bytes on each side
+    bufs = {}
+    for k in ("state", "conv_state"):
+        n = t[k].numel()
+        big = torch.full((n + 2 * pad,), float("nan"), device=dev)
+        big[pad:pad + n] = t[k].reshape(-1)
+        bufs[k] = big
+        t[k] = big[pad:pad + n].view(t[k].shape)
+    ny = t["z"].numel()
+    ybig = torch.full((ny + 2 * pad,), float("nan"), device=dev)
+    y = ybig[pad:pad + ny].view(t["z"].shape)
+    U.run_step(g, t, y=y)
+    torch.cuda.synchronize()
+    for big in list(bufs.values()) + [ybig]:
+        assert torch.isnan(big[:pad]).all() and torch.isnan(big[-pad:]).all()
+    assert torch.isfinite(y).all()
+
+
+def test_bad_arguments_raise_and_launch_nothing(g):
+    w, h = _small(dict(B=1, L=1, T=2), name="decode_b64_l36_t1")
+    dev = torch.device("cuda:0")
+    t = U.to_device(h, dev)
+    before = t["state"].clone()
+    y = torch.zeros(t["z"].shape, device=dev)
+    args = [t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"],
+            t["conv_state"], t["state"], y]
+    lib = g.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    ptrs = [a.data_ptr() for a in args]
+    # misaligned state pointer, y aliasing state, y aliasing qkv, null conv_state
+    for i, val, code in [(9, ptrs[9] + 4, 3), (10, ptrs[9], 4), (10, ptrs[0], 4), (8, None, 1)]:
+        p = list(ptrs)
+        p[i] = val
+        assert lib.gdn_decode_step(*p, 1, 1, 2, stream) == code
+    with pytest.raises(g.GdnError):
+        g.gdn_decode_step_ex(*args, flags=0x100)
+    with pytest.raises(ValueError):
+        g.gdn_decode_step(*args[:10], torch.zeros(1, 1, 3, 6144, device=dev))
+    torch.cuda.synchronize()
+    assert torch.equal(t["state"], before) and torch.all(y == 0)
