@@ -52,10 +52,12 @@ KERNEL_SOURCE = os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", "
 def parse():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="sequences per GPU (default: the workload's B); smaller values are for profiling")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -156,58 +158,89 @@ def committed_traffic():
 
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples SM clocks, power and throttle reasons with nvidia-smi around the timed region.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    A reader thread stamps each sample with the host clock on arrival, and
+    ``summary`` keeps the samples that fall inside [mark_start, mark_end].
+    """
 
-    def __init__(self, index: int):
-        self.index = index
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device):
+        self.device = device
         self.proc = None
-        self.path = os.path.join("/tmp", f"gdn_clocks_{os.getpid()}.csv")
+        self.samples = []
+        self.t0 = self.t1 = None
+
+    def _gpu_id(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.device).uuid)
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:  # noqa: BLE001 - older torch: fall back to the visible index
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            ids = [v for v in vis.split(",") if v.strip()]
+            return ids[self.device.index] if self.device.index < len(ids) else str(self.device.index)
 
     def __enter__(self):
+        import threading
+
         try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self._gpu_id()}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.samples.append((time.time(), line))
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.2)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            self.fh.close()
+            self.thread.join(timeout=2)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        for line in open(self.path):
+        for ts, line in self.samples:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-            except ValueError:
+                rows.append((ts, float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
+            except (ValueError, IndexError):
                 continue
-        os.remove(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
-        loaded = [r[0] for r in rows]
-        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1 + 0.05]
+        note = None
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: abs(r[0] - (self.t0 or r[0])))[:2]
+            note = "timed region shorter than the 50 ms sampling period; nearest samples"
+        reasons = sorted({self.NAMES[i] for r in inside for i, v in enumerate(r[4]) if v.lower() == "active"})
+        out = {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+               "power_w_max": max(r[3] for r in inside), "samples": len(inside), "reasons": reasons}
+        if note:
+            out["note"] = note
+        return out
 
 
 # ----------------------------------------------------------- cpu legs ----
@@ -269,7 +302,7 @@ def run_gdn(args, w_global, world, rank, local):
     g.load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    per_rank = W.WORKLOADS[args.workload].B
+    per_rank = args.batch if args.batch is not None else W.WORKLOADS[args.workload].B
     rows = shard_rows(rank, per_rank)
     w = w_global.scaled(B=per_rank) if world > 1 else w_global
     t = W.device_inputs(w_global, dev, threads=16, batch_rows=rows)
@@ -293,7 +326,8 @@ def run_gdn(args, w_global, world, rank, local):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
+        clocks.mark_start()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -303,6 +337,7 @@ def run_gdn(args, w_global, world, rank, local):
             e.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clocks.mark_end()
     barrier(world)
     elapsed_ms = t_start.elapsed_time(t_end)
     launch_ms = [s.elapsed_time(e) for s, e in ev]
@@ -383,6 +418,8 @@ def main():
     if args.gpus != world and world > 1:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     base = W.WORKLOADS[args.workload]
+    if args.batch is not None:
+        base = base.scaled(B=args.batch, name=f"{base.name}_b{args.batch}")
     w_global = base.scaled(B=base.B * world) if world > 1 else base
     if args.impl == "reference":
         run_reference(args, base, world, rank)
