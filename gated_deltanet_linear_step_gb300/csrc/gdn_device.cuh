@@ -1,0 +1,294 @@
+// gdn_device.cuh - device-side pieces shared by the decode-step kernels:
+// inline PTX for mbarriers and bulk async copies, bounded waits, warp
+// reductions, the scalar activations of the GDN step, and the register-tile
+// form of the gated delta rule.
+#pragma once
+
+#include <cstdint>
+
+#include "gdn_launch.h"
+
+namespace gdn {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
+constexpr uint32_t kErrWaitTimeout = 1u;
+constexpr float kEps = 1e-6f;                    // RMS epsilon of both norms
+constexpr float kQScale = 0.08838834764831845f;  // 1/sqrt(128)
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for phase `parity` of the mbarrier, giving up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later
+// bulk async (async-proxy) accesses to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// An L2 policy that marks lines as first to evict: state tiles are touched once per call.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// One contiguous global -> shared bulk copy (16-byte aligned addresses, size a
+// multiple of 16); completion is signalled on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// bulk_load with the evict-first L2 policy, for data read once per call.
+__device__ __forceinline__ void bulk_load_stream(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(evict_first_policy())
+        : "memory");
+}
+
+// Pulls [src, src + bytes) into L2 without waiting (16-byte aligned, 16-byte multiple).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Keeps the compiler from hoisting every shared-memory load of a long unrolled
+// loop ahead of its FMAs while a whole state block is held in registers.
+__device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
+
+// Global conv channel of the unit's channel slot cc (k head g): q of head g at
+// slots [0,128), k at [128,256), v of heads 3g..3g+2 at [256,640).
+__device__ __forceinline__ int unit_channel(int cc, int g) {
+    return cc < kHeadDim ? g * kHeadDim + cc
+                         : (cc < 2 * kHeadDim ? kKOffset + g * kHeadDim + (cc - kHeadDim)
+                                              : kVOffset + g * kGroup * kHeadDim + (cc - 2 * kHeadDim));
+}
+
+// Conv output of one channel: taps 0-2 on the history (oldest first), tap 3 on x.
+__device__ __forceinline__ float conv4(float4 w, float h0, float h1, float h2, float x) {
+    float xc = w.x * h0;
+    xc = fmaf(w.y, h1, xc);
+    xc = fmaf(w.z, h2, xc);
+    return fmaf(w.w, x, xc);
+}
+
+// beta and decay of one v head from the raw projections and the layer's dt, ssm_a.
+__device__ __forceinline__ void head_gates(float alpha_raw, float beta_raw, float dt, float ssm_a, float& beta,
+                                           float& decay) {
+    beta = sigmoidf_(beta_raw);
+    decay = expf(softplusf_(alpha_raw + dt) * ssm_a);
+}
+
+// In place, by one warp: q <- q / sqrt(|q|^2 + eps) / sqrt(128) and
+// k <- k / sqrt(|k|^2 + eps), 128 floats each, 16-byte aligned.
+__device__ __forceinline__ void normalize_qk(float* qv, float* kv, int lane) {
+    float4 q4 = *reinterpret_cast<float4*>(qv + lane * 4);
+    float4 k4 = *reinterpret_cast<float4*>(kv + lane * 4);
+    const float sq = warp_sum(q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w);
+    const float sk = warp_sum(k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w);
+    const float rq = rsqrtf(sq + kEps) * kQScale;
+    const float rk = rsqrtf(sk + kEps);
+    q4.x *= rq;
+    q4.y *= rq;
+    q4.z *= rq;
+    q4.w *= rq;
+    k4.x *= rk;
+    k4.y *= rk;
+    k4.z *= rk;
+    k4.w *= rk;
+    *reinterpret_cast<float4*>(qv + lane * 4) = q4;
+    *reinterpret_cast<float4*>(kv + lane * 4) = k4;
+}
+
+// y for one head's 128 values (4 per lane): rms_norm(o) * w * gate(z).
+__device__ __forceinline__ float4 gated_rms_norm4(float4 o4, float4 z4, float4 w4, bool silu_gate) {
+    const float ss = warp_sum(o4.x * o4.x + o4.y * o4.y + o4.z * o4.z + o4.w * o4.w);
+    const float rr = rsqrtf(ss * (1.0f / kHeadDim) + kEps);
+    float4 y;
+    if (silu_gate) {
+        y.x = o4.x * rr * w4.x * siluf_(z4.x);
+        y.y = o4.y * rr * w4.y * siluf_(z4.y);
+        y.z = o4.z * rr * w4.z * siluf_(z4.z);
+        y.w = o4.w * rr * w4.w * siluf_(z4.w);
+    } else {
+        y.x = o4.x * rr * w4.x * sigmoidf_(z4.x);
+        y.y = o4.y * rr * w4.y * sigmoidf_(z4.y);
+        y.z = o4.z * rr * w4.z * sigmoidf_(z4.z);
+        y.w = o4.w * rr * w4.w * sigmoidf_(z4.w);
+    }
+    return y;
+}
+
+// ------------------------------------------------------------------------
+// The state tile in registers ("quad" mapping). A tile group of 128 threads
+// (4 warps) owns one 128x128 tile. Lane 8 rb + qd of warp wg in the group holds
+// rows [32 rb, 32 rb + 32) of the four columns [32 wg + 4 qd, +4): 128 fp32
+// values, s[4 r + c] = S[32 rb + r][32 wg + 4 qd + c]. A warp's 128-bit shared
+// loads and global stores then cover four full 128-byte row segments without
+// bank conflicts, and a column reduction is 32 in-thread FMAs plus two warp
+// shuffles across rb.
+// ------------------------------------------------------------------------
+struct Quad {
+    int row0;  // first row held
+    int col0;  // first of the four columns held
+    int rb;    // row block (0..3): lane bits 3-4
+};
+
+__device__ __forceinline__ Quad quad_of(int tid_in_group) {
+    const int lane = tid_in_group & 31;
+    Quad q;
+    q.rb = lane >> 3;
+    q.row0 = 32 * q.rb;
+    q.col0 = 32 * (tid_in_group >> 5) + 4 * (lane & 7);
+    return q;
+}
+
+// Shared memory (row-major 128x128 fp32 tile) -> registers.
+__device__ __forceinline__ void tile_load_quad(float (&s)[128], const float* tile, const Quad& q) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float4 v = *reinterpret_cast<const float4*>(tile + (q.row0 + r) * kHeadDim + q.col0);
+        s[4 * r + 0] = v.x;
+        s[4 * r + 1] = v.y;
+        s[4 * r + 2] = v.z;
+        s[4 * r + 3] = v.w;
+    }
+}
+
+// Registers -> global with streaming stores (the tile is not read again by this call).
+__device__ __forceinline__ void tile_store_quad(const float (&s)[128], float* tile, const Quad& q) {
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+        __stcs(reinterpret_cast<float4*>(tile + (q.row0 + r) * kHeadDim + q.col0),
+               make_float4(s[4 * r + 0], s[4 * r + 1], s[4 * r + 2], s[4 * r + 3]));
+}
+
+// One gated delta-rule step on the thread's 32x4 block of a tile. `qv` and
+// `kv` point at the normalised q (already scaled) and k of the tile's k head in
+// shared memory; v4 holds v of the four columns. Returns o of the four
+// columns. Two passes over the registers (the four lanes of a row-block group
+// compute the same d and o):
+//   pass 1:  a_c = sum_i S[i][c] k[i];  d_c = beta (v_c - decay a_c)        (kv = (decay S)^T k)
+//   pass 2:  S[i][c] <- decay S[i][c] + k[i] d_c;  o_c = sum_i S[i][c] q[i]  (S += k d^T; o = S^T q)
+// With `out` non-null, pass 2 also streams each updated row to `out` (the
+// tile's place in global memory) as soon as it is computed, so the stores
+// drain while the rest of the pass runs.
+__device__ __forceinline__ float4 delta_step_quad(float (&s)[128], const float* qv, const float* kv, const Quad& q,
+                                                  float4 v4, float beta, float decay, float* out = nullptr) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            a0 = fmaf(s[i + 0], kk[e], a0);
+            a1 = fmaf(s[i + 1], kk[e], a1);
+            a2 = fmaf(s[i + 2], kk[e], a2);
+            a3 = fmaf(s[i + 3], kk[e], a3);
+        }
+    }
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
+        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
+    }
+    const float d0 = beta * (v4.x - decay * a0);
+    const float d1 = beta * (v4.y - decay * a1);
+    const float d2 = beta * (v4.z - decay * a2);
+    const float d3 = beta * (v4.w - decay * a3);
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 32; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float4 q4 = *reinterpret_cast<const float4*>(qv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            s[i + 0] = fmaf(kk[e], d0, decay * s[i + 0]);
+            s[i + 1] = fmaf(kk[e], d1, decay * s[i + 1]);
+            s[i + 2] = fmaf(kk[e], d2, decay * s[i + 2]);
+            s[i + 3] = fmaf(kk[e], d3, decay * s[i + 3]);
+            o0 = fmaf(s[i + 0], qq[e], o0);
+            o1 = fmaf(s[i + 1], qq[e], o1);
+            o2 = fmaf(s[i + 2], qq[e], o2);
+            o3 = fmaf(s[i + 3], qq[e], o3);
+            if (out != nullptr)
+                __stcs(reinterpret_cast<float4*>(out + (q.row0 + r + e) * kHeadDim + q.col0),
+                       make_float4(s[i + 0], s[i + 1], s[i + 2], s[i + 3]));
+        }
+        if ((r & 7) == 4) compiler_fence();
+    }
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {
+        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
+    }
+    return make_float4(o0, o1, o2, o3);
+}
+
+}  // namespace gdn

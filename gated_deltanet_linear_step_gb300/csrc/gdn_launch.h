@@ -43,10 +43,17 @@ struct StepArgs {
     uint32_t flags;
 };
 
-// Launches the fused decode-step kernel on `stream`. Returns the launch status.
+// Launches the fused decode step on `stream`: the single-token kernel when
+// T == 1, the multi-token kernel otherwise. Returns the launch status.
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream);
 
-// Synchronises `stream`, then reads and clears the device error word.
+// The single-token kernel (gdn_decode_t1.cu); requires a.T == 1.
+cudaError_t launch_decode_t1(const StepArgs& a, cudaStream_t stream);
+
+// Reads and clears the single-token kernel's device error word.
+cudaError_t read_t1_error(uint32_t* out);
+
+// Synchronises `stream`, then reads and clears the device error words of both kernels.
 cudaError_t read_device_error(cudaStream_t stream, uint32_t* out);
 
 }  // namespace gdn
