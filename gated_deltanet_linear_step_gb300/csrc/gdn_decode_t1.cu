@@ -16,10 +16,15 @@
 //   - each unit's small inputs (conv history, q|k|v slice, alpha and beta
 //     rows, z slice: 12,160 bytes) two units ahead (two slots),
 //   - the layer weights of an (l, g) run (conv taps, dt, ssm_a, ssm_norm).
-// * Conv, SiLU, norms and gates then read and write shared memory only; each
-//   tile moves to registers in the quad mapping (gdn_device.cuh) and its rows
-//   stream back to HBM with 128-bit stores as the update produces them; o
-//   overwrites v in place and y leaves with 128-bit stores.
+// * Conv, SiLU, norms and gates then read and write shared memory only.
+// * Each tile stays in its shared-memory slot: the group's threads (32x4
+//   blocks, the quad mapping of gdn_device.cuh) reduce it, update it in place
+//   and accumulate o, then one bulk async store writes it back. The stores
+//   drain through the copy engine while the warps go on to y and the next
+//   unit; plain per-thread stores of 192 KB per unit would instead clog each
+//   SM's memory-instruction path and stall everything behind them. The slot
+//   is refilled with the next unit's tile once the store has read it.
+// * o overwrites v in the staging slot; y leaves with 128-bit stores.
 
 #include <mutex>
 
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
     const bool write_state = (p.flags & kNoStateWrite) == 0;
     const bool write_y = (p.flags & kNoY) == 0;
     const bool silu_gate = (p.flags & kSiluGate) != 0;
-    const float* my_tile = tiles + hh * kTile;
+    float* my_tile = tiles + hh * kTile;
     const uint32_t my_tile_s = smem_addr(my_tile);
     const uint32_t my_bar = smem_addr(&bars[kBarTile + hh]);
 
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
     uint32_t tile_par = 0, stage_par = 0, wt_par = 0;
     bool wt_pending = true;
     bool failed = false;
-    float s[128];
+    bool store_pending = false;  // a bulk store of this group's tile has not yet been waited for
 
     for (long long u = u_begin; u < u_end; ++u) {
         const int slot = static_cast<int>((u - u_begin) & 1);
@@ -264,26 +269,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
         if (n > 0 && warp == 0) normalize_qk(S + kStX, S + kStX + kS, lane);
         __syncthreads();
 
-        // ---- this unit's tile into registers; its slot takes the next unit's tile
+        // ---- this unit's tile
         if (!mbar_wait_bounded(my_bar, tile_par)) failed = true;
         tile_par ^= 1u;
-        if (n > 0) tile_load_quad(s, my_tile, q);
-        named_barrier(1 + hh, kS);
-        if (group_leader && has_next) {
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(my_bar, kTileBytes);
-            bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
-        }
 
-        // ---- the gated delta rule, rows streamed out as updated; o replaces v
+        // ---- the gated delta rule on the tile in its slot; o replaces v
         if (n > 0) {
             float* vo = S + kStX + 2 * kS + hh * kS + q.col0;
             const float4 v4 = *reinterpret_cast<const float4*>(vo);
-            float* out = write_state ? p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile
-                                     : nullptr;
-            const float4 o4 = delta_step_quad(s, S + kStX, S + kStX + kS, q, v4, gates[hh], gates[kGroup + hh], out);
+            const float4 o4 = delta_step_smem(my_tile, S + kStX, S + kStX + kS, q, v4, gates[hh], gates[kGroup + hh]);
             __syncwarp();
             if (q.rb == 0) *reinterpret_cast<float4*>(vo) = o4;
+            fence_proxy_async_smem();  // the updated tile is read next by the bulk store
+        }
+        named_barrier(1 + hh, kS);
+        if (group_leader && n > 0 && write_state) {
+            bulk_store(p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile, my_tile_s,
+                       kTileBytes);
+            bulk_commit();
+            store_pending = true;
         }
         __syncthreads();
 
@@ -304,8 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
                 if (has_next)
                     (void)mbar_wait_bounded(smem_addr(&bars[kBarStage + (slot ^ 1)]), (stage_par >> (slot ^ 1)) & 1u);
             }
-            if (has_next) (void)mbar_wait_bounded(my_bar, tile_par);
+            if (group_leader) bulk_wait_all();
             return;
+        }
+        // The tile slot takes the next unit's tile once the store has read it.
+        if (group_leader && has_next) {
+            if (store_pending) bulk_wait_read();
+            store_pending = false;
+            mbar_arrive_expect_tx(my_bar, kTileBytes);
+            bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
         }
         // The staging slot is free again: bring in the unit after next.
         if (warp == 0 && u + 2 < u_end) {
@@ -313,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
             issue_stage(p, next_unit(p, xn), smem_addr(S), smem_addr(&bars[kBarStage + slot]), lane);
         }
     }
+    if (group_leader) bulk_wait_all();  // the last stores must finish reading shared memory before exit
 }
 
 std::mutex g_mutex;

@@ -90,6 +90,21 @@ __device__ __forceinline__ void bulk_load_stream(uint32_t dst, const void* src, 
         : "memory");
 }
 
+// One contiguous shared -> global bulk copy, tracked by this thread's bulk
+// async-group (commit with bulk_commit, wait with bulk_wait_read / bulk_wait_all).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until every committed bulk store of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Pulls [src, src + bytes) into L2 without waiting (16-byte aligned, 16-byte multiple).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -280,6 +295,60 @@ __device__ __forceinline__ float4 delta_step_quad(float (&s)[128], const float* 
                        make_float4(s[i + 0], s[i + 1], s[i + 2], s[i + 3]));
         }
         if ((r & 7) == 4) compiler_fence();
+    }
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {
+        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
+    }
+    return make_float4(o0, o1, o2, o3);
+}
+
+// The same step on a tile that stays in shared memory (row-major 128x128):
+// pass 1 reads the thread's 32x4 block for a = S^T k; pass 2 reads it again,
+// writes the updated block back in place and accumulates o = S_new^T q. Every
+// sum runs in the same order as delta_step_quad, so both give identical bits.
+__device__ __forceinline__ float4 delta_step_smem(float* tile, const float* qv, const float* kv, const Quad& q,
+                                                  float4 v4, float beta, float decay) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+        const float4 sv = *reinterpret_cast<const float4*>(tile + (q.row0 + r) * kHeadDim + q.col0);
+        const float k = kv[q.row0 + r];
+        a0 = fmaf(sv.x, k, a0);
+        a1 = fmaf(sv.y, k, a1);
+        a2 = fmaf(sv.z, k, a2);
+        a3 = fmaf(sv.w, k, a3);
+    }
+#pragma unroll
+    for (int m = 8; m <= 16; m <<= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
+        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
+    }
+    const float d0 = beta * (v4.x - decay * a0);
+    const float d1 = beta * (v4.y - decay * a1);
+    const float d2 = beta * (v4.z - decay * a2);
+    const float d3 = beta * (v4.w - decay * a3);
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+        float4* row = reinterpret_cast<float4*>(tile + (q.row0 + r) * kHeadDim + q.col0);
+        float4 sv = *row;
+        const float k = kv[q.row0 + r];
+        const float qq = qv[q.row0 + r];
+        sv.x = fmaf(k, d0, decay * sv.x);
+        sv.y = fmaf(k, d1, decay * sv.y);
+        sv.z = fmaf(k, d2, decay * sv.z);
+        sv.w = fmaf(k, d3, decay * sv.w);
+        *row = sv;
+        o0 = fmaf(sv.x, qq, o0);
+        o1 = fmaf(sv.y, qq, o1);
+        o2 = fmaf(sv.z, qq, o2);
+        o3 = fmaf(sv.w, qq, o3);
     }
 #pragma unroll
     for (int m = 8; m <= 16; m <<= 1) {
