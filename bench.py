@@ -45,7 +45,8 @@ DEFAULT_WORKLOAD = "decode_b64_l36_t1"
 METRIC = "GDN state-updates/sec (seq*layer*token) and achieved HBM GB/s vs GB300 peak"
 UNIT = "state-updates/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_decode_step_kernel_traffic.txt")
-KERNEL_SOURCE = os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")
+KERNEL_SOURCES = [os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", f)
+                  for f in ("gdn_decode_t1.cu", "gdn_device.cuh")]
 
 
 # ------------------------------------------------------------------ args --
@@ -143,17 +144,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def committed_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel source."""
+def committed_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel source and workload."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     text = open(TRAFFIC_FILE).read()
+    wm = re.search(r"workload:\s*(\S+)", text)
+    if not wm or wm.group(1) != workload:
+        return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
-    return float(m.group(1)) if h.group(1) == src else None
+    digest = hashlib.sha256()
+    for path in KERNEL_SOURCES:
+        digest.update(open(path, "rb").read())
+    return float(m.group(1)) if h.group(1) == digest.hexdigest() else None
 
 
 # --------------------------------------------------------------- clocks --
@@ -384,7 +390,7 @@ def run_gdn(args, w_global, world, rank, local):
     peak, peak_kind = measured_peaks()
     achieved = bytes_alg["total"] / mean_launch_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": committed_traffic(), "peak_kind": peak_kind,
+                "traffic": committed_traffic(w_global.name) if world == 1 else None, "peak_kind": peak_kind,
                 "state_only_gbs": bytes_alg["state"] / mean_launch_s / 1e9,
                 "algorithmic_bytes_per_launch": bytes_alg["total"]}
 
