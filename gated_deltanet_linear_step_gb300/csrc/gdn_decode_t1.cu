@@ -2,7 +2,7 @@
 // hot path, where every (sequence, layer) state is read and written once per
 // call and the step is bound by HBM bandwidth.
 //
-// Same arithmetic, in the same order, as the multi-token kernel (the operation
+// Same arithmetic as the multi-token kernel (the operation
 // order of the header comment of Winery-Strata include/strata/core/layer.hpp,
 // composed by gdn_layer steps 3-7 on src/core/layer.cpp), organised so that
 // nothing on a unit's critical path waits on global memory:

@@ -1,7 +1,7 @@
 // gdn_device.cuh - device-side pieces shared by the decode-step kernels:
-// inline PTX for mbarriers and bulk async copies, bounded waits, warp
-// reductions, the scalar activations of the GDN step, and the register-tile
-// form of the gated delta rule.
+// inline PTX for mbarriers, bulk async copies and clusters, bounded waits,
+// warp reductions, the scalar activations of the GDN step, and the two forms of
+// the gated delta rule (tile in shared memory, tile in registers).
 #pragma once
 
 #include <cstdint>
@@ -114,10 +114,6 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// Keeps the compiler from hoisting every shared-memory load of a long unrolled
-// loop ahead of its FMAs while a whole state block is held in registers.
-__device__ __forceinline__ void compiler_fence() { asm volatile("" ::: "memory"); }
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
@@ -192,13 +188,11 @@ __device__ __forceinline__ float4 gated_rms_norm4(float4 o4, float4 z4, float4 w
 }
 
 // ------------------------------------------------------------------------
-// The state tile in registers ("quad" mapping). A tile group of 128 threads
-// (4 warps) owns one 128x128 tile. Lane 8 rb + qd of warp wg in the group holds
-// rows [32 rb, 32 rb + 32) of the four columns [32 wg + 4 qd, +4): 128 fp32
-// values, s[4 r + c] = S[32 rb + r][32 wg + 4 qd + c]. A warp's 128-bit shared
-// loads and global stores then cover four full 128-byte row segments without
-// bank conflicts, and a column reduction is 32 in-thread FMAs plus two warp
-// shuffles across rb.
+// The "quad" mapping of a 128x128 tile onto a 128-thread group (4 warps):
+// lane 8 rb + qd of warp wg handles rows [32 rb, 32 rb + 32) of the four
+// columns [32 wg + 4 qd, +4). A warp's 128-bit shared accesses then cover four
+// full 128-byte row segments without bank conflicts, and a column reduction
+// is 32 in-thread FMAs plus two warp shuffles across rb.
 // ------------------------------------------------------------------------
 struct Quad {
     int row0;  // first row held
@@ -215,101 +209,13 @@ __device__ __forceinline__ Quad quad_of(int tid_in_group) {
     return q;
 }
 
-// Shared memory (row-major 128x128 fp32 tile) -> registers.
-__device__ __forceinline__ void tile_load_quad(float (&s)[128], const float* tile, const Quad& q) {
-#pragma unroll
-    for (int r = 0; r < 32; ++r) {
-        const float4 v = *reinterpret_cast<const float4*>(tile + (q.row0 + r) * kHeadDim + q.col0);
-        s[4 * r + 0] = v.x;
-        s[4 * r + 1] = v.y;
-        s[4 * r + 2] = v.z;
-        s[4 * r + 3] = v.w;
-    }
-}
-
-// Registers -> global with streaming stores (the tile is not read again by this call).
-__device__ __forceinline__ void tile_store_quad(const float (&s)[128], float* tile, const Quad& q) {
-#pragma unroll
-    for (int r = 0; r < 32; ++r)
-        __stcs(reinterpret_cast<float4*>(tile + (q.row0 + r) * kHeadDim + q.col0),
-               make_float4(s[4 * r + 0], s[4 * r + 1], s[4 * r + 2], s[4 * r + 3]));
-}
-
-// One gated delta-rule step on the thread's 32x4 block of a tile. `qv` and
-// `kv` point at the normalised q (already scaled) and k of the tile's k head in
-// shared memory; v4 holds v of the four columns. Returns o of the four
-// columns. Two passes over the registers (the four lanes of a row-block group
-// compute the same d and o):
-//   pass 1:  a_c = sum_i S[i][c] k[i];  d_c = beta (v_c - decay a_c)        (kv = (decay S)^T k)
-//   pass 2:  S[i][c] <- decay S[i][c] + k[i] d_c;  o_c = sum_i S[i][c] q[i]  (S += k d^T; o = S^T q)
-// With `out` non-null, pass 2 also streams each updated row to `out` (the
-// tile's place in global memory) as soon as it is computed, so the stores
-// drain while the rest of the pass runs.
-__device__ __forceinline__ float4 delta_step_quad(float (&s)[128], const float* qv, const float* kv, const Quad& q,
-                                                  float4 v4, float beta, float decay, float* out = nullptr) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int r = 0; r < 32; r += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 4 * (r + e);
-            a0 = fmaf(s[i + 0], kk[e], a0);
-            a1 = fmaf(s[i + 1], kk[e], a1);
-            a2 = fmaf(s[i + 2], kk[e], a2);
-            a3 = fmaf(s[i + 3], kk[e], a3);
-        }
-    }
-#pragma unroll
-    for (int m = 8; m <= 16; m <<= 1) {
-        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
-        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
-        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
-    }
-    const float d0 = beta * (v4.x - decay * a0);
-    const float d1 = beta * (v4.y - decay * a1);
-    const float d2 = beta * (v4.z - decay * a2);
-    const float d3 = beta * (v4.w - decay * a3);
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-    for (int r = 0; r < 32; r += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
-        const float4 q4 = *reinterpret_cast<const float4*>(qv + q.row0 + r);
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 4 * (r + e);
-            s[i + 0] = fmaf(kk[e], d0, decay * s[i + 0]);
-            s[i + 1] = fmaf(kk[e], d1, decay * s[i + 1]);
-            s[i + 2] = fmaf(kk[e], d2, decay * s[i + 2]);
-            s[i + 3] = fmaf(kk[e], d3, decay * s[i + 3]);
-            o0 = fmaf(s[i + 0], qq[e], o0);
-            o1 = fmaf(s[i + 1], qq[e], o1);
-            o2 = fmaf(s[i + 2], qq[e], o2);
-            o3 = fmaf(s[i + 3], qq[e], o3);
-            if (out != nullptr)
-                __stcs(reinterpret_cast<float4*>(out + (q.row0 + r + e) * kHeadDim + q.col0),
-                       make_float4(s[i + 0], s[i + 1], s[i + 2], s[i + 3]));
-        }
-        if ((r & 7) == 4) compiler_fence();
-    }
-#pragma unroll
-    for (int m = 8; m <= 16; m <<= 1) {
-        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
-        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
-        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
-        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
-    }
-    return make_float4(o0, o1, o2, o3);
-}
-
-// The same step on a tile that stays in shared memory (row-major 128x128):
-// pass 1 reads the thread's 32x4 block for a = S^T k; pass 2 reads it again,
-// writes the updated block back in place and accumulates o = S_new^T q. Every
-// sum runs in the same order as delta_step_quad, so both give identical bits.
+// One gated delta-rule step on the thread's 32x4 block of a tile that stays in
+// shared memory (row-major 128x128). `qv` and `kv` point at the normalised q
+// (already scaled) and k of the tile's k head; v4 holds v of the four columns;
+// the four lanes of a row-block group compute the same d and o:
+//   pass 1:  a_c = sum_i S[i][c] k[i];  d_c = beta (v_c - decay a_c)         (kv = (decay S)^T k)
+//   pass 2:  S[i][c] <- decay S[i][c] + k[i] d_c, written back in place;
+//            o_c = sum_i S[i][c] q[i]                                       (S += k d^T; o = S^T q)
 __device__ __forceinline__ float4 delta_step_smem(float* tile, const float* qv, const float* kv, const Quad& q,
                                                   float4 v4, float beta, float decay) {
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -352,6 +258,173 @@ __device__ __forceinline__ float4 delta_step_smem(float* tile, const float* qv, 
     }
 #pragma unroll
     for (int m = 8; m <= 16; m <<= 1) {
+        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
+    }
+    return make_float4(o0, o1, o2, o3);
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+// ------------------------------------------------------------------------
+// Thread-block-cluster helpers (the multi-token kernel runs a 3-CTA cluster
+// per unit).
+// ------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The address of `local` (a shared-memory address of this CTA) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+// Arrives on an mbarrier of another CTA of the cluster, releasing this thread's
+// earlier memory accesses (and those it has observed) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_bounded with acquire at cluster scope (arrivals come from other CTAs).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ------------------------------------------------------------------------
+// The state tile in registers, 64 values per thread ("octet" mapping) for a
+// 256-thread CTA that owns one 128x128 tile. Lane 4 rb + qd of warp w holds
+// rows [16 rb, 16 rb + 16) of the four columns [16 w + 4 qd, +4):
+// s[4 r + c] = S[16 rb + r][16 w + 4 qd + c]. A column reduction is 16
+// in-thread FMAs plus three shuffles across rb.
+// ------------------------------------------------------------------------
+struct Octet {
+    int row0;  // first row held
+    int col0;  // first of the four columns held
+    int rb;    // row block (0..7): lane bits 2-4
+};
+
+__device__ __forceinline__ Octet octet_of(int tid) {
+    const int lane = tid & 31;
+    Octet q;
+    q.rb = lane >> 2;
+    q.row0 = 16 * q.rb;
+    q.col0 = 16 * (tid >> 5) + 4 * (lane & 3);
+    return q;
+}
+
+__device__ __forceinline__ void tile_load_octet(float (&s)[64], const float* tile, const Octet& q) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const float4 v = *reinterpret_cast<const float4*>(tile + (q.row0 + r) * kHeadDim + q.col0);
+        s[4 * r + 0] = v.x;
+        s[4 * r + 1] = v.y;
+        s[4 * r + 2] = v.z;
+        s[4 * r + 3] = v.w;
+    }
+}
+
+__device__ __forceinline__ void tile_save_octet(const float (&s)[64], float* tile, const Octet& q) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        *reinterpret_cast<float4*>(tile + (q.row0 + r) * kHeadDim + q.col0) =
+            make_float4(s[4 * r + 0], s[4 * r + 1], s[4 * r + 2], s[4 * r + 3]);
+}
+
+// The gated delta rule on the thread's 16x4 block, with the same two passes as
+// delta_step_smem (pass 1: a = S^T k and d; pass 2: S += k d^T after the
+// decay, o = S_new^T q), the block in registers, and 16-row partial sums
+// reduced over the 8 row blocks of the warp.
+__device__ __forceinline__ float4 delta_step_octet(float (&s)[64], const float* qv, const float* kv, const Octet& q,
+                                                   float4 v4, float beta, float decay) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            a0 = fmaf(s[i + 0], kk[e], a0);
+            a1 = fmaf(s[i + 1], kk[e], a1);
+            a2 = fmaf(s[i + 2], kk[e], a2);
+            a3 = fmaf(s[i + 3], kk[e], a3);
+        }
+    }
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
+        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
+    }
+    const float d0 = beta * (v4.x - decay * a0);
+    const float d1 = beta * (v4.y - decay * a1);
+    const float d2 = beta * (v4.z - decay * a2);
+    const float d3 = beta * (v4.w - decay * a3);
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float4 q4 = *reinterpret_cast<const float4*>(qv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            s[i + 0] = fmaf(kk[e], d0, decay * s[i + 0]);
+            s[i + 1] = fmaf(kk[e], d1, decay * s[i + 1]);
+            s[i + 2] = fmaf(kk[e], d2, decay * s[i + 2]);
+            s[i + 3] = fmaf(kk[e], d3, decay * s[i + 3]);
+            o0 = fmaf(s[i + 0], qq[e], o0);
+            o1 = fmaf(s[i + 1], qq[e], o1);
+            o2 = fmaf(s[i + 2], qq[e], o2);
+            o3 = fmaf(s[i + 3], qq[e], o3);
+        }
+    }
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
         o0 += __shfl_xor_sync(0xffffffffu, o0, m);
         o1 += __shfl_xor_sync(0xffffffffu, o1, m);
         o2 += __shfl_xor_sync(0xffffffffu, o2, m);

@@ -10,31 +10,35 @@
 // state held on chip (Verifier::record_window on src/core/verify.cpp).
 //
 // Work unit. One unit is (b, l, k head g): the 3 v heads 3g..3g+2 that read
-// q/k head g, their three 64 KB state tiles, and the 640 conv channels they
-// need (q and k of head g, v of the three heads). Because one CTA owns all the
-// conv channels of its unit, it reads the old conv history and writes the new
-// one with no other CTA touching those channels.
+// q/k head g. A thread-block cluster of 3 CTAs takes a unit; CTA rank h owns
+// the 64 KB tile of v head 3g + h, which its 256 threads hold in registers
+// (64 values each, the octet mapping of gdn_device.cuh) across all T tokens.
+// Two such CTAs fit on an SM, so an SM holds two tiles in registers with room
+// to spare and the kernel does not spill.
 //
-// Thread mapping. 384 threads = 3 groups of 128, one group per tile. Within a
-// group each thread holds a 32-row x 4-column block of its tile in registers
-// for the whole unit (the quad mapping of gdn_device.cuh).
+// Conv history. Each CTA convolves its own 128 v channels and, redundantly,
+// the 256 q/k channels of head g. All three CTAs read the old q/k history in
+// a unit's first chunk; a cluster barrier follows, and only after it does
+// rank 0 write the new q/k history (in the unit's last chunk). Each CTA writes
+// the history of its own v channels. The barrier also keeps the three CTAs on
+// the same unit.
 //
-// Memory pipeline. Each CTA runs on its own SM and walks units u, u + grid,
-// ... . A tile reaches shared memory through one 64 KB bulk async copy
-// (cp.async.bulk, completion on an mbarrier, evict-first in L2); as soon as a
-// group has copied its tile into registers, the group's leader issues the copy
-// of the same tile slot of the CTA's next unit. The next unit's small inputs
-// are pulled into L2 one unit ahead. Updated tiles return with 128-bit
-// streaming stores.
+// Tokens. The conv, norms and gates of up to kChunk tokens are computed into
+// shared-memory records, the recurrence walks them with the tile in
+// registers, then y is produced for the chunk. z arrives in the records by
+// bulk copy while the chunk computes. The conv history of a later chunk is
+// re-read from the previous chunk's qkv rows.
 //
-// Tokens. The conv, norms and gates of up to kChunk tokens are computed in
-// parallel into shared-memory records, then the recurrence walks those tokens
-// with the tiles in registers, then y is produced for the chunk. The conv
-// history of a chunk is re-read from the previous chunk's qkv rows.
+// Tiles. A unit's tile arrives in the CTA's slot by bulk copy, moves to
+// registers, and after the last token returns to the slot and leaves with one
+// bulk store; the slot then takes the next unit's tile. The other CTA on the
+// SM computes while one waits.
 //
-// The single-token call runs gdn_decode_t1.cu instead, with the same
-// arithmetic in the same order, so a T-token call equals T one-token calls
-// bit for bit.
+// Waits are bounded; a wait that gives up marks the CTA failed, after which it
+// computes and writes nothing but still takes part in every cluster barrier,
+// waits (bounded) for its own copies, sets the device error word and returns.
+//
+// The single-token call runs gdn_decode_t1.cu instead.
 
 #include <mutex>
 
@@ -45,30 +49,33 @@ namespace gdn {
 namespace {
 
 constexpr int kS = kHeadDim;
-constexpr int kTile = kS * kS;                       // floats per state tile
-constexpr uint32_t kTileBytes = kTile * 4;           // 65536
-constexpr int kChunk = 8;                            // tokens whose inputs are staged at once
-constexpr int kUnitChannels = 2 * kS + kGroup * kS;  // 640 conv channels per unit
-constexpr int kWarps = kThreads / 32;                // 12
+constexpr int kTile = kS * kS;              // floats per state tile
+constexpr uint32_t kTileBytes = kTile * 4;  // 65536
+constexpr int kCtaThreads = 256;            // one tile per CTA
+constexpr int kWarps = kCtaThreads / 32;    // 8
+constexpr int kChunk = 8;                   // tokens whose inputs are staged at once
+constexpr int kCtaChannels = 3 * kS;        // 384 conv channels per CTA: q, k of head g, v of its head
 
-// Per-token record in shared memory (floats). Channel slot cc of the unit maps
-// to record offset cc: q at [0,128), k at [128,256), v at [256,640).
+// Per-token record in shared memory (floats): channel slot cc of the CTA maps
+// to offset cc (q at [0,128), k at [128,256), v at [256,384)); the recurrence
+// overwrites v with o.
 constexpr int kRecQ = 0;
 constexpr int kRecK = kS;
-constexpr int kRecV = 2 * kS;
-constexpr int kRecO = kUnitChannels;        // o of the 3 heads, 384 floats
-constexpr int kRecG = kRecO + kGroup * kS;  // beta[3], decay[3], pad
-constexpr int kRecFloats = kRecG + 8;       // 1032 floats = 4128 bytes (16-byte multiple)
+constexpr int kRecV = 2 * kS;          // v, then o
+constexpr int kRecZ = 3 * kS;          // z of the CTA's head, by bulk copy
+constexpr int kRecG = 4 * kS;          // beta, decay, pad
+constexpr int kRecFloats = kRecG + 8;  // 520 floats = 2080 bytes
 
-constexpr size_t kSmemTiles = size_t(kGroup) * kTileBytes;                 // 196608
-constexpr size_t kSmemRecs = size_t(kChunk) * kRecFloats * sizeof(float);  // 33024
-constexpr size_t kSmemBars = 64;
-constexpr size_t kSmemBytes = kSmemTiles + kSmemRecs + kSmemBars;         // 229696
+constexpr size_t kOffRecs = kTileBytes;
+constexpr size_t kOffBars = kOffRecs + size_t(kChunk) * kRecFloats * 4;  // 82176
+constexpr int kBarTile = 0, kBarZ = 1, kNumBars = 2;
+constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;  // 82192
 
-static_assert(kSmemBytes <= 232448, "shared memory budget exceeds 227 KB");
-static_assert(kRecFloats % 4 == 0, "records must stay 16-byte aligned");
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit in one SM's shared memory");
+static_assert((kRecFloats * 4) % 16 == 0 && (kRecZ * 4) % 16 == 0, "records must stay 16-byte aligned");
 static_assert(kWarps >= kChunk, "one warp normalises one token's q and k");
 static_assert(kChunk >= kDConv - 1, "a chunk's conv history must come from the previous chunk");
+static_assert(kCtaThreads == 2 * kS, "slot A of a thread is a q/k channel, slot B (first 128 threads) a v channel");
 
 __device__ unsigned int g_device_error = 0;
 
@@ -90,75 +97,18 @@ struct Params {
     long long n_units;
 };
 
-// Decodes unit u into (b * L + l, k head g).
-__device__ __forceinline__ void unit_coords(long long u, long long& bl, int& g) {
-    bl = u / kKHeads;
-    g = static_cast<int>(u - bl * kKHeads);
-}
-
-// Starts L2 prefetches of everything unit u reads besides its state tiles: the
-// conv history, conv weights, per-token q/k/v slices, z slices and the alpha
-// and beta rows. Issued one unit ahead, these make the next unit's prologue and
-// epilogue loads L2 hits instead of DRAM round trips on its critical path.
-__device__ __forceinline__ void prefetch_unit_inputs(const Params& p, long long u, int tid) {
-    long long bl;
-    int g;
-    unit_coords(u, bl, g);
-    const int l = static_cast<int>(bl % p.L);
-    const int b = static_cast<int>(bl / p.L);
-    int n = p.T;
-    if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + b), 0), p.T);
-    const int items = 6 + 6 * n;
-    for (int it = tid; it < items; it += kThreads) {
-        if (it < 6) {
-            const int k = it % 3;
-            const int c = unit_channel(k == 0 ? 0 : (k == 1 ? kS : 2 * kS), g);
-            const int ch = k < 2 ? kS : kGroup * kS;
-            if (it < 3)
-                prefetch_l2(p.conv_state + (static_cast<size_t>(bl) * kConvChannels + c) * (kDConv - 1),
-                            ch * (kDConv - 1) * 4);
-            else
-                prefetch_l2(p.conv_w + (static_cast<size_t>(l) * kConvChannels + c) * kDConv, ch * kDConv * 4);
-        } else {
-            const int t = (it - 6) / 6;
-            const int k = (it - 6) - 6 * t;
-            const size_t row = static_cast<size_t>(bl) * p.T + t;
-            if (k < 3) {
-                const int c = unit_channel(k == 0 ? 0 : (k == 1 ? kS : 2 * kS), g);
-                prefetch_l2(p.qkv + row * kConvChannels + c, (k < 2 ? kS : kGroup * kS) * 4);
-            } else if (k == 3) {
-                if ((p.flags & kNoY) == 0) prefetch_l2(p.z + row * kValueDim + g * kGroup * kS, kGroup * kS * 4);
-            } else {
-                prefetch_l2((k == 4 ? p.alpha : p.beta) + row * kVHeads, kVHeads * 4);
-            }
-        }
-    }
-}
-
-// Issues the bulk copy of tile `hh` of unit `u` into its shared-memory slot.
-__device__ __forceinline__ void issue_tile(const Params& p, long long u, int hh, uint32_t dst, uint32_t bar) {
-    long long bl;
-    int g;
-    unit_coords(u, bl, g);
-    const float* src = p.state + (static_cast<size_t>(bl) * kVHeads + g * kGroup + hh) * kTile;
-    mbar_arrive_expect_tx(bar, kTileBytes);
-    bulk_load_stream(dst, src, kTileBytes, bar);
-}
-
-// Conv + SiLU of one channel slot for the chunk's tokens [c0, c0 + tc). The
-// 3-entry history before c0 (oldest first) comes from conv_state for the first
-// chunk and from the previous three qkv rows otherwise (kChunk >= 3), so no
-// history stays in registers between chunks. After the last chunk the rolled
-// window is the new conv_state.
-__device__ __forceinline__ void conv_slot(const Params& p, float* rec, int cc, int g, long long bl, int l, int c0,
-                                          int tc, bool last_chunk, bool write_state) {
-    const int c = unit_channel(cc, g);
+// Conv + SiLU of one channel c (record slot cc) for the chunk's tokens
+// [c0, c0 + tc). The 3-entry history before c0 (oldest first) is conv_state
+// for the first chunk and the previous three qkv rows otherwise; the rolled
+// window after the chunk goes to `hist`.
+__device__ __forceinline__ void conv_slot(const Params& p, float* rec, int cc, int c, long long bl, int l, int c0,
+                                          int tc, float (&hist)[3]) {
     const float4 w =
         __ldg(reinterpret_cast<const float4*>(p.conv_w + (static_cast<size_t>(l) * kConvChannels + c) * kDConv));
-    float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + c) * (kDConv - 1);
     const float* xq = p.qkv + (static_cast<size_t>(bl) * p.T + c0) * kConvChannels + c;
     float h0, h1, h2;
     if (c0 == 0) {
+        const float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + c) * (kDConv - 1);
         h0 = cs[0];
         h1 = cs[1];
         h2 = cs[2];
@@ -180,164 +130,250 @@ __device__ __forceinline__ void conv_slot(const Params& p, float* rec, int cc, i
             rec[t * kRecFloats + cc] = siluf_(xc);
         }
     }
-    if (last_chunk && write_state) {
-        cs[0] = h0;
-        cs[1] = h1;
-        cs[2] = h2;
-    }
+    hist[0] = h0;
+    hist[1] = h1;
+    hist[2] = h2;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) gdn_decode_step_kernel(const __grid_constant__ Params p) {
+__device__ __forceinline__ void store_history(const Params& p, long long bl, int c, const float (&hist)[3]) {
+    float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + c) * (kDConv - 1);
+    cs[0] = hist[0];
+    cs[1] = hist[1];
+    cs[2] = hist[2];
+}
+
+__global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    float* tiles = reinterpret_cast<float*>(smem);
-    float* rec = reinterpret_cast<float*>(smem + kSmemTiles);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemTiles + kSmemRecs);
+    float* tile = reinterpret_cast<float*>(smem);
+    float* rec = reinterpret_cast<float*>(smem + kOffRecs);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int hh = tid / kS;  // tile group = v head within the unit
-    const Quad qd = quad_of(tid % kS);
-    const bool group_leader = (tid % kS) == 0;
-    const float* my_tile = tiles + hh * kTile;
-    const uint32_t my_tile_s = smem_addr(my_tile);
-    const uint32_t my_bar = smem_addr(&bars[hh]);
+    const int hh = static_cast<int>(cluster_rank());  // v head 3g + hh of the unit
+    const long long cid = cluster_id_x();
+    const long long n_clusters = cluster_count_x();
+    const Octet oc = octet_of(tid);
+    const uint32_t tile_s = smem_addr(tile);
+    const uint32_t tile_bar = smem_addr(&bars[kBarTile]);
+    const uint32_t z_bar = smem_addr(&bars[kBarZ]);
     const bool write_state = (p.flags & kNoStateWrite) == 0;
     const bool write_y = (p.flags & kNoY) == 0;
     const bool silu_gate = (p.flags & kSiluGate) != 0;
 
     if (tid == 0) {
-        for (int h = 0; h < kGroup; ++h) mbar_init(smem_addr(&bars[h]), 1);
+        mbar_init(tile_bar, 1);
+        mbar_init(z_bar, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    __syncthreads();
 
-    long long u = blockIdx.x;
-    const long long stride = gridDim.x;
-    if (group_leader && u < p.n_units) issue_tile(p, u, hh, my_tile_s, my_bar);
-    if (u < p.n_units) prefetch_unit_inputs(p, u, tid);
-    uint32_t parity = 0;
-    bool failed = false;
+    uint32_t tile_par = 0, z_par = 0;
+    bool tile_pending = false, z_pending = false;  // copies issued and not yet waited for
+    bool failed = false;  // a bounded wait gave up: stop computing, keep taking part in cluster barriers
+    if (tid == 0 && cid < p.n_units) {
+        const long long bl = cid / kKHeads;
+        const int g = static_cast<int>(cid - bl * kKHeads);
+        mbar_arrive_expect_tx(tile_bar, kTileBytes);
+        bulk_load_stream(tile_s, p.state + (static_cast<size_t>(bl) * kVHeads + g * kGroup + hh) * kTile, kTileBytes,
+                         tile_bar);
+    }
+    tile_pending = cid < p.n_units;
+    float s[64];
 
-    for (; u < p.n_units; u += stride) {
-        if (u + stride < p.n_units) prefetch_unit_inputs(p, u + stride, tid);
-        long long bl;
-        int g;
-        unit_coords(u, bl, g);
+    for (long long u = cid; u < p.n_units; u += n_clusters) {
+        const long long bl = u / kKHeads;
+        const int g = static_cast<int>(u - bl * kKHeads);
         const int l = static_cast<int>(bl % p.L);
         const int b = static_cast<int>(bl / p.L);
+        const int vh = g * kGroup + hh;
+        const int cA = g * kS + (tid < kS ? tid : kKOffset - kS + tid);  // slot A: q or k channel of head g
+        const int cB = kVOffset + vh * kS + tid;                         // slot B: v channel (tid < 128)
         int n = p.T;
-        if (p.seq_len != nullptr) n = min(max(p.seq_len[b], 0), p.T);
+        if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + b), 0), p.T);
 
-        float s[128];
-
-        // Chunks of up to kChunk tokens. A sequence with no valid token still
-        // runs one empty chunk, so that its tile slot is consumed and refilled.
         int c0 = 0;
         do {
             const int tc = min(kChunk, n - c0);
             const bool last_chunk = (c0 + tc == n) && n > 0;
+            const bool work = !failed && tc > 0;
 
-            // ---- conv + SiLU of the unit's 640 channels; gates of its 3 heads
-            conv_slot(p, rec, tid, g, bl, l, c0, tc, last_chunk, write_state);
-            if (tid + kThreads < kUnitChannels)
-                conv_slot(p, rec, tid + kThreads, g, bl, l, c0, tc, last_chunk, write_state);
-            if (tid >= kThreads - kGroup * kChunk) {
-                const int idx = tid - (kThreads - kGroup * kChunk);
-                const int t = idx / kGroup;
-                const int hv = idx - t * kGroup;
-                if (t < tc) {
-                    const int head = g * kGroup + hv;
-                    const size_t row = (static_cast<size_t>(bl) * p.T + c0 + t) * kVHeads + head;
-                    float bt, dc;
-                    head_gates(__ldg(p.alpha + row), __ldg(p.beta + row),
-                               __ldg(p.dt + static_cast<size_t>(l) * kVHeads + head),
-                               __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + head), bt, dc);
-                    rec[t * kRecFloats + kRecG + hv] = bt;
-                    rec[t * kRecFloats + kRecG + kGroup + hv] = dc;
+            // ---- z of the chunk's tokens by bulk copy, read in the epilogue
+            if (work && write_y) {
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(z_bar, tc * kS * 4);
+                    for (int t = 0; t < tc; ++t)
+                        bulk_load(smem_addr(rec + t * kRecFloats + kRecZ),
+                                  p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, z_bar);
+                }
+                z_pending = true;
+            }
+
+            // ---- conv + SiLU of the CTA's 384 channels; the gates of its head
+            float histA[3], histB[3];
+            if (work) {
+                conv_slot(p, rec, tid, cA, bl, l, c0, tc, histA);
+                if (tid < kS) conv_slot(p, rec, 2 * kS + tid, cB, bl, l, c0, tc, histB);
+                if (tid >= kCtaThreads - kChunk) {
+                    const int t = tid - (kCtaThreads - kChunk);
+                    if (t < tc) {
+                        const size_t row = (static_cast<size_t>(bl) * p.T + c0 + t) * kVHeads + vh;
+                        float bt, dc;
+                        head_gates(__ldg(p.alpha + row), __ldg(p.beta + row),
+                                   __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh),
+                                   __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
+                        rec[t * kRecFloats + kRecG + 0] = bt;
+                        rec[t * kRecFloats + kRecG + 1] = dc;
+                    }
                 }
             }
-            __syncthreads();
+            // All three CTAs have read this unit's old q/k history (first chunk).
+            if (c0 == 0) cluster_sync();
+            else __syncthreads();
+            // The new history: q/k by rank 0 only, v by each CTA.
+            if (last_chunk && write_state && !failed) {
+                if (hh == 0) store_history(p, bl, cA, histA);
+                if (tid < kS) store_history(p, bl, cB, histB);
+            }
 
             // ---- L2 norm of q and k (one warp per token) and the q scale
-            if (warp < tc) normalize_qk(rec + warp * kRecFloats + kRecQ, rec + warp * kRecFloats + kRecK, lane);
+            if (work && warp < tc) normalize_qk(rec + warp * kRecFloats + kRecQ, rec + warp * kRecFloats + kRecK, lane);
             __syncthreads();
 
-            if (c0 == 0) {
-                // This unit's tile: wait for its copy, move it into registers,
-                // then hand the slot to the copy of the next unit's tile.
-                if (!mbar_wait_bounded(my_bar, parity)) failed = true;
-                parity ^= 1u;
-                tile_load_quad(s, my_tile, qd);
-                named_barrier(1 + hh, kS);
-                const long long next = u + stride;
-                if (group_leader && next < p.n_units) {
-                    fence_proxy_async_smem();
-                    issue_tile(p, next, hh, my_tile_s, my_bar);
+            if (c0 == 0 && !failed) {
+                // This unit's tile moves from its slot into registers.
+                const bool late = !mbar_wait_bounded(tile_bar, tile_par);
+                if (__syncthreads_or(late ? 1 : 0)) {
+                    failed = true;
+                } else {
+                    tile_par ^= 1u;
+                    tile_pending = false;
+                    if (n > 0) tile_load_octet(s, tile, oc);
                 }
             }
 
-            // ---- the gated delta rule, token by token, on the tile in registers
-            for (int t = 0; t < tc; ++t) {
-                float* r = rec + t * kRecFloats;
-                const float4 v4 = *reinterpret_cast<const float4*>(r + kRecV + hh * kS + qd.col0);
-                const float4 o4 =
-                    delta_step_quad(s, r + kRecQ, r + kRecK, qd, v4, r[kRecG + hh], r[kRecG + kGroup + hh]);
-                if (qd.rb == 0) *reinterpret_cast<float4*>(r + kRecO + hh * kS + qd.col0) = o4;
+            // ---- the gated delta rule, token by token; o overwrites v
+            if (work && !failed) {
+                for (int t = 0; t < tc; ++t) {
+                    float* r = rec + t * kRecFloats;
+                    float* vo = r + kRecV + oc.col0;
+                    const float4 v4 = *reinterpret_cast<const float4*>(vo);
+                    const float4 o4 = delta_step_octet(s, r + kRecQ, r + kRecK, oc, v4, r[kRecG], r[kRecG + 1]);
+                    __syncwarp();
+                    if (oc.rb == 0) *reinterpret_cast<float4*>(vo) = o4;
+                }
             }
 
-            if (last_chunk && write_state)
-                tile_store_quad(s, p.state + (static_cast<size_t>(bl) * kVHeads + g * kGroup + hh) * kTile, qd);
+            // ---- after the last token the tile returns through its slot
+            const bool store_tile = last_chunk && write_state && !failed;
+            if (store_tile) {
+                tile_save_octet(s, tile, oc);
+                fence_proxy_async_smem();
+            }
             __syncthreads();
+            if (tid == 0 && store_tile) {
+                bulk_store(p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile, tile_s, kTileBytes);
+                bulk_commit();
+            }
 
-            // ---- y = rms_norm(o) * ssm_norm * gate(z), one warp per (token, head)
-            if (write_y) {
-                for (int pi = warp; pi < tc * kGroup; pi += kWarps) {
-                    const int t = pi / kGroup;
-                    const int hv = pi - t * kGroup;
-                    const int head = g * kGroup + hv;
-                    const float4 o4 =
-                        *reinterpret_cast<const float4*>(rec + t * kRecFloats + kRecO + hv * kS + lane * 4);
-                    const size_t off = (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + head * kS + lane * 4;
-                    const float4 z4 = __ldg(reinterpret_cast<const float4*>(p.z + off));
-                    const float4 w4 =
-                        __ldg(reinterpret_cast<const float4*>(p.ssm_norm + static_cast<size_t>(l) * kS + lane * 4));
-                    __stcs(reinterpret_cast<float4*>(p.y + off), gated_rms_norm4(o4, z4, w4, silu_gate));
+            // ---- y = rms_norm(o) * ssm_norm * gate(z), one warp per token
+            if (z_pending && !failed) {
+                const bool late = !mbar_wait_bounded(z_bar, z_par);
+                if (__syncthreads_or(late ? 1 : 0)) {
+                    failed = true;
+                } else {
+                    z_par ^= 1u;
+                    z_pending = false;
+                    if (warp < tc) {
+                        const float* r = rec + warp * kRecFloats;
+                        const float4 o4 = *reinterpret_cast<const float4*>(r + kRecV + lane * 4);
+                        const float4 z4 = *reinterpret_cast<const float4*>(r + kRecZ + lane * 4);
+                        const float4 w4 = __ldg(
+                            reinterpret_cast<const float4*>(p.ssm_norm + static_cast<size_t>(l) * kS + lane * 4));
+                        __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + warp) * kValueDim +
+                                                         vh * kS + lane * 4),
+                               gated_rms_norm4(o4, z4, w4, silu_gate));
+                    }
                 }
             }
             c0 += kChunk;
+            __syncthreads();  // the records are rewritten by the next chunk
         } while (c0 < n);
 
-        // A wait that gave up anywhere in the CTA stops the whole CTA after this unit.
-        if (__syncthreads_or(failed ? 1 : 0)) {
-            if (tid == 0) atomicOr(&g_device_error, kErrWaitTimeout);
-            // Let the copy already issued for the next unit land before the CTA exits.
-            if (u + stride < p.n_units) (void)mbar_wait_bounded(my_bar, parity);
-            return;
+        // The slot takes the next unit's tile once the store has read it.
+        const long long next = u + n_clusters;
+        if (next < p.n_units && !failed) {
+            if (tid == 0) {
+                const long long nbl = next / kKHeads;
+                const int ng = static_cast<int>(next - nbl * kKHeads);
+                bulk_wait_read();
+                mbar_arrive_expect_tx(tile_bar, kTileBytes);
+                bulk_load_stream(tile_s, p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + hh) * kTile,
+                                 kTileBytes, tile_bar);
+            }
+            tile_pending = true;
         }
     }
+
+    if (tid == 0) {
+        // Copies still in flight land before the CTA leaves (bounded), and so do the stores.
+        if (tile_pending) (void)mbar_wait_bounded(tile_bar, tile_par);
+        if (z_pending) (void)mbar_wait_bounded(z_bar, z_par);
+        bulk_wait_all();
+        if (failed) atomicOr(&g_device_error, kErrWaitTimeout);
+    }
+    cluster_sync();  // the three CTAs of a cluster leave together
 }
 
 std::mutex g_mutex;
-int g_sms[64] = {0};
+struct DeviceSetup {
+    bool ready = false;
+    int clusters = 0;
+};
+DeviceSetup g_setup[64];
 
-cudaError_t device_setup(int* sms) {
+cudaLaunchConfig_t window_config(unsigned grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kCtaThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kGroup;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+cudaError_t device_setup(int* clusters) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_sms[dev] == 0) {
-        int n = 0;
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gdn_decode_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    DeviceSetup& d = g_setup[dev];
+    if (!d.ready) {
+        e = cudaFuncSetAttribute(gdn_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
-        g_sms[dev] = n;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = window_config(static_cast<unsigned>(kGroup * sms), nullptr, attr);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, gdn_window_kernel, &cfg);
+        if (e != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = (2 * sms) / kGroup;  // two CTAs per SM
+        }
+        d.clusters = n;
+        d.ready = true;
     }
-    *sms = g_sms[dev];
+    *clusters = d.clusters;
     return cudaSuccess;
 }
 
@@ -345,8 +381,8 @@ cudaError_t device_setup(int* sms) {
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     if (a.T == 1) return launch_decode_t1(a, stream);
-    int sms = 0;
-    cudaError_t e = device_setup(&sms);
+    int clusters = 0;
+    cudaError_t e = device_setup(&clusters);
     if (e != cudaSuccess) return e;
     Params p;
     p.qkv = a.qkv;
@@ -366,8 +402,11 @@ cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     p.T = a.T;
     p.flags = a.flags;
     p.n_units = static_cast<long long>(a.B) * a.L * kKHeads;
-    const long long grid = p.n_units < sms ? p.n_units : sms;
-    gdn_decode_step_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(p);
+    const long long n_cl = p.n_units < clusters ? p.n_units : clusters;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = window_config(static_cast<unsigned>(n_cl * kGroup), stream, attr);
+    e = cudaLaunchKernelEx(&cfg, gdn_window_kernel, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

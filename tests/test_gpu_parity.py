@@ -110,7 +110,9 @@ def _small(scale=dict(B=3, L=2, T=9), name="verify_b16_l36_t8_ragged"):
     return w, W.host_inputs(w, threads=8)
 
 
-def test_t_tokens_in_one_call_equal_t_single_calls_bitwise(g):
+def test_t_tokens_in_one_call_equal_t_single_calls(g):
+    """One T-token call and T one-token calls agree to rounding: the two kernels
+    sum the same terms in different groupings (32- vs 16-row partial sums)."""
     w, h = _small(name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     a = U.to_device(h, dev)
@@ -123,8 +125,9 @@ def test_t_tokens_in_one_call_equal_t_single_calls_bitwise(g):
             one[k] = b[k][:, :, tt:tt + 1].contiguous()
         ys.append(U.run_step(g, one))
     torch.cuda.synchronize()
-    assert torch.equal(ya, torch.cat(ys, dim=2))
-    assert torch.equal(a["state"], b["state"]) and torch.equal(a["conv_state"], b["conv_state"])
+    assert U.y_errors(ya.cpu().numpy(), torch.cat(ys, dim=2).cpu().numpy().astype("float64")) <= 1e-5
+    assert U.state_errors(a["state"].cpu().numpy(), b["state"].cpu().numpy().astype("float64")) <= 1e-5
+    assert torch.equal(a["conv_state"], b["conv_state"])
 
 
 def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g):
