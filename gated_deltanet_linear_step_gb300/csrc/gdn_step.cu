@@ -53,7 +53,7 @@ constexpr int kTile = kS * kS;              // floats per state tile
 constexpr uint32_t kTileBytes = kTile * 4;  // 65536
 constexpr int kCtaThreads = 256;            // one tile per CTA
 constexpr int kWarps = kCtaThreads / 32;    // 8
-constexpr int kChunk = 8;                   // tokens whose inputs are staged at once
+constexpr int kChunk = 16;                  // tokens whose inputs are staged at once
 constexpr int kCtaChannels = 3 * kS;        // 384 conv channels per CTA: q, k of head g, v of its head
 
 // Per-token record in shared memory (floats): channel slot cc of the CTA maps
@@ -67,13 +67,12 @@ constexpr int kRecG = 4 * kS;          // beta, decay, pad
 constexpr int kRecFloats = kRecG + 8;  // 520 floats = 2080 bytes
 
 constexpr size_t kOffRecs = kTileBytes;
-constexpr size_t kOffBars = kOffRecs + size_t(kChunk) * kRecFloats * 4;  // 82176
+constexpr size_t kOffBars = kOffRecs + size_t(kChunk) * kRecFloats * 4;  // 98816
 constexpr int kBarTile = 0, kBarZ = 1, kNumBars = 2;
-constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;  // 82192
+constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;  // 98832
 
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit in one SM's shared memory");
 static_assert((kRecFloats * 4) % 16 == 0 && (kRecZ * 4) % 16 == 0, "records must stay 16-byte aligned");
-static_assert(kWarps >= kChunk, "one warp normalises one token's q and k");
 static_assert(kChunk >= kDConv - 1, "a chunk's conv history must come from the previous chunk");
 static_assert(kCtaThreads == 2 * kS, "slot A of a thread is a q/k channel, slot B (first 128 threads) a v channel");
 
@@ -238,7 +237,9 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             }
 
             // ---- L2 norm of q and k (one warp per token) and the q scale
-            if (work && warp < tc) normalize_qk(rec + warp * kRecFloats + kRecQ, rec + warp * kRecFloats + kRecK, lane);
+            if (work)
+                for (int t = warp; t < tc; t += kWarps)
+                    normalize_qk(rec + t * kRecFloats + kRecQ, rec + t * kRecFloats + kRecK, lane);
             __syncthreads();
 
             if (c0 == 0 && !failed) {
@@ -285,13 +286,13 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                 } else {
                     z_par ^= 1u;
                     z_pending = false;
-                    if (warp < tc) {
-                        const float* r = rec + warp * kRecFloats;
+                    for (int t = warp; t < tc; t += kWarps) {
+                        const float* r = rec + t * kRecFloats;
                         const float4 o4 = *reinterpret_cast<const float4*>(r + kRecV + lane * 4);
                         const float4 z4 = *reinterpret_cast<const float4*>(r + kRecZ + lane * 4);
                         const float4 w4 = __ldg(
                             reinterpret_cast<const float4*>(p.ssm_norm + static_cast<size_t>(l) * kS + lane * 4));
-                        __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + warp) * kValueDim +
+                        __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim +
                                                          vh * kS + lane * 4),
                                gated_rms_norm4(o4, z4, w4, silu_gate));
                     }
