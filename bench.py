@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--op", default="step", choices=["step", "ab_gates"],
+                    help="step: the decode step (the default bench line); ab_gates: the fused alpha/beta projection")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
@@ -436,6 +438,58 @@ def run_gdn(args, w_global, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ab_gates(args, w):
+    """Times the fused alpha/beta projection with its gate epilogue on the workload's shape."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    g.load_library()
+    dev = torch.device("cuda", 0)
+    h = W.host_ab_inputs(w)
+    x = torch.from_numpy(h["x"]).to(dev)
+    wa = torch.from_numpy(h["w_alpha"].view(np.int16)).to(dev).view(torch.bfloat16)
+    wb = torch.from_numpy(h["w_beta"].view(np.int16)).to(dev).view(torch.bfloat16)
+    dt = torch.from_numpy(h["dt"]).to(dev)
+    sa = torch.from_numpy(h["ssm_a"]).to(dev)
+    gate = torch.empty((w.B, w.L, w.T, 48), device=dev)
+    beta = torch.empty_like(gate)
+
+    def step():
+        g.gdn_ab_gates(x, wa, wb, dt, sa, gate, beta)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clocks:
+        clocks.mark_start()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+    ms = a.elapsed_time(b) / args.steps
+    rows = w.B * w.L * w.T
+    flops = 2.0 * rows * 96 * W.N_EMBD
+    peak = 152 * 128 * 2 * 2070e6 / 1e12  # FP32 lanes x FMA x max SM clock
+    achieved = flops / (ms / 1e3) / 1e12
+    byts = rows * W.N_EMBD * 4 + w.L * 96 * W.N_EMBD * 2 + rows * 96 * 4
+    print(json.dumps({
+        "metric": "alpha/beta projection + gate epilogue, rows (seq*layer*token) per second", "op": "ab_gates",
+        "value": rows / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 x bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "T": w.T, "n_embd": W.N_EMBD, "outputs": 96,
+                   "timing": f"{args.steps} launches in one captured CUDA graph"},
+        "clocks": clocks.summary(), "gpu_launches": args.steps,
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
+                     "hbm_gbs": byts / (ms / 1e3) / 1e9},
+    }), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -445,7 +499,10 @@ def main():
     if args.batch is not None:
         base = base.scaled(B=args.batch, name=f"{base.name}_b{args.batch}")
     w_global = base.scaled(B=base.B * world) if world > 1 else base
-    if args.impl == "reference":
+    if args.op == "ab_gates":
+        if rank == 0:
+            run_ab_gates(args, base)
+    elif args.impl == "reference":
         run_reference(args, base, world, rank)
     else:
         run_gdn(args, w_global, world, rank, local)

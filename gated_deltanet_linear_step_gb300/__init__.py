@@ -6,10 +6,12 @@ the same function names. Importing the package loads nothing; the first call
 loads the library and raises if it has not been built.
 """
 from ._binding import (  # noqa: F401
+    FLAG_GATES_READY,
     FLAG_NO_STATE_WRITE,
     FLAG_NO_Y,
     FLAG_SILU_GATE,
     GdnError,
+    gdn_ab_gates,
     gdn_decode_step,
     gdn_decode_step_ex,
     gdn_decode_step_varlen,

@@ -28,6 +28,7 @@ D_CONV = 4
 FLAG_NO_STATE_WRITE = 0x1
 FLAG_NO_Y = 0x2
 FLAG_SILU_GATE = 0x4
+FLAG_GATES_READY = 0x8
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_ALIAS",
           5: "GDN_ERR_CUDA", 6: "GDN_ERR_FLAGS"}
@@ -57,8 +58,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_verify_window.argtypes = [_P] * 12 + [_I, _I, _I, _P]
         lib.gdn_verify_commit.argtypes = [_P] * 9 + [_I, _I, _I, _P]
         lib.gdn_decode_step_ex.argtypes = [_P] * 12 + [_I, _I, _I, ctypes.c_uint32, _P]
+        lib.gdn_ab_gates.argtypes = [_P] * 7 + [_I, _I, _I, _I, _P]
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_get_geometry", "gdn_read_device_error"):
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_get_geometry", "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         lib.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -186,6 +188,31 @@ def gdn_decode_step_ex(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_st
     sl = _ptr(seq_len, "seq_len", (B,), dtype=torch.int32, device=dev, optional=True)
     with torch.cuda.device(dev):
         _check(lib.gdn_decode_step_ex(*p, sl, B, L, T, int(flags), _stream_handle(stream, dev)))
+
+
+def gdn_ab_gates(x, w_alpha, w_beta, dt, ssm_a, gate, beta, stream=None):
+    """alpha/beta projections with the gate epilogue: writes the log decay to ``gate`` and
+    sigmoid(beta_raw) to ``beta`` ([B][L][T][48]); the weights are [L][48][n_embd] BF16
+    (torch.bfloat16, or their bit patterns as int16/uint16)."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    for name, w in (("w_alpha", w_alpha), ("w_beta", w_beta)):
+        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    p = [
+        _ptr(x, "x", (B, L, T, E), device=dev),
+        _ptr(w_alpha, "w_alpha", (L, V_HEADS, E), dtype=w_alpha.dtype, device=dev),
+        _ptr(w_beta, "w_beta", (L, V_HEADS, E), dtype=w_beta.dtype, device=dev),
+        _ptr(dt, "dt", (L, V_HEADS), device=dev),
+        _ptr(ssm_a, "ssm_a", (L, V_HEADS), device=dev),
+        _ptr(gate, "gate", (B, L, T, V_HEADS), device=dev),
+        _ptr(beta, "beta", (B, L, T, V_HEADS), device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_ab_gates(*p, B, L, T, E, _stream_handle(stream, dev)))
 
 
 def gdn_get_geometry() -> dict:

@@ -1,0 +1,202 @@
+// gdn_ab.cu - the alpha/beta projections of a GDN layer with their gate
+// epilogue, fused (the fused_gdn_ab stage of gdn_layer step 5 on the
+// Winery-Strata page src/core/layer.cpp): for every (sequence b, layer l,
+// token t) and v head h,
+//
+//   alpha_raw = x . Wa[l][h],  beta_raw = x . Wb[l][h]      (BF16 weights, fp32 activations, fp32 sums)
+//   gate      = softplus(alpha_raw + dt[l][h]) * ssm_a[l][h] (the log of the decay)
+//   beta      = sigmoid(beta_raw)
+//
+// x is read once for both projections. Per layer this is a small GEMM:
+// [rows = B*T] x [n_embd] times [n_embd] x [96]. A cluster of kSplit CTAs takes
+// 16 rows of one layer, each CTA a contiguous share of n_embd. x and both
+// weight blocks stream through double-buffered shared memory in 64-wide
+// slices by 16-byte asynchronous copies (weight rows padded to 144 bytes, so a
+// thread reads eight weights of an output with one 16-byte load), and each of
+// the 128 threads accumulates 2 rows x 6 outputs in fp32 registers. Rank 0 then
+// adds the other ranks' partial sums, read from their shared memory across
+// the cluster, and applies the gate epilogue; no global workspace is involved.
+
+#include <cuda_bf16.h>
+
+#include "gdn_device.cuh"
+#include "gdn_launch.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kAbThreads = 128;
+constexpr int kRowsPerCta = 16;
+constexpr int kOut = 2 * kVHeads;  // 96: alpha heads, then beta heads
+constexpr int kKSlice = 64;        // n_embd elements per shared-memory slice
+constexpr int kSplit = 4;          // CTAs per cluster, each summing a share of n_embd
+
+struct AbParams {
+    const float* x;          // [B][L][T][E]
+    const uint16_t* wa;      // [L][48][E] bf16 bits
+    const uint16_t* wb;      // [L][48][E] bf16 bits
+    const float* dt;         // [L][48]
+    const float* ssm_a;      // [L][48]
+    float* gate;             // [B][L][T][48]
+    float* beta;             // [B][L][T][48]
+    int B, L, T, E;
+};
+
+__global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_constant__ AbParams p) {
+    __shared__ __align__(16) float xs[2][kRowsPerCta][kKSlice];          // 8 KB, double-buffered
+    __shared__ __align__(16) __nv_bfloat16 ws[2][kOut][kKSlice + 8];    // 27 KB, rows padded to 144 bytes
+    __shared__ __align__(16) float part[kAbThreads][12];               // 6 KB: this CTA's partial sums
+
+    const int tid = threadIdx.x;
+    const int l = blockIdx.y;
+    const int rank = static_cast<int>(cluster_rank());
+    const int M = p.B * p.T;                 // rows of this layer
+    const int m0 = (blockIdx.x / kSplit) * kRowsPerCta;
+    const int n_slices = p.E / kKSlice;
+    const int s_begin = n_slices * rank / kSplit, s_end = n_slices * (rank + 1) / kSplit;
+    const int mp = tid >> 4;                 // row pair 0..7 -> rows 2 mp, 2 mp + 1
+    const int n0 = (tid & 15) * 6;           // first of six outputs
+
+    // Global row of layer-local row m (m = b * T + t).
+    auto x_row = [&](int m) -> const float* {
+        const int b = m / p.T, t = m - (m / p.T) * p.T;
+        return p.x + ((static_cast<size_t>(b) * p.L + l) * p.T + t) * p.E;
+    };
+
+    float acc[2][6];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 6; ++j) acc[i][j] = 0.f;
+
+    // Slice loads: 16-byte asynchronous copies into buffer `buf`.
+    auto load_slice = [&](int sl, int buf) {
+        const int k0 = sl * kKSlice;
+        for (int i = tid; i < kRowsPerCta * kKSlice / 4; i += kAbThreads) {
+            const int r = i / (kKSlice / 4), c = (i % (kKSlice / 4)) * 4;
+            const int m = m0 + r < M ? m0 + r : M - 1;  // rows past M read a valid row; their sums are not stored
+            cp_async16(smem_addr(&xs[buf][r][c]), x_row(m) + k0 + c);
+        }
+        for (int i = tid; i < kOut * kKSlice / 8; i += kAbThreads) {
+            const int n = i / (kKSlice / 8), c = (i % (kKSlice / 8)) * 8;
+            const uint16_t* src = (n < kVHeads ? p.wa + (static_cast<size_t>(l) * kVHeads + n) * p.E
+                                               : p.wb + (static_cast<size_t>(l) * kVHeads + n - kVHeads) * p.E) +
+                                  k0 + c;
+            cp_async16(smem_addr(&ws[buf][n][c]), src);
+        }
+        cp_async_commit();
+    };
+
+    if (s_begin < s_end) load_slice(s_begin, 0);
+    for (int sl = s_begin; sl < s_end; ++sl) {
+        const int buf = (sl - s_begin) & 1;
+        if (sl + 1 < s_end) {
+            load_slice(sl + 1, buf ^ 1);
+            cp_async_wait_one();  // this slice has landed; the next may still be in flight
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int k = 0; k < kKSlice; k += 8) {
+            float xv[2][8];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float4 a = *reinterpret_cast<const float4*>(&xs[buf][2 * mp + i][k]);
+                const float4 b = *reinterpret_cast<const float4*>(&xs[buf][2 * mp + i][k + 4]);
+                xv[i][0] = a.x; xv[i][1] = a.y; xv[i][2] = a.z; xv[i][3] = a.w;
+                xv[i][4] = b.x; xv[i][5] = b.y; xv[i][6] = b.z; xv[i][7] = b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(&ws[buf][n0 + j][k]);
+                const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 w = __bfloat1622float2(w2[e]);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        acc[i][j] = fmaf(xv[i][2 * e], w.x, acc[i][j]);
+                        acc[i][j] = fmaf(xv[i][2 * e + 1], w.y, acc[i][j]);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // the buffer is refilled two slices later
+    }
+
+    // Partial sums meet on rank 0.
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 6; ++j) part[tid][6 * i + j] = acc[i][j];
+    cluster_sync();
+    if (rank == 0) {
+        for (int r = 1; r < kSplit; ++r) {
+            const uint32_t remote = cluster_map(smem_addr(&part[tid][0]), r);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 6; ++j) {
+                    float v;
+                    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote + 4 * (6 * i + j)));
+                    acc[i][j] += v;
+                }
+        }
+    }
+    cluster_sync();  // the other ranks' partial sums stay in place until rank 0 has read them
+    if (rank != 0) return;
+
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int m = m0 + 2 * mp + i;
+        if (m >= M) continue;
+        const int b = m / p.T, t = m - (m / p.T) * p.T;
+        const size_t row = ((static_cast<size_t>(b) * p.L + l) * p.T + t) * kVHeads;
+#pragma unroll
+        for (int j = 0; j < 6; ++j) {
+            const int n = n0 + j;
+            if (n < kVHeads) {
+                p.gate[row + n] = softplusf_(acc[i][j] + p.dt[static_cast<size_t>(l) * kVHeads + n]) *
+                                  p.ssm_a[static_cast<size_t>(l) * kVHeads + n];
+            } else {
+                p.beta[row + n - kVHeads] = sigmoidf_(acc[i][j]);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream) {
+    AbParams p;
+    p.x = a.x;
+    p.wa = a.w_alpha;
+    p.wb = a.w_beta;
+    p.dt = a.dt;
+    p.ssm_a = a.ssm_a;
+    p.gate = a.gate;
+    p.beta = a.beta;
+    p.B = a.B;
+    p.L = a.L;
+    p.T = a.T;
+    p.E = a.n_embd;
+    const int M = a.B * a.T;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(((M + kRowsPerCta - 1) / kRowsPerCta) * kSplit, a.L, 1);
+    cfg.blockDim = dim3(kAbThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gdn_ab_gates_kernel, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

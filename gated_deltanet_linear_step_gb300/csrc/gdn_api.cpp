@@ -18,7 +18,7 @@ static_assert(GDN_VALUE_DIM == gdn::kValueDim, "geometry mismatch");
 static_assert(GDN_D_CONV == gdn::kDConv, "geometry mismatch");
 static_assert(GDN_MAX_T == gdn::kMaxT, "geometry mismatch");
 static_assert(GDN_FLAG_NO_STATE_WRITE == gdn::kNoStateWrite && GDN_FLAG_NO_Y == gdn::kNoY &&
-                  GDN_FLAG_SILU_GATE == gdn::kSiluGate,
+                  GDN_FLAG_SILU_GATE == gdn::kSiluGate && GDN_FLAG_GATES_READY == gdn::kGatesReady,
               "flag mismatch");
 
 namespace {
@@ -56,7 +56,7 @@ gdn_status run(const float* qkv, const float* z, const float* alpha, const float
                float* y, const int32_t* seq_len, int B, int L, int T, uint32_t flags, void* stream,
                const char* fn) {
     t_last_error.clear();
-    const uint32_t known = gdn::kNoStateWrite | gdn::kNoY | gdn::kSiluGate;
+    const uint32_t known = gdn::kNoStateWrite | gdn::kNoY | gdn::kSiluGate | gdn::kGatesReady;
     if (flags & ~known) return fail(GDN_ERR_FLAGS, "%s: unknown flag bits 0x%x", fn, flags & ~known);
     const bool want_y = (flags & gdn::kNoY) == 0;
     const bool write_state = (flags & gdn::kNoStateWrite) == 0;
@@ -171,6 +171,59 @@ gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alp
                               int T, uint32_t flags, void* stream) {
     return run(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state, y, seq_len, B, L, T, flags,
                stream, "gdn_decode_step_ex");
+}
+
+gdn_status gdn_ab_gates(const float* x, const uint16_t* w_alpha, const uint16_t* w_beta, const float* dt,
+                        const float* ssm_a, float* gate, float* beta, int B, int L, int T, int n_embd, void* stream) {
+    t_last_error.clear();
+    const char* fn = "gdn_ab_gates";
+    const struct {
+        const char* name;
+        const void* p;
+    } ptrs[] = {{"x", x}, {"w_alpha", w_alpha}, {"w_beta", w_beta}, {"dt", dt},
+                {"ssm_a", ssm_a}, {"gate", gate}, {"beta", beta}};
+    for (const auto& q : ptrs) {
+        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
+    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
+    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
+    const unsigned long long b = B, l = L, t = T, e = n_embd;
+    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
+    const Span spans[] = {
+        {"x", x, b * l * t * e * 4, false},
+        {"w_alpha", w_alpha, l * gdn::kVHeads * e * 2, false},
+        {"w_beta", w_beta, l * gdn::kVHeads * e * 2, false},
+        {"dt", dt, l * gdn::kVHeads * 4, false},
+        {"ssm_a", ssm_a, l * gdn::kVHeads * 4, false},
+        {"gate", gate, b * l * t * gdn::kVHeads * 4, true},
+        {"beta", beta, b * l * t * gdn::kVHeads * 4, true},
+    };
+    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
+    for (int i = 0; i < n; ++i) {
+        if (!spans[i].output) continue;
+        for (int k = 0; k < n; ++k)
+            if (k != i && overlaps(spans[i], spans[k]))
+                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
+    }
+    gdn::AbArgs a;
+    a.x = x;
+    a.w_alpha = w_alpha;
+    a.w_beta = w_beta;
+    a.dt = dt;
+    a.ssm_a = ssm_a;
+    a.gate = gate;
+    a.beta = beta;
+    a.B = B;
+    a.L = L;
+    a.T = T;
+    a.n_embd = n_embd;
+    const cudaError_t err = gdn::launch_ab_gates(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
+    return GDN_OK;
 }
 
 const char* gdn_last_error(void) { return t_last_error.c_str(); }

@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
                 const int hv = tid - (kThreads - kGroup);
                 const int head = x.g * kGroup + hv;
                 float bt, dc;
-                head_gates(S[kStAlpha + head], S[kStBeta + head], wt[kWtDt + head], wt[kWtA + head], bt, dc);
+                head_gates_in((p.flags & kGatesReady) != 0, S[kStAlpha + head], S[kStBeta + head], wt[kWtDt + head],
+                              wt[kWtA + head], bt, dc);
                 gates[hv] = bt;
                 gates[kGroup + hv] = dc;
             }

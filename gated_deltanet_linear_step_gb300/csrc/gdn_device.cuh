@@ -105,6 +105,21 @@ __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.w
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// One 16-byte global -> shared asynchronous copy by this thread (both addresses
+// 16-byte aligned), cached in L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Closes this thread's current group of cp.async copies.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most one of this thread's committed cp.async groups is still in flight.
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Waits until all of this thread's committed cp.async groups have landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Pulls [src, src + bytes) into L2 without waiting (16-byte aligned, 16-byte multiple).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -145,6 +160,18 @@ __device__ __forceinline__ void head_gates(float alpha_raw, float beta_raw, floa
                                            float& decay) {
     beta = sigmoidf_(beta_raw);
     decay = expf(softplusf_(alpha_raw + dt) * ssm_a);
+}
+
+// beta and decay of one v head, from raw projections or, with `ready`, from
+// a precomputed log decay (in alpha_or_gate) and beta (in beta_in).
+__device__ __forceinline__ void head_gates_in(bool ready, float alpha_or_gate, float beta_in, float dt, float ssm_a,
+                                              float& beta, float& decay) {
+    if (ready) {
+        beta = beta_in;
+        decay = expf(alpha_or_gate);
+    } else {
+        head_gates(alpha_or_gate, beta_in, dt, ssm_a, beta, decay);
+    }
 }
 
 // In place, by one warp: q <- q / sqrt(|q|^2 + eps) / sqrt(128) and

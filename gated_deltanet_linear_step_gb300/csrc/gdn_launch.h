@@ -25,6 +25,7 @@ constexpr int kThreads = kGroup * kHeadDim;       // 384: one thread per state c
 constexpr uint32_t kNoStateWrite = 0x1u;
 constexpr uint32_t kNoY = 0x2u;
 constexpr uint32_t kSiluGate = 0x4u;
+constexpr uint32_t kGatesReady = 0x8u;  // alpha holds the log decay, beta holds beta (post-activation)
 
 struct StepArgs {
     const float* qkv;
@@ -42,6 +43,20 @@ struct StepArgs {
     int B, L, T;
     uint32_t flags;
 };
+
+struct AbArgs {
+    const float* x;
+    const uint16_t* w_alpha;
+    const uint16_t* w_beta;
+    const float* dt;
+    const float* ssm_a;
+    float* gate;
+    float* beta;
+    int B, L, T, n_embd;
+};
+
+// The fused alpha/beta projections with their gate epilogue (gdn_ab.cu).
+cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream);
 
 // Launches the fused decode step on `stream`: the single-token kernel when
 // T == 1, the multi-token kernel otherwise. Returns the launch status.

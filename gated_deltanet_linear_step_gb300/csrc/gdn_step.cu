@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                     if (t < tc) {
                         const size_t row = (static_cast<size_t>(bl) * p.T + c0 + t) * kVHeads + vh;
                         float bt, dc;
-                        head_gates(__ldg(p.alpha + row), __ldg(p.beta + row),
+                        head_gates_in((p.flags & kGatesReady) != 0, __ldg(p.alpha + row), __ldg(p.beta + row),
                                    __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh),
                                    __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
                         rec[t * kRecFloats + kRecG + 0] = bt;

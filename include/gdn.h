@@ -69,6 +69,8 @@ typedef enum gdn_status {
 #define GDN_FLAG_NO_STATE_WRITE 0x1u /* leave state and conv_state untouched */
 #define GDN_FLAG_NO_Y 0x2u           /* write no y (y may be NULL) */
 #define GDN_FLAG_SILU_GATE 0x4u      /* y = rms_norm(o) * w * SiLU(z): the earlier model variant's gate */
+#define GDN_FLAG_GATES_READY 0x8u    /* alpha holds the log decay and beta holds beta, as gdn_ab_gates writes them;
+                                        dt and ssm_a are still passed but do not enter the result */
 
 /*
  * gdn_decode_step - one decode call: T tokens applied in order per (sequence, layer).
@@ -141,6 +143,29 @@ gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alp
                               const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
                               float* conv_state, float* state, float* y, const int32_t* seq_len, int B, int L,
                               int T, uint32_t flags, void* stream);
+
+/*
+ * gdn_ab_gates - the alpha/beta projections of the layer with their gate
+ * epilogue, fused (fused_gdn_ab in gdn_layer step 5 on the page
+ * src/core/layer.cpp). For every (b, l, t) row of x and v head h:
+ *
+ *   alpha_raw = sum_k x[k] * w_alpha[l][h][k],  beta_raw likewise with w_beta
+ *   gate[b][l][t][h] = softplus(alpha_raw + dt[l][h]) * ssm_a[l][h]   (log decay)
+ *   beta[b][l][t][h] = sigmoid(beta_raw)
+ *
+ *   x        [B][L][T][n_embd] fp32 activations (input)
+ *   w_alpha  [L][48][n_embd]   BF16 bit patterns (uint16), the ssm_alpha weight (input)
+ *   w_beta   [L][48][n_embd]   BF16 bit patterns, the ssm_beta weight (input)
+ *   dt, ssm_a [L][48]          (input)
+ *   gate, beta [B][L][T][48]   (outputs; feed gdn_decode_step_ex with GDN_FLAG_GATES_READY)
+ *   n_embd: a positive multiple of 64, at most 65536.
+ *
+ * Products are formed in fp32 from the exactly widened BF16 weights and summed
+ * in fp32. Same conventions (device memory, 16-byte alignment, asynchronous on
+ * `stream`, outputs overlap nothing) as the calls above.
+ */
+gdn_status gdn_ab_gates(const float* x, const uint16_t* w_alpha, const uint16_t* w_beta, const float* dt,
+                        const float* ssm_a, float* gate, float* beta, int B, int L, int T, int n_embd, void* stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);

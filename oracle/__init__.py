@@ -130,6 +130,22 @@ def gates(alpha_raw, beta_raw, dt, ssm_a):
     return beta, np.exp(g)
 
 
+def ab_gates(x, w_alpha, w_beta, dt, ssm_a):
+    """The alpha/beta projections with their gate epilogue (the fused_gdn_ab stage of
+    gdn_layer step 5 on src/core/layer.cpp): alpha_raw = x . w_alpha[h], beta_raw =
+    x . w_beta[h]; returns (gate, beta) with gate = softplus(alpha_raw + dt) * ssm_a,
+    the log of the decay, and beta = sigmoid(beta_raw).
+
+    ``x`` is [..., n_embd]; the weights are [48][n_embd] (the BF16 values, exactly as
+    float); ``dt`` and ``ssm_a`` are [48].
+    """
+    x = np.asarray(x, np.float64)
+    alpha_raw = x @ np.asarray(w_alpha, np.float64).T
+    beta_raw = x @ np.asarray(w_beta, np.float64).T
+    gate = softplus(alpha_raw + np.asarray(dt, np.float64)) * np.asarray(ssm_a, np.float64)
+    return gate, sigmoid(beta_raw)
+
+
 # ---------------------------------------------------------------- step 6 --
 def delta_rule_step(S, k, q, v, beta, decay):
     """One gated delta-rule step on one head's state, in the definition's order.
@@ -157,8 +173,10 @@ def gated_rms_norm(o, z, w, eps: float = EPS, gate: str = "sigmoid"):
 
 
 # ------------------------------------------------------------ steps 1-5 --
-def preprocess_token(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a):
-    """Steps 1-5 for one token of one (sequence, layer).
+def preprocess_token(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a, gates_ready: bool = False):
+    """Steps 1-5 for one token of one (sequence, layer). With ``gates_ready``,
+    ``alpha_raw`` already holds the log decay and ``beta_raw`` holds beta (the
+    outputs of ``ab_gates``).
 
     Returns a dict with the normalised and scaled q (16x128), the normalised
     k (16x128), v (48x128), beta and decay (48 each), the conv output before
@@ -171,7 +189,10 @@ def preprocess_token(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a):
     v = h[V_OFFSET:].reshape(V_HEADS, HEAD_DIM)           # not normalised
     q = l2_normalize(q) * (1.0 / math.sqrt(HEAD_DIM))     # scale after the norm
     k = l2_normalize(k)
-    beta, decay = gates(alpha_raw, beta_raw, dt, ssm_a)
+    if gates_ready:
+        beta, decay = np.asarray(beta_raw, np.float64), np.exp(np.asarray(alpha_raw, np.float64))
+    else:
+        beta, decay = gates(alpha_raw, beta_raw, dt, ssm_a)
     return {"q": q, "k": k, "v": v, "beta": beta, "decay": decay, "xc": xc,
             "conv_state": roll_conv_state(conv_state, x)}
 
@@ -182,12 +203,12 @@ def v_head_to_k_head(h: int) -> int:
 
 
 def gdn_layer_step(x, z, alpha_raw, beta_raw, dt, ssm_a, conv_w, ssm_norm, conv_state, state,
-                   gate: str = "sigmoid"):
+                   gate: str = "sigmoid", gates_ready: bool = False):
     """Steps 1-7 for one token of one (sequence, layer).
 
     ``state`` is (48, 128, 128). Returns (y (6144,), new state, new conv history).
     """
-    p = preprocess_token(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a)
+    p = preprocess_token(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a, gates_ready)
     new_state = np.empty((V_HEADS, HEAD_DIM, HEAD_DIM), np.float64)
     o = np.empty((V_HEADS, HEAD_DIM), np.float64)
     for h in range(V_HEADS):
@@ -200,7 +221,7 @@ def gdn_layer_step(x, z, alpha_raw, beta_raw, dt, ssm_a, conv_w, ssm_norm, conv_
 
 
 def gdn_decode(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, state,
-               seq_len=None, gate: str = "sigmoid"):
+               seq_len=None, gate: str = "sigmoid", gates_ready: bool = False):
     """The whole decode call: B sequences x L layers x T tokens.
 
     Shapes (outermost first): qkv [B][L][T][10240], z [B][L][T][6144],
@@ -224,11 +245,12 @@ def gdn_decode(qkv, z, alpha, beta, dt, ssm_a, conv_w, ssm_norm, conv_state, sta
             sl = {"qkv": qkv[b, l], "z": z[b, l], "alpha": alpha[b, l], "beta": beta[b, l],
                   "conv_state": conv_state[b, l], "state": state[b, l]}
             wts = {"dt": dt[l], "ssm_a": ssm_a[l], "conv_w": conv_w[l], "ssm_norm": ssm_norm[l]}
-            y[b, l], state_out[b, l], conv_out[b, l] = gdn_decode_slice(sl, wts, n, gate=gate)
+            y[b, l], state_out[b, l], conv_out[b, l] = gdn_decode_slice(sl, wts, n, gate=gate,
+                                                                        gates_ready=gates_ready)
     return y, state_out, conv_out
 
 
-def gdn_decode_slice(sl: dict, wts: dict, n: int | None = None, gate: str = "sigmoid"):
+def gdn_decode_slice(sl: dict, wts: dict, n: int | None = None, gate: str = "sigmoid", gates_ready: bool = False):
     """``gdn_decode`` for one (sequence, layer): ``sl`` holds qkv [T][C], z, alpha,
     beta, conv_state, state; ``wts`` holds dt, ssm_a, conv_w, ssm_norm of the layer.
 
@@ -241,5 +263,6 @@ def gdn_decode_slice(sl: dict, wts: dict, n: int | None = None, gate: str = "sig
     cs = np.asarray(sl["conv_state"], np.float32)
     for t in range(n):
         y[t], st, cs = gdn_layer_step(sl["qkv"][t], sl["z"][t], sl["alpha"][t], sl["beta"][t], wts["dt"],
-                                      wts["ssm_a"], wts["conv_w"], wts["ssm_norm"], cs, st, gate=gate)
+                                      wts["ssm_a"], wts["conv_w"], wts["ssm_norm"], cs, st, gate=gate,
+                                      gates_ready=gates_ready)
     return y, st, cs

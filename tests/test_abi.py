@@ -38,7 +38,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-               "gdn_decode_step_ex", "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
+               "gdn_decode_step_ex", "gdn_ab_gates", "gdn_last_error", "gdn_get_geometry",
+               "gdn_read_device_error"):
         assert fn in names
 
 
@@ -133,7 +134,7 @@ def test_output_aliasing_rejected(lib):
 def test_flags_and_window_rules(lib):
     p = fake_ptrs()
     args = [p[k] for k in ORDER]
-    assert lib.gdn_decode_step_ex(*args, None, B, L, T, 0x8, None) == 6
+    assert lib.gdn_decode_step_ex(*args, None, B, L, T, 0x10, None) == 6
     # the verify window reads the states: y may not overlap them
     w = dict(p)
     w["y"] = w["state"]
@@ -143,3 +144,22 @@ def test_flags_and_window_rules(lib):
                                  p["conv_state"], p["state"], None, B, L, T, None) == 1
     # misaligned seq_len
     assert lib.gdn_decode_step_varlen(*args, (1 << 39) + 2, B, L, T, None) == 3
+
+
+@no_gpu
+def test_ab_gates_argument_checks(lib):
+    base = 1 << 41
+    E = 128
+    ptr = {"x": base, "wa": base + (1 << 30), "wb": base + (2 << 30), "dt": base + (3 << 30),
+           "sa": base + (4 << 30), "gate": base + (5 << 30), "beta": base + (6 << 30)}
+    args = lambda p: [p[k] for k in ("x", "wa", "wb", "dt", "sa", "gate", "beta")]  # noqa: E731
+    assert lib.gdn_ab_gates(*args(ptr), 2, 3, 1, 100, None) == 2       # n_embd not a multiple of 64
+    assert lib.gdn_ab_gates(*args(ptr), 0, 3, 1, E, None) == 2
+    p = dict(ptr, wb=None)
+    assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 1
+    p = dict(ptr, gate=ptr["x"] + 64)
+    assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 4
+    p = dict(ptr, beta=ptr["gate"] + 16)
+    assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 4
+    p = dict(ptr, x=ptr["x"] + 8)
+    assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 3

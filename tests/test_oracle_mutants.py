@@ -100,8 +100,8 @@ def _softplus_wrong(x):
 def _make_pre(normalize_v=False, scale_q=True, silu_qk_only=False):
     orig = O.preprocess_token
 
-    def pre(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a):
-        p = orig(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a)
+    def pre(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a, gates_ready=False):
+        p = orig(x, conv_state, conv_w, alpha_raw, beta_raw, dt, ssm_a, gates_ready)
         if normalize_v:
             p["v"] = O.l2_normalize(p["v"])
         if not scale_q:

@@ -376,3 +376,47 @@ def test_batch_permutation_equivariance():
     assert np.array_equal(np.isnan(yp), np.isnan(y[perm]))
     assert np.array_equal(np.nan_to_num(yp), np.nan_to_num(y[perm]))
     assert np.array_equal(stp, st[perm]) and np.array_equal(csp, cs[perm])
+
+
+# ------------------------------------------- the alpha/beta projection --
+def test_ab_gates_one_hot_input_picks_a_weight_column():
+    r = _rng(50)
+    E = 64
+    wa = r.standard_normal((48, E))
+    wb = r.standard_normal((48, E))
+    dt = r.standard_normal(48)
+    ssm_a = -np.exp(r.random(48))
+    x = np.zeros(E)
+    x[17] = 1.0
+    gate, beta = O.ab_gates(x, wa, wb, dt, ssm_a)
+    for h in (0, 20, 47):
+        a = wa[h, 17] + dt[h]
+        assert gate[h] == pytest.approx((max(a, 0) + math.log1p(math.exp(-abs(a)))) * ssm_a[h], rel=1e-14)
+        assert beta[h] == pytest.approx(1.0 / (1.0 + math.exp(-wb[h, 17])), rel=1e-14)
+
+
+def test_ab_gates_matches_scalar_sums_and_feeds_the_step():
+    r = _rng(51)
+    E = 96
+    x = r.standard_normal((3, E))
+    wa = r.standard_normal((48, E)) / math.sqrt(E)
+    wb = r.standard_normal((48, E)) / math.sqrt(E)
+    dt = r.standard_normal(48) * 0.5
+    ssm_a = -np.exp(r.random(48) * math.log(16))
+    gate, beta = O.ab_gates(x, wa, wb, dt, ssm_a)
+    assert gate.shape == (3, 48) and beta.shape == (3, 48)
+    for i, h in ((0, 0), (1, 33), (2, 47)):
+        ar = math.fsum(x[i, k] * wa[h, k] for k in range(E))
+        br = math.fsum(x[i, k] * wb[h, k] for k in range(E))
+        assert gate[i, h] == pytest.approx(O.softplus(ar + dt[h]) * ssm_a[h], rel=1e-12)
+        assert beta[i, h] == pytest.approx(1.0 / (1.0 + math.exp(-br)), rel=1e-12)
+    # the step fed with (log decay, beta) equals the step fed with the raw projections
+    sl, wts = _one_layer_inputs(52)
+    ar = (x[:1] @ wa.T).astype(np.float64)
+    br = (x[:1] @ wb.T).astype(np.float64)
+    raw = dict(sl, alpha=ar, beta=br)
+    wts = dict(wts, dt=dt, ssm_a=ssm_a)
+    y1, s1, _ = O.gdn_decode_slice(raw, wts)
+    g1, b1 = O.ab_gates(x[:1], wa, wb, dt, ssm_a)
+    y2, s2, _ = O.gdn_decode_slice(dict(sl, alpha=g1, beta=b1), wts, gates_ready=True)
+    assert np.allclose(y1, y2, rtol=1e-12, atol=1e-14) and np.allclose(s1, s2, rtol=1e-12, atol=1e-16)

@@ -43,11 +43,13 @@ V_HEADS = 48
 CONV_CHANNELS = 10240
 VALUE_DIM = 6144
 D_CONV = 4
+N_EMBD = 2560  # model width feeding the alpha/beta projections (their rows hold 2,560 elements)
 
 # Tensor ids mixed into every Philox key.
 _TID = {
     "qkv": 1, "z": 2, "alpha": 3, "beta": 4, "dt": 5, "ssm_a": 6,
     "conv_w": 7, "ssm_norm": 8, "conv_state": 9, "state": 10, "seq_len": 11,
+    "x": 12, "w_alpha": 13, "w_beta": 14,
 }
 
 
@@ -228,3 +230,54 @@ def device_inputs(w: Workload, device, threads: int = 16, batch_rows: tuple | No
     lens = seq_lens(w)
     t["seq_len"] = None if lens is None else torch.from_numpy(lens[b0:b1].copy()).to(device)
     return t
+
+
+# ---------------------------------------------------------------------------
+# Inputs of the fused alpha/beta projection: the layer input x ~ N(0, 1) per
+# token and BF16 weights ~ N(0, 1/sqrt(n_embd)) (so the raw projections are
+# about N(0, 1), like the raw alpha and beta of the decode workloads).
+# ---------------------------------------------------------------------------
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest BF16 (ties to even); returns the 16-bit patterns."""
+    u = np.ascontiguousarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def ab_weights(w: Workload, l: int, n_embd: int = N_EMBD) -> dict:
+    """BF16 alpha/beta projection weights of layer l: bit patterns [48][n_embd] and their float32 values."""
+    out = {}
+    for name in ("w_alpha", "w_beta"):
+        bits = to_bf16_bits(_normal(w.seed, name, (l,), (V_HEADS, n_embd), std=1.0 / math.sqrt(n_embd)))
+        out[name] = bits
+        out[name + "_f32"] = bf16_bits_to_float(bits)
+    return out
+
+
+def ab_x(w: Workload, b: int, l: int, n_embd: int = N_EMBD) -> np.ndarray:
+    """The layer input rows [T][n_embd] of (sequence b, layer l)."""
+    return _normal(w.seed, "x", (b, l), (w.T, n_embd))
+
+
+def host_ab_inputs(w: Workload, n_embd: int = N_EMBD) -> dict:
+    """x [B][L][T][n_embd], BF16 weights [L][48][n_embd] (bits and float32 values), dt and ssm_a [L][48]."""
+    B, L, T = w.B, w.L, w.T
+    x = np.empty((B, L, T, n_embd), np.float32)
+    for b in range(B):
+        for l in range(L):
+            x[b, l] = ab_x(w, b, l, n_embd)
+    wts = [ab_weights(w, l, n_embd) for l in range(L)]
+    lw = [layer_weights(w, l) for l in range(L)]
+    return {
+        "x": x,
+        "w_alpha": np.stack([d["w_alpha"] for d in wts]),
+        "w_beta": np.stack([d["w_beta"] for d in wts]),
+        "w_alpha_f32": np.stack([d["w_alpha_f32"] for d in wts]),
+        "w_beta_f32": np.stack([d["w_beta_f32"] for d in wts]),
+        "dt": np.stack([d["dt"] for d in lw]),
+        "ssm_a": np.stack([d["ssm_a"] for d in lw]),
+    }
