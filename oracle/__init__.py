@@ -39,7 +39,11 @@ its reason in the design notes):
 * conv taps: ``w[c][0]`` multiplies the oldest history entry and ``w[c][3]``
   the current input; the history is stored oldest first as ``[C][3]``;
 * state tile orientation ``S[i][j]``: i indexes k (rows), j indexes v
-  (columns), so ``kv = S^T k`` reduces over rows.
+  (columns), so ``kv = S^T k`` reduces over rows;
+* the input projections (``in_proj``) take dense BF16 weights and the float32
+  layer input unrounded: the pages' qkv and gate weights are quantized packs
+  that need trained values, and their BF16 path offers a float32-activation
+  form.
 
 Pinning. Every function here is pinned by ``tests/test_oracle_pins.py`` to
 closed forms, exact rational arithmetic on tiny cases, invariants the
@@ -145,6 +149,21 @@ def ab_gates(x, w_alpha, w_beta, dt, ssm_a):
     gate = softplus(alpha_raw + np.asarray(dt, np.float64)) * np.asarray(ssm_a, np.float64)
     return gate, sigmoid(beta_raw)
 
+
+
+def in_proj(x, w_qkv, w_gate):
+    """The mixer's two input projections of the layer input: qkv = w_qkv x, the
+    10240 conv channels q|k|v (gdn_layer step 2 on src/core/layer.cpp), and
+    z = w_gate x, the 6144-wide output gate (the start of gdn_layer step 7).
+
+    The weights are dense BF16 matrices [n_out][n_embd], passed as their exact
+    float values; ``x`` is [..., n_embd]. Returns (qkv, z) in float64, with no
+    rounding of x or of the products.
+    """
+    x = np.asarray(x, np.float64)
+    qkv = x @ np.asarray(w_qkv, np.float64).T
+    z = x @ np.asarray(w_gate, np.float64).T
+    return qkv, z
 
 # ---------------------------------------------------------------- step 6 --
 def delta_rule_step(S, k, q, v, beta, decay):

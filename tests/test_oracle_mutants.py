@@ -113,6 +113,21 @@ def _make_pre(normalize_v=False, scale_q=True, silu_qk_only=False):
     return pre
 
 
+def _proj_drop_last(x, w_qkv, w_gate):
+    x = np.asarray(x, np.float64)
+    return x[..., :-1] @ np.asarray(w_qkv)[:, :-1].T, x[..., :-1] @ np.asarray(w_gate)[:, :-1].T
+
+
+def _proj_rows_shifted(x, w_qkv, w_gate):
+    x = np.asarray(x, np.float64)
+    return x @ np.roll(np.asarray(w_qkv), 1, axis=0).T, x @ np.roll(np.asarray(w_gate), 1, axis=0).T
+
+
+def _proj_swapped(x, w_qkv, w_gate):
+    x = np.asarray(x, np.float64)
+    return x @ np.asarray(w_gate).T, x @ np.asarray(w_qkv).T
+
+
 MUTANTS = {
     "no decay": ("delta_rule_step", _step_no_decay),
     "sign of delta": ("delta_rule_step", _step_sign),
@@ -129,6 +144,9 @@ MUTANTS = {
     "v normalised": ("preprocess_token", None),
     "q not scaled": ("preprocess_token", None),
     "SiLU after split": ("preprocess_token", None),
+    "projection drops an input": ("in_proj", _proj_drop_last),
+    "projection rows shifted": ("in_proj", _proj_rows_shifted),
+    "projections swapped": ("in_proj", _proj_swapped),
 }
 
 

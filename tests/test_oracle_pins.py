@@ -420,3 +420,42 @@ def test_ab_gates_matches_scalar_sums_and_feeds_the_step():
     g1, b1 = O.ab_gates(x[:1], wa, wb, dt, ssm_a)
     y2, s2, _ = O.gdn_decode_slice(dict(sl, alpha=g1, beta=b1), wts, gates_ready=True)
     assert np.allclose(y1, y2, rtol=1e-12, atol=1e-14) and np.allclose(s1, s2, rtol=1e-12, atol=1e-16)
+
+
+# ------------------------------------------------ the input projections --
+def test_in_proj_one_hot_rows_select_and_scale_inputs():
+    """A weight row with one non-zero entry c picks x[c] times that entry: exact for
+    power-of-two entries, whatever the row order."""
+    r = _rng(60)
+    E = 40
+    x = r.standard_normal((2, E)).astype(np.float32)
+    cols_q, cols_g = r.permutation(E)[:9], r.permutation(E)[:5]
+    sq = np.array([1.0, -0.5, 0.125, 2.0, -1.0, 4.0, 0.25, -8.0, 1.0])
+    sg = np.array([-1.0, 0.5, 16.0, -0.0625, 1.0])
+    wq = np.zeros((9, E))
+    wq[np.arange(9), cols_q] = sq
+    wg = np.zeros((5, E))
+    wg[np.arange(5), cols_g] = sg
+    qkv, z = O.in_proj(x, wq, wg)
+    assert qkv.shape == (2, 9) and z.shape == (2, 5)
+    assert np.array_equal(qkv, x[:, cols_q].astype(np.float64) * sq)
+    assert np.array_equal(z, x[:, cols_g].astype(np.float64) * sg)
+
+
+def test_in_proj_equals_exact_rational_sums():
+    """On small dyadic inputs every product and partial sum is exact in float64, so the
+    projection must equal the rational dot product of each weight row with x exactly."""
+    from fractions import Fraction
+
+    r = _rng(61)
+    E, NQ, NZ, M = 11, 7, 4, 3
+    x = r.integers(-64, 64, (M, E)) / 16.0
+    wq = r.integers(-128, 128, (NQ, E)) / 64.0
+    wg = r.integers(-128, 128, (NZ, E)) / 64.0
+    qkv, z = O.in_proj(x, wq, wg)
+    assert qkv.shape == (M, NQ) and z.shape == (M, NZ)
+    for m in range(M):
+        for c in range(NQ):
+            assert qkv[m, c] == float(sum(Fraction(x[m, k]) * Fraction(wq[c, k]) for k in range(E)))
+        for c in range(NZ):
+            assert z[m, c] == float(sum(Fraction(x[m, k]) * Fraction(wg[c, k]) for k in range(E)))

@@ -50,3 +50,25 @@ def test_distributions():
     lens = W.seq_lens(W.WORKLOADS["verify_b16_l36_t8_ragged"])
     assert lens.min() >= 1 and lens.max() <= 8 and len(set(lens.tolist())) > 2
     assert W.seq_lens(w) is None
+
+
+def test_bf16_rounding_is_nearest_even_and_decodes_exactly():
+    vals = np.array([1.0, -2.0, 1 + 2**-8, 1 + 3 * 2**-8, 1 + 2**-8 + 2**-20, 3.140625, 0.0, -0.0], np.float32)
+    bits = W.to_bf16_bits(vals)
+    assert bits.tolist() == [0x3F80, 0xC000, 0x3F80, 0x3F82, 0x3F81, 0x4049, 0x0000, 0x8000]
+    back = W.bf16_bits_to_float(bits)
+    assert back.tolist() == [1.0, -2.0, 1.0, 1 + 2**-6, 1 + 2**-7, 3.140625, 0.0, -0.0]
+
+
+def test_projection_head_streams_are_independent_and_scaled():
+    w = W.WORKLOADS["decode_b1_l1_t1"]
+    a = W.proj_head_weights(w, "w_qkv", 0, 5, n_embd=256)
+    b = W.proj_head_weights(w, "w_qkv", 0, 6, n_embd=256)
+    g = W.proj_head_weights(w, "w_gate", 0, 5, n_embd=256)
+    assert a.shape == (128, 256) and a.dtype == np.uint16
+    assert not np.array_equal(a, b) and not np.array_equal(a, g)
+    full = W.proj_weights(w, 0, n_embd=256)
+    assert full["w_qkv"].shape == (10240, 256) and full["w_gate"].shape == (6144, 256)
+    assert np.array_equal(full["w_qkv"][640:768], a) and np.array_equal(full["w_gate"][640:768], g)
+    std = W.bf16_bits_to_float(full["w_qkv"]).std()
+    assert abs(std * 16.0 - 1.0) < 0.01

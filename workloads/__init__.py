@@ -49,7 +49,7 @@ N_EMBD = 2560  # model width feeding the alpha/beta projections (their rows hold
 _TID = {
     "qkv": 1, "z": 2, "alpha": 3, "beta": 4, "dt": 5, "ssm_a": 6,
     "conv_w": 7, "ssm_norm": 8, "conv_state": 9, "state": 10, "seq_len": 11,
-    "x": 12, "w_alpha": 13, "w_beta": 14,
+    "x": 12, "w_alpha": 13, "w_beta": 14, "w_qkv": 15, "w_gate": 16,
 }
 
 
@@ -280,4 +280,26 @@ def host_ab_inputs(w: Workload, n_embd: int = N_EMBD) -> dict:
         "w_beta_f32": np.stack([d["w_beta_f32"] for d in wts]),
         "dt": np.stack([d["dt"] for d in lw]),
         "ssm_a": np.stack([d["ssm_a"] for d in lw]),
+    }
+
+
+# ---------------------------------------------------------------------------
+# Weights of the two input projections (qkv: 10240 outputs, z: 6144 outputs)
+# as dense BF16 ~ N(0, 1/sqrt(n_embd)), so that qkv and z come out about
+# N(0, 1) like the decode workloads' qkv and z. The layer input x is ab_x.
+# ---------------------------------------------------------------------------
+def proj_head_weights(w: Workload, name: str, l: int, head: int, n_embd: int = N_EMBD) -> np.ndarray:
+    """BF16 bit patterns [128][n_embd] of the rows of one 128-wide output head of layer l.
+
+    ``name`` is "w_qkv" (80 heads: 16 q, 16 k, 48 v; rows 128 head .. 128 head + 127 of the
+    10240) or "w_gate" (48 heads of z). Each (layer, head) block is its own Philox stream.
+    """
+    return to_bf16_bits(_normal(w.seed, name, (l, head), (HEAD_DIM, n_embd), std=1.0 / math.sqrt(n_embd)))
+
+
+def proj_weights(w: Workload, l: int, n_embd: int = N_EMBD) -> dict:
+    """BF16 bit patterns of layer l's w_qkv [10240][n_embd] and w_gate [6144][n_embd]."""
+    return {
+        "w_qkv": np.concatenate([proj_head_weights(w, "w_qkv", l, h, n_embd) for h in range(CONV_CHANNELS // HEAD_DIM)]),
+        "w_gate": np.concatenate([proj_head_weights(w, "w_gate", l, h, n_embd) for h in range(VALUE_DIM // HEAD_DIM)]),
     }
