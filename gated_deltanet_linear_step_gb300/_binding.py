@@ -59,8 +59,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_verify_commit.argtypes = [_P] * 9 + [_I, _I, _I, _P]
         lib.gdn_decode_step_ex.argtypes = [_P] * 12 + [_I, _I, _I, ctypes.c_uint32, _P]
         lib.gdn_ab_gates.argtypes = [_P] * 7 + [_I, _I, _I, _I, _P]
+        lib.gdn_in_proj.argtypes = [_P] * 6 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
+        lib.gdn_in_proj_workspace_size.argtypes = [_I, _I, _I, _I]
+        lib.gdn_in_proj_workspace_size.restype = ctypes.c_size_t
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_get_geometry", "gdn_read_device_error"):
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_get_geometry",
+                   "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]
         lib.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -213,6 +217,38 @@ def gdn_ab_gates(x, w_alpha, w_beta, dt, ssm_a, gate, beta, stream=None):
     ]
     with torch.cuda.device(dev):
         _check(lib.gdn_ab_gates(*p, B, L, T, E, _stream_handle(stream, dev)))
+
+
+def gdn_in_proj_workspace_size(B: int, L: int, T: int, n_embd: int) -> int:
+    """Bytes of device workspace gdn_in_proj needs (0 for sizes out of range)."""
+    return int(load_library().gdn_in_proj_workspace_size(int(B), int(L), int(T), int(n_embd)))
+
+
+def gdn_in_proj(x, w_qkv, w_gate, qkv, z, workspace, stream=None):
+    """The qkv and z input projections on the tensor cores: qkv = w_qkv x ([B][L][T][10240])
+    and z = w_gate x ([B][L][T][6144]). The weights are [L][10240][n_embd] and
+    [L][6144][n_embd] BF16 (torch.bfloat16, or their bit patterns as int16/uint16);
+    ``workspace`` is a uint8 CUDA tensor of at least gdn_in_proj_workspace_size() bytes."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate)):
+        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
+        raise TypeError("workspace must be a 1-D torch.uint8 tensor")
+    p = [
+        _ptr(x, "x", (B, L, T, E), device=dev),
+        _ptr(w_qkv, "w_qkv", (L, CONV_CHANNELS, E), dtype=w_qkv.dtype, device=dev),
+        _ptr(w_gate, "w_gate", (L, VALUE_DIM, E), dtype=w_gate.dtype, device=dev),
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev),
+        _ptr(workspace, "workspace", tuple(workspace.shape), dtype=torch.uint8, device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_in_proj(*p, int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
 
 
 def gdn_get_geometry() -> dict:

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (gdn_api.cpp) and the CUDA kernels (gdn_step.cu).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -54,6 +55,31 @@ struct AbArgs {
     float* beta;
     int B, L, T, n_embd;
 };
+
+struct ProjArgs {
+    const float* x;
+    const uint16_t* w_qkv;
+    const uint16_t* w_gate;
+    float* qkv;
+    float* z;
+    void* workspace;
+    int B, L, T, n_embd;
+};
+
+// Blocking of the input projections: token blocks, rows per block (a multiple
+// of 16), 64-wide slices of n_embd, pipeline stages.
+struct ProjGeometry {
+    int n_tb, n_blk, n_ks, n_stages;
+};
+
+ProjGeometry proj_geometry(int B, int T, int n_embd);
+size_t proj_workspace_bytes(int B, int L, int T, int n_embd);
+
+// The split of x, then the tensor-core projection (gdn_proj.cu).
+cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream);
+
+// Reads and clears the projection kernel's device error word.
+cudaError_t read_proj_error(uint32_t* out);
 
 // The fused alpha/beta projections with their gate epilogue (gdn_ab.cu).
 cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream);

@@ -420,9 +420,11 @@ cudaError_t read_device_error(cudaStream_t stream, uint32_t* out) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
     if (e != cudaSuccess) return e;
-    uint32_t v1 = 0;
+    uint32_t v1 = 0, v2 = 0;
     e = read_t1_error(&v1);
-    *out = v | v1;
+    if (e != cudaSuccess) return e;
+    e = read_proj_error(&v2);
+    *out = v | v1 | v2;
     return e;
 }
 

@@ -41,6 +41,7 @@
 #ifndef GDN_H
 #define GDN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -166,6 +167,47 @@ gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alp
  */
 gdn_status gdn_ab_gates(const float* x, const uint16_t* w_alpha, const uint16_t* w_beta, const float* dt,
                         const float* ssm_a, float* gate, float* beta, int B, int L, int T, int n_embd, void* stream);
+
+/*
+ * gdn_in_proj_workspace_size - bytes of device workspace gdn_in_proj needs
+ * for these sizes (0 if they are out of range). It is about the size of x:
+ * L x ceil(B T / 128) blocks x (n_embd / 64) slices x 2 x rows x 128 bytes,
+ * rows = B T rounded up to a multiple of 16 (128 when B T > 128).
+ */
+size_t gdn_in_proj_workspace_size(int B, int L, int T, int n_embd);
+
+/*
+ * gdn_in_proj - the mixer's two input projections of the layer input x, on
+ * the tensor cores: qkv = w_qkv x, the 10240 conv channels q|k|v (gdn_layer
+ * step 2 on the page src/core/layer.cpp), and z = w_gate x, the 6144-wide
+ * output gate (the start of gdn_layer step 7). For every (b, l, t) row:
+ *
+ *   qkv[b][l][t][c] = sum_k w_qkv[l][c][k] * x[b][l][t][k]
+ *   z[b][l][t][c]   = sum_k w_gate[l][c][k] * x[b][l][t][k]
+ *
+ *   x          [B][L][T][n_embd] fp32 activations (input)
+ *   w_qkv      [L][10240][n_embd] BF16 bit patterns (uint16), dense (input)
+ *   w_gate     [L][6144][n_embd]  BF16 bit patterns, dense (input)
+ *   qkv        [B][L][T][10240] fp32 (output; the qkv input of the decode step)
+ *   z          [B][L][T][6144]  fp32 (output; the z input of the decode step)
+ *   workspace  device scratch of at least gdn_in_proj_workspace_size() bytes,
+ *              16-byte aligned, owned by the caller; overwritten (it holds x
+ *              split into two BF16 halves for the tensor cores)
+ *   n_embd: a positive multiple of 64, at most 65536.
+ *
+ * Precision: x is split as hi + lo, hi = x truncated to BF16 and lo = the
+ * remainder rounded to BF16; both halves are multiplied by the BF16 weights
+ * and summed in fp32, so each product carries x to within 2^-16 relative.
+ * The pages' own qkv and gate weights are quantized packs; this call takes
+ * dense BF16 weights instead.
+ *
+ * Same conventions as the calls above; the outputs and the workspace overlap
+ * nothing (GDN_ERR_ALIAS), and a workspace smaller than required gives
+ * GDN_ERR_SHAPE. Two kernels run on `stream`: the split of x, then the
+ * projection.
+ */
+gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
+                       void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);

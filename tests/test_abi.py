@@ -32,14 +32,14 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*|size_t)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-               "gdn_decode_step_ex", "gdn_ab_gates", "gdn_last_error", "gdn_get_geometry",
-               "gdn_read_device_error"):
+               "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_workspace_size",
+               "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
         assert fn in names
 
 
@@ -163,3 +163,33 @@ def test_ab_gates_argument_checks(lib):
     assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 4
     p = dict(ptr, x=ptr["x"] + 8)
     assert lib.gdn_ab_gates(*args(p), 2, 3, 1, E, None) == 3
+
+
+def test_in_proj_workspace_size(lib):
+    # L x token blocks x (n_embd / 64) slices x 2 halves x rows x 128 bytes
+    assert lib.gdn_in_proj_workspace_size(64, 36, 1, 2560) == 36 * 1 * 40 * 2 * 64 * 128
+    assert lib.gdn_in_proj_workspace_size(1, 1, 1, 64) == 1 * 1 * 1 * 2 * 16 * 128
+    assert lib.gdn_in_proj_workspace_size(16, 36, 8, 2560) == 36 * 1 * 40 * 2 * 128 * 128
+    assert lib.gdn_in_proj_workspace_size(200, 2, 1, 128) == 2 * 2 * 2 * 2 * 128 * 128
+    assert lib.gdn_in_proj_workspace_size(3, 2, 5, 128) == 2 * 1 * 2 * 2 * 16 * 128
+    assert lib.gdn_in_proj_workspace_size(0, 2, 5, 128) == 0
+    assert lib.gdn_in_proj_workspace_size(2, 2, 5, 100) == 0
+
+
+@no_gpu
+def test_in_proj_argument_checks(lib):
+    base = 1 << 41
+    E, B, L, T = 128, 2, 3, 1
+    ws = lib.gdn_in_proj_workspace_size(B, L, T, E)
+    ptr = {"x": base, "wq": base + (1 << 30), "wg": base + (2 << 30), "qkv": base + (3 << 30),
+           "z": base + (4 << 30), "ws": base + (5 << 30)}
+    args = lambda p: [p[k] for k in ("x", "wq", "wg", "qkv", "z", "ws")]  # noqa: E731
+    assert lib.gdn_in_proj(*args(ptr), ws, B, L, T, 100, None) == 2        # n_embd not a multiple of 64
+    assert lib.gdn_in_proj(*args(ptr), ws, 0, L, T, E, None) == 2
+    assert lib.gdn_in_proj(*args(ptr), ws - 16, B, L, T, E, None) == 2     # workspace too small
+    assert lib.gdn_in_proj(*args(dict(ptr, ws=None)), ws, B, L, T, E, None) == 1
+    assert lib.gdn_in_proj(*args(dict(ptr, wg=None)), ws, B, L, T, E, None) == 1
+    assert lib.gdn_in_proj(*args(dict(ptr, z=ptr["x"] + 64)), ws, B, L, T, E, None) == 4
+    assert lib.gdn_in_proj(*args(dict(ptr, z=ptr["qkv"] + 16)), ws, B, L, T, E, None) == 4
+    assert lib.gdn_in_proj(*args(dict(ptr, ws=ptr["wq"] + 32)), ws, B, L, T, E, None) == 4
+    assert lib.gdn_in_proj(*args(dict(ptr, qkv=ptr["qkv"] + 8)), ws, B, L, T, E, None) == 3

@@ -1,0 +1,171 @@
+"""GPU parity of the tensor-core input projections (qkv = w_qkv x, z = w_gate x)
+against the oracle, and of the mixer step fed by them end to end."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+# x is carried to within 2^-16 of its value (hi + lo halves), so the projection
+# errors sit far below the 1e-4 bar; x rounded to BF16 alone would give ~1e-3.
+SPLIT_TOL = 2e-5
+
+
+def _bf16(bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def _x(w, E):
+    return np.stack([np.stack([W.ab_x(w, b, l, E) for l in range(w.L)]) for b in range(w.B)])
+
+
+def _weights(w, E):
+    wts = [W.proj_weights(w, l, E) for l in range(w.L)]
+    return np.stack([d["w_qkv"] for d in wts]), np.stack([d["w_gate"] for d in wts])
+
+
+def _guarded(shape, dev, guard=4096):
+    """A NaN-filled buffer with `guard` floats on each side of the output view."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * guard,), float("nan"), device=dev)
+    return buf, buf[guard:guard + n].view(*shape), guard
+
+
+def _rows_rel_err(g, r):
+    g = g.reshape(-1, g.shape[-1]).astype(np.float64)
+    r = r.reshape(-1, r.shape[-1])
+    return float(np.max(np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)))
+
+
+def _oracle(x, wq, wg):
+    B, L, T, _ = x.shape
+    rq = np.empty((B, L, T, W.CONV_CHANNELS))
+    rz = np.empty((B, L, T, W.VALUE_DIM))
+    for l in range(L):
+        rq[:, l], rz[:, l] = oracle.in_proj(x[:, l], W.bf16_bits_to_float(wq[l]), W.bf16_bits_to_float(wg[l]))
+    return rq, rz
+
+
+@pytest.mark.parametrize("B,L,T,E", [
+    (3, 2, 5, 128),     # 15 tokens: one block of 16 rows, one padded row
+    (1, 1, 1, 64),      # a single token and a single 64-wide slice
+    (150, 1, 1, 64),    # two token blocks, the second ragged (22 of 128)
+    (7, 2, 37, 256),    # 259 tokens: three blocks, the last 3 tokens
+    (16, 1, 8, 2560),   # exactly 128 tokens, the model's n_embd
+    (64, 2, 1, 2560),   # the batched-decode token count
+])
+def test_in_proj_matches_oracle(cuda_device, B, L, T, E):
+    import gated_deltanet_linear_step_gb300 as g
+
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
+    x = _x(w, E)
+    wq, wg = _weights(w, E)
+    qbuf, qkv, gq = _guarded((B, L, T, W.CONV_CHANNELS), cuda_device)
+    zbuf, z, gz = _guarded((B, L, T, W.VALUE_DIM), cuda_device)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=cuda_device)
+    g.gdn_in_proj(torch.from_numpy(x).to(cuda_device), _bf16(wq, cuda_device), _bf16(wg, cuda_device), qkv, z, ws)
+    assert g.gdn_read_device_error() == 0
+    for buf, gd in ((qbuf, gq), (zbuf, gz)):
+        assert torch.isnan(buf[:gd]).all() and torch.isnan(buf[-gd:]).all(), "write outside the output"
+    gq_, gz_ = qkv.cpu().numpy(), z.cpu().numpy()
+    assert not np.isnan(gq_).any() and not np.isnan(gz_).any(), "an output element was not written"
+    rq, rz = _oracle(x, wq, wg)
+    eq, ez = _rows_rel_err(gq_, rq), _rows_rel_err(gz_, rz)
+    assert eq <= U.TOL and ez <= U.TOL, (eq, ez)
+    assert max(eq, ez) <= SPLIT_TOL, (eq, ez)
+
+
+def test_in_proj_is_deterministic(cuda_device):
+    import gated_deltanet_linear_step_gb300 as g
+
+    B, L, T, E = 5, 2, 3, 192
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
+    tx = torch.from_numpy(_x(w, E)).to(cuda_device)
+    wq, wg = (_bf16(a, cuda_device) for a in _weights(w, E))
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=cuda_device)
+    outs = []
+    for _ in range(2):
+        qkv = torch.empty((B, L, T, W.CONV_CHANNELS), device=cuda_device)
+        z = torch.empty((B, L, T, W.VALUE_DIM), device=cuda_device)
+        g.gdn_in_proj(tx, wq, wg, qkv, z, ws)
+        outs.append((qkv, z))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_in_proj_full_size_sampled(cuda_device):
+    """The bench launch (64 sequences x 36 layers x 1 token, n_embd 2560). Layers 0, 17
+    and 35 carry the seeded weights and are compared for sequences 0, 31 and 63; the
+    other layers get other random weights and only load the kernel."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    w = W.WORKLOADS["decode_b64_l36_t1"]
+    B, L, T, E = w.B, w.L, w.T, W.N_EMBD
+    x = _x(w, E)
+    gen = torch.Generator(device=cuda_device).manual_seed(7)
+    wq = (torch.randn((L, W.CONV_CHANNELS, E), device=cuda_device, generator=gen) * E ** -0.5).to(torch.bfloat16)
+    wg = (torch.randn((L, W.VALUE_DIM, E), device=cuda_device, generator=gen) * E ** -0.5).to(torch.bfloat16)
+    layers, seqs = (0, 17, 35), (0, 31, 63)
+    host = {}
+    for l in layers:
+        d = W.proj_weights(w, l, E)
+        host[l] = d
+        wq[l] = _bf16(d["w_qkv"], cuda_device)
+        wg[l] = _bf16(d["w_gate"], cuda_device)
+    qkv = torch.full((B, L, T, W.CONV_CHANNELS), float("nan"), device=cuda_device)
+    z = torch.full((B, L, T, W.VALUE_DIM), float("nan"), device=cuda_device)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=cuda_device)
+    g.gdn_in_proj(torch.from_numpy(x).to(cuda_device), wq, wg, qkv, z, ws)
+    assert g.gdn_read_device_error() == 0
+    assert not torch.isnan(qkv).any().item() and not torch.isnan(z).any().item()
+    for l in layers:
+        rq, rz = oracle.in_proj(x[list(seqs), l], W.bf16_bits_to_float(host[l]["w_qkv"]),
+                                W.bf16_bits_to_float(host[l]["w_gate"]))
+        gq_ = qkv[list(seqs), l].cpu().numpy()
+        gz_ = z[list(seqs), l].cpu().numpy()
+        assert _rows_rel_err(gq_, rq) <= SPLIT_TOL and _rows_rel_err(gz_, rz) <= SPLIT_TOL
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_mixer_step_fed_by_the_projections(cuda_device, T):
+    """x -> gdn_in_proj -> gdn_ab_gates -> gdn_decode_step_ex(GATES_READY) against the
+    oracle's chain in_proj -> ab_gates -> gdn_decode. The conv history then holds
+    projected values, which differ from the oracle's by the projection's rounding,
+    so it is compared within the tolerance rather than bit for bit."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    B, L, E = 2, 2, 256
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
+    h = W.host_inputs(w, threads=8)
+    ha = W.host_ab_inputs(w, E)
+    wq, wg = _weights(w, E)
+    t = U.to_device(h, cuda_device)
+    tx = torch.from_numpy(ha["x"]).to(cuda_device)
+    qkv = torch.empty(t["qkv"].shape, device=cuda_device)
+    z = torch.empty(t["z"].shape, device=cuda_device)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=cuda_device)
+    g.gdn_in_proj(tx, _bf16(wq, cuda_device), _bf16(wg, cuda_device), qkv, z, ws)
+    gate = torch.empty(t["alpha"].shape, device=cuda_device)
+    beta = torch.empty(t["beta"].shape, device=cuda_device)
+    g.gdn_ab_gates(tx, _bf16(ha["w_alpha"], cuda_device), _bf16(ha["w_beta"], cuda_device), t["dt"], t["ssm_a"],
+                   gate, beta)
+    y = torch.empty(t["z"].shape, device=cuda_device)
+    g.gdn_decode_step_ex(qkv, z, gate, beta, t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"], t["conv_state"],
+                         t["state"], y, flags=g.FLAG_GATES_READY)
+    assert g.gdn_read_device_error() == 0
+    rq, rz = _oracle(ha["x"], wq, wg)
+    rg = np.empty(h["alpha"].shape)
+    rb = np.empty(h["beta"].shape)
+    for l in range(L):
+        rg[:, l], rb[:, l] = oracle.ab_gates(ha["x"][:, l], ha["w_alpha_f32"][l], ha["w_beta_f32"][l], h["dt"][l],
+                                             h["ssm_a"][l])
+    ry, rs, rc = oracle.gdn_decode(rq, rz, rg, rb, h["dt"], h["ssm_a"], h["conv_w"], h["ssm_norm"], h["conv_state"],
+                                   h["state"], gates_ready=True)
+    assert U.y_errors(y.cpu().numpy(), ry) <= U.TOL
+    assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    gc = t["conv_state"].cpu().numpy().astype(np.float64)
+    assert float(np.abs(gc - rc).max() / np.abs(rc).max()) <= U.TOL
