@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers (default: the workload's L); smaller values are for profiling")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--timing", default="graph", choices=["graph", "direct"],
                     help="graph: the K timed steps are one captured CUDA graph (no host gaps between launches); "
@@ -567,6 +569,8 @@ def main():
     base = W.WORKLOADS[args.workload]
     if args.batch is not None:
         base = base.scaled(B=args.batch, name=f"{base.name}_b{args.batch}")
+    if args.layers is not None:
+        base = base.scaled(L=args.layers, name=f"{base.name}_l{args.layers}")
     w_global = base.scaled(B=base.B * world) if world > 1 else base
     if args.op == "ab_gates":
         if rank == 0:

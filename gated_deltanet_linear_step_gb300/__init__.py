@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     gdn_decode_step_varlen,
     gdn_get_geometry,
     gdn_in_proj,
+    gdn_in_proj_noalloc,
     gdn_in_proj_workspace_size,
     gdn_last_error,
     gdn_read_device_error,

@@ -60,10 +60,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_decode_step_ex.argtypes = [_P] * 12 + [_I, _I, _I, ctypes.c_uint32, _P]
         lib.gdn_ab_gates.argtypes = [_P] * 7 + [_I, _I, _I, _I, _P]
         lib.gdn_in_proj.argtypes = [_P] * 6 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
+        lib.gdn_in_proj_noalloc.argtypes = [_P] * 5 + [_I, _I, _I, _I, _P]
         lib.gdn_in_proj_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.gdn_in_proj_workspace_size.restype = ctypes.c_size_t
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_get_geometry",
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_get_geometry",
                    "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -249,6 +250,28 @@ def gdn_in_proj(x, w_qkv, w_gate, qkv, z, workspace, stream=None):
     ]
     with torch.cuda.device(dev):
         _check(lib.gdn_in_proj(*p, int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
+
+
+def gdn_in_proj_noalloc(x, w_qkv, w_gate, qkv, z, stream=None):
+    """gdn_in_proj with the split of x in the library's fixed 48 MiB scratch array instead of
+    a caller workspace; calls on one device must not overlap in time."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate)):
+        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    p = [
+        _ptr(x, "x", (B, L, T, E), device=dev),
+        _ptr(w_qkv, "w_qkv", (L, CONV_CHANNELS, E), dtype=w_qkv.dtype, device=dev),
+        _ptr(w_gate, "w_gate", (L, VALUE_DIM, E), dtype=w_gate.dtype, device=dev),
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_in_proj_noalloc(*p, B, L, T, E, _stream_handle(stream, dev)))
 
 
 def gdn_get_geometry() -> dict:

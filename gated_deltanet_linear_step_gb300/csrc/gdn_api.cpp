@@ -286,6 +286,59 @@ gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_
     return GDN_OK;
 }
 
+gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
+                               int B, int L, int T, int n_embd, void* stream) {
+    t_last_error.clear();
+    const char* fn = "gdn_in_proj_noalloc";
+    const struct {
+        const char* name;
+        const void* p;
+    } ptrs[] = {{"x", x}, {"w_qkv", w_qkv}, {"w_gate", w_gate}, {"qkv", qkv}, {"z", z}};
+    for (const auto& q : ptrs) {
+        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
+    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
+    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
+    const unsigned long long b = B, l = L, t = T, e = n_embd;
+    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
+    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
+    if (need > gdn::proj_static_scratch_bytes())
+        return fail(GDN_ERR_SHAPE, "%s: these sizes need %zu bytes of scratch, the library holds %zu", fn, need,
+                    gdn::proj_static_scratch_bytes());
+    const Span spans[] = {
+        {"x", x, b * l * t * e * 4, false},
+        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
+        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
+        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
+        {"z", z, b * l * t * gdn::kValueDim * 4, true},
+    };
+    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
+    for (int i = 0; i < n; ++i) {
+        if (!spans[i].output) continue;
+        for (int k = 0; k < n; ++k)
+            if (k != i && overlaps(spans[i], spans[k]))
+                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
+    }
+    gdn::ProjArgs a;
+    a.x = x;
+    a.w_qkv = w_qkv;
+    a.w_gate = w_gate;
+    a.qkv = qkv;
+    a.z = z;
+    a.workspace = nullptr;
+    a.B = B;
+    a.L = L;
+    a.T = T;
+    a.n_embd = n_embd;
+    const cudaError_t err = gdn::launch_in_proj_static(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
+    return GDN_OK;
+}
+
 const char* gdn_last_error(void) { return t_last_error.c_str(); }
 
 gdn_status gdn_get_geometry(int32_t out[8]) {

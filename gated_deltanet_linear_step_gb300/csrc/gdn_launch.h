@@ -78,6 +78,12 @@ size_t proj_workspace_bytes(int B, int L, int T, int n_embd);
 // The split of x, then the tensor-core projection (gdn_proj.cu).
 cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream);
 
+// launch_in_proj with the workspace in the library's static scratch array
+// (gdn_proj_noalloc.cu); the caller checks the size against
+// proj_static_scratch_bytes().
+cudaError_t launch_in_proj_static(const ProjArgs& a, cudaStream_t stream);
+size_t proj_static_scratch_bytes();
+
 // Reads and clears the projection kernel's device error word.
 cudaError_t read_proj_error(uint32_t* out);
 

@@ -209,6 +209,23 @@ size_t gdn_in_proj_workspace_size(int B, int L, int T, int n_embd);
 gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                        void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream);
 
+/*
+ * gdn_in_proj_noalloc - gdn_in_proj without a caller workspace: the split of
+ * x goes to a fixed 48 MiB scratch array compiled into the library, one per
+ * device, so the call needs no allocation by anyone. The Winery-Strata pages
+ * have no counterpart to this call; it is a convenience of this library.
+ *
+ * Arguments, layouts and results are those of gdn_in_proj. Sizes whose
+ * workspace (gdn_in_proj_workspace_size) exceeds 48 MiB give GDN_ERR_SHAPE.
+ * Every call of this function on a device shares the one scratch array, so
+ * calls must not overlap in time: issue them on one stream, or synchronise
+ * between the streams that issue them. The other conventions above hold,
+ * except that nothing is stated here about capturing this call in a CUDA
+ * graph.
+ */
+gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
+                               int B, int L, int T, int n_embd, void* stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);
 
