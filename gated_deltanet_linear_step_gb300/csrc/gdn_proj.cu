@@ -8,13 +8,15 @@
 // weight matrix (16384 x n_embd BF16, 84 MB at n_embd 2560) is read once, so the
 // weight stream from HBM bounds it. Weight rows become the MMA's M side (128
 // output channels per tile) and tokens its N side; the accumulator lives in
-// tensor memory, one lane per output channel and one column per token.
+// tensor memory, one lane per output channel and one column per token and half.
 //
 // Precision. kind::f16 multiplies BF16 by BF16. The weights are BF16 already;
 // x is split as x = hi + lo with hi = x truncated to BF16 and lo = the
-// remainder rounded to BF16, and both halves are multiplied into the same
-// accumulator, so every product carries x to within 2^-16 of its value and the
-// sums stay fp32.
+// remainder rounded to BF16, so every product carries x to within 2^-16 of its
+// value. The lo rows follow the hi rows on the MMA's N side: one MMA of
+// N = 2 x tokens per K step multiplies the weight slice by both halves (the
+// weights are read from shared memory once), and the epilogue adds column j
+// and column tokens + j. Sums stay fp32.
 //
 // Two kernels:
 // * gdn_x_split_kernel writes hi and lo of every (layer, token block, 64-wide
@@ -24,9 +26,10 @@
 //     warp 0 lane 0  - producer: per stage, the weight slice [128][64] by TMA
 //                      (tensor map, 128-byte swizzle, evict-first) and the
 //                      split x blocks by one bulk copy, both on one mbarrier;
-//     warp 1         - allocates 256 tensor-memory columns (two accumulators);
-//                      lane 0 issues tcgen05.mma (M 128, N = token block, K 16)
-//                      and commits each stage back to its producer;
+//     warp 1         - allocates all 512 tensor-memory columns (two
+//                      accumulators of up to 256); lane 0 issues tcgen05.mma
+//                      (M 128, N = 2 x token block, K 16) and commits each
+//                      stage back to its producer;
 //     warps 2-5      - epilogue: tcgen05.ld of the accumulator, 32 tokens at a
 //                      time, and coalesced fp32 stores of the outputs.
 //   The epilogue of one tile overlaps the next tile's main loop through the
@@ -58,7 +61,7 @@ constexpr int kChTiles = kQkvTiles + kGateTiles;
 constexpr int kProjThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kWBytes = kBM * kBK * 2;    // 16384
-constexpr uint32_t kAccCols = 128;             // columns per accumulator
+constexpr uint32_t kAccCols = 2 * kMaxTok;     // columns per accumulator: hi tokens, then lo tokens
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr size_t kStageBudget = 200 * 1024;
 constexpr size_t kBarBytes = 256;
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
     } else if (warp == 1) {
         if (lane == 0) {
             // ----------------------------------------------- MMA issuer --
-            const uint32_t idesc = mma_idesc(n_blk);
+            const uint32_t idesc = mma_idesc(2 * n_blk);  // the hi rows, then the lo rows
             uint32_t it = 0, local = 0;
             uint32_t last_bar = 0, last_par = 0;
             bool issued = false;
@@ -332,14 +335,12 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
                     tc_fence_after();
                     const uint32_t st = base + s * stage_bytes;
                     const uint64_t wd = sw128_desc(st);
-                    const uint64_t hd = sw128_desc(st + kWBytes);
-                    const uint64_t ld = sw128_desc(st + kWBytes + static_cast<uint32_t>(n_blk) * 128u);
+                    const uint64_t xd = sw128_desc(st + kWBytes);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         // K advances 16 BF16 = 32 bytes inside the swizzled row: +2 in the descriptor's address field.
                         const uint64_t dk = static_cast<uint64_t>(2 * kk);
-                        mma_bf16(d_tmem, wd + dk, hd + dk, idesc, (ks | kk) != 0 ? 1u : 0u);
-                        mma_bf16(d_tmem, wd + dk, ld + dk, idesc, 1u);
+                        mma_bf16(d_tmem, wd + dk, xd + dk, idesc, (ks | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(empty_bar(s));
                     last_bar = empty_bar(s);
@@ -385,15 +386,17 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(a) * kAccCols;
             for (int j0 = 0; j0 < P; j0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr + static_cast<uint32_t>(j0), v);
+                uint32_t hi[32], lo[32];
+                tmem_ld32(taddr + static_cast<uint32_t>(j0), hi);
+                tmem_ld32(taddr + static_cast<uint32_t>(n_blk + j0), lo);
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = j0 + jj;
                     if (j < P) {
                         const int m = m0 + j;
                         const int sb = m / p.T, t = m - (m / p.T) * p.T;
-                        out[((static_cast<size_t>(sb) * p.L + l) * p.T + t) * width + ch] = __uint_as_float(v[jj]);
+                        out[((static_cast<size_t>(sb) * p.L + l) * p.T + t) * width + ch] =
+                            __uint_as_float(hi[jj]) + __uint_as_float(lo[jj]);
                     }
                 }
             }
