@@ -56,9 +56,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
-    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj"],
+    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj", "step_inputs"],
                     help="step: the decode step (the default bench line); ab_gates: the fused alpha/beta projection; "
-                         "in_proj: the qkv and z input projections on the tensor cores")
+                         "in_proj: the qkv and z input projections on the tensor cores; step_inputs: qkv, z and "
+                         "the alpha/beta gates in one tensor-core pass")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
@@ -493,8 +494,9 @@ def run_ab_gates(args, w):
     }), flush=True)
 
 
-def run_in_proj(args, w):
-    """Times the qkv and z input projections (x split + tensor-core GEMM) on the workload's shape."""
+def run_in_proj(args, w, with_ab=False):
+    """Times the qkv and z input projections (x split + tensor-core GEMM) on the workload's shape;
+    with_ab: also the alpha/beta projections with the gate epilogue (gdn_step_inputs)."""
     from concurrent.futures import ThreadPoolExecutor
 
     import gated_deltanet_linear_step_gb300 as g
@@ -518,9 +520,20 @@ def run_in_proj(args, w):
     qkv = torch.empty((B, L, T, W.CONV_CHANNELS), device=dev)
     z = torch.empty((B, L, T, W.VALUE_DIM), device=dev)
     ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=dev)
+    if with_ab:
+        h = W.host_ab_inputs(w, E)
+        wa = torch.from_numpy(h["w_alpha"].view(np.int16)).to(dev).view(torch.bfloat16)
+        wb = torch.from_numpy(h["w_beta"].view(np.int16)).to(dev).view(torch.bfloat16)
+        dt = torch.from_numpy(h["dt"]).to(dev)
+        sa = torch.from_numpy(h["ssm_a"]).to(dev)
+        gate = torch.empty((B, L, T, 48), device=dev)
+        beta = torch.empty_like(gate)
 
     def step():
-        g.gdn_in_proj(x, wq, wg, qkv, z, ws)
+        if with_ab:
+            g.gdn_step_inputs(x, wq, wg, wa, wb, dt, sa, qkv, z, gate, beta, ws)
+        else:
+            g.gdn_in_proj(x, wq, wg, qkv, z, ws)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -540,13 +553,14 @@ def run_in_proj(args, w):
     assert g.gdn_read_device_error(device=dev) == 0, "the kernel reported a device error"
     ms = a.elapsed_time(b) / args.steps
     rows = B * L * T
-    n_out = W.CONV_CHANNELS + W.VALUE_DIM
-    byts = L * n_out * E * 2 + rows * E * 4 + rows * n_out * 4
+    n_out = W.CONV_CHANNELS + W.VALUE_DIM + (2 * 48 if with_ab else 0)
+    byts = L * n_out * E * 2 + rows * E * 4 + rows * n_out * 4 + (L * 2 * 48 * 4 if with_ab else 0)
     flops = 2.0 * rows * n_out * E
     peak, peak_kind = measured_peaks()
     achieved = byts / (ms / 1e3) / 1e9
     print(json.dumps({
-        "metric": "qkv + z input projections, rows (seq*layer*token) per second", "op": "in_proj",
+        "metric": ("qkv + z + alpha/beta gate projections" if with_ab else "qkv + z input projections")
+                  + ", rows (seq*layer*token) per second", "op": "step_inputs" if with_ab else "in_proj",
         "value": rows / (ms / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16 x (bf16 hi + lo of f32), f32 accumulate",
         "data": "synthetic",
@@ -575,9 +589,9 @@ def main():
     if args.op == "ab_gates":
         if rank == 0:
             run_ab_gates(args, base)
-    elif args.op == "in_proj":
+    elif args.op in ("in_proj", "step_inputs"):
         if rank == 0:
-            run_in_proj(args, base)
+            run_in_proj(args, base, with_ab=args.op == "step_inputs")
     elif args.impl == "reference":
         run_reference(args, base, world, rank)
     else:

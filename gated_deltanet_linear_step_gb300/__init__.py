@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     gdn_in_proj_workspace_size,
     gdn_last_error,
     gdn_read_device_error,
+    gdn_step_inputs,
     gdn_verify_commit,
     gdn_verify_window,
     load_library,

@@ -61,10 +61,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_ab_gates.argtypes = [_P] * 7 + [_I, _I, _I, _I, _P]
         lib.gdn_in_proj.argtypes = [_P] * 6 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
         lib.gdn_in_proj_noalloc.argtypes = [_P] * 5 + [_I, _I, _I, _I, _P]
+        lib.gdn_step_inputs.argtypes = [_P] * 12 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
         lib.gdn_in_proj_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.gdn_in_proj_workspace_size.restype = ctypes.c_size_t
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_get_geometry",
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_get_geometry",
                    "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -250,6 +251,38 @@ def gdn_in_proj(x, w_qkv, w_gate, qkv, z, workspace, stream=None):
     ]
     with torch.cuda.device(dev):
         _check(lib.gdn_in_proj(*p, int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
+
+
+def gdn_step_inputs(x, w_qkv, w_gate, w_alpha, w_beta, dt, ssm_a, qkv, z, gate, beta, workspace, stream=None):
+    """All four decode-step inputs from the layer input on the tensor cores: qkv and z as
+    gdn_in_proj, gate (log decay) and beta as gdn_ab_gates. Weights are BF16 (torch.bfloat16,
+    or their 16-bit patterns); ``workspace`` as for gdn_in_proj."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate), ("w_alpha", w_alpha), ("w_beta", w_beta)):
+        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
+        raise TypeError("workspace must be a 1-D torch.uint8 tensor")
+    p = [
+        _ptr(x, "x", (B, L, T, E), device=dev),
+        _ptr(w_qkv, "w_qkv", (L, CONV_CHANNELS, E), dtype=w_qkv.dtype, device=dev),
+        _ptr(w_gate, "w_gate", (L, VALUE_DIM, E), dtype=w_gate.dtype, device=dev),
+        _ptr(w_alpha, "w_alpha", (L, V_HEADS, E), dtype=w_alpha.dtype, device=dev),
+        _ptr(w_beta, "w_beta", (L, V_HEADS, E), dtype=w_beta.dtype, device=dev),
+        _ptr(dt, "dt", (L, V_HEADS), device=dev),
+        _ptr(ssm_a, "ssm_a", (L, V_HEADS), device=dev),
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev),
+        _ptr(gate, "gate", (B, L, T, V_HEADS), device=dev),
+        _ptr(beta, "beta", (B, L, T, V_HEADS), device=dev),
+        _ptr(workspace, "workspace", tuple(workspace.shape), dtype=torch.uint8, device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_step_inputs(*p, int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
 
 
 def gdn_in_proj_noalloc(x, w_qkv, w_gate, qkv, z, stream=None):

@@ -286,6 +286,75 @@ gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_
     return GDN_OK;
 }
 
+gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, const uint16_t* w_alpha,
+                           const uint16_t* w_beta, const float* dt, const float* ssm_a, float* qkv, float* z,
+                           float* gate, float* beta, void* workspace, size_t workspace_bytes, int B, int L, int T,
+                           int n_embd, void* stream) {
+    t_last_error.clear();
+    const char* fn = "gdn_step_inputs";
+    const struct {
+        const char* name;
+        const void* p;
+    } ptrs[] = {{"x", x},     {"w_qkv", w_qkv}, {"w_gate", w_gate}, {"w_alpha", w_alpha},      {"w_beta", w_beta},
+                {"dt", dt},   {"ssm_a", ssm_a}, {"qkv", qkv},       {"z", z},                  {"gate", gate},
+                {"beta", beta}, {"workspace", workspace}};
+    for (const auto& q : ptrs) {
+        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
+    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
+    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
+    const unsigned long long b = B, l = L, t = T, e = n_embd;
+    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
+    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
+    const Span spans[] = {
+        {"x", x, b * l * t * e * 4, false},
+        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
+        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
+        {"w_alpha", w_alpha, l * gdn::kVHeads * e * 2, false},
+        {"w_beta", w_beta, l * gdn::kVHeads * e * 2, false},
+        {"dt", dt, l * gdn::kVHeads * 4, false},
+        {"ssm_a", ssm_a, l * gdn::kVHeads * 4, false},
+        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
+        {"z", z, b * l * t * gdn::kValueDim * 4, true},
+        {"gate", gate, b * l * t * gdn::kVHeads * 4, true},
+        {"beta", beta, b * l * t * gdn::kVHeads * 4, true},
+        {"workspace", workspace, need, true},
+    };
+    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
+    for (int i = 0; i < n; ++i) {
+        if (!spans[i].output) continue;
+        for (int k = 0; k < n; ++k)
+            if (k != i && overlaps(spans[i], spans[k]))
+                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
+    }
+    gdn::ProjArgs a;
+    a.x = x;
+    a.w_qkv = w_qkv;
+    a.w_gate = w_gate;
+    a.qkv = qkv;
+    a.z = z;
+    a.workspace = workspace;
+    a.B = B;
+    a.L = L;
+    a.T = T;
+    a.n_embd = n_embd;
+    a.w_alpha = w_alpha;
+    a.w_beta = w_beta;
+    a.dt = dt;
+    a.ssm_a = ssm_a;
+    a.gate = gate;
+    a.beta = beta;
+    const cudaError_t err = gdn::launch_in_proj(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
+    return GDN_OK;
+}
+
 gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                                int B, int L, int T, int n_embd, void* stream) {
     t_last_error.clear();

@@ -64,6 +64,13 @@ struct ProjArgs {
     float* z;
     void* workspace;
     int B, L, T, n_embd;
+    // Optional (all NULL, or all set): the alpha/beta projections with the gate epilogue.
+    const uint16_t* w_alpha = nullptr;
+    const uint16_t* w_beta = nullptr;
+    const float* dt = nullptr;
+    const float* ssm_a = nullptr;
+    float* gate = nullptr;
+    float* beta = nullptr;
 };
 
 // Blocking of the input projections: token blocks, rows per block (a multiple

@@ -18,6 +18,13 @@
 // weights are read from shared memory once), and the epilogue adds column j
 // and column tokens + j. Sums stay fp32.
 //
+// With the alpha/beta weights given, every layer gets one more tile: the 48
+// alpha rows and the 48 beta rows (two TMA boxes) as the MMA's rows 0-95, with
+// the gate epilogue of fused_gdn_ab (gdn_layer step 5): gate = softplus(alpha
+// + dt) * ssm_a, the log of the decay, and beta = sigmoid(beta_raw). Rows
+// 96-127 of that tile hold whatever the stage held before; each accumulator
+// lane depends on its own row only, and those lanes are not stored.
+//
 // Two kernels:
 // * gdn_x_split_kernel writes hi and lo of every (layer, token block, 64-wide
 //   slice of n_embd) as two [N][64] BF16 blocks, already in the 128-byte
@@ -44,6 +51,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "gdn_device.cuh"
@@ -57,7 +65,8 @@ constexpr int kBK = 64;                        // n_embd elements per stage: one
 constexpr int kMaxTok = 128;                   // tokens per block (MMA N <= 128)
 constexpr int kQkvTiles = kConvChannels / kBM;  // 80
 constexpr int kGateTiles = kValueDim / kBM;     // 48
-constexpr int kChTiles = kQkvTiles + kGateTiles;
+constexpr int kChTiles = kQkvTiles + kGateTiles;  // 128; the alpha/beta tile is number 128
+constexpr int kAbRows = kVHeads;                   // 48 alpha rows, then 48 beta rows
 constexpr int kProjThreads = 192;
 constexpr int kMaxStages = 8;
 constexpr uint32_t kWBytes = kBM * kBK * 2;    // 16384
@@ -70,8 +79,15 @@ constexpr size_t kProjSmem = kStageBudget + kBarBytes + 1024;  // + alignment sl
 __device__ unsigned int g_proj_error = 0;
 
 struct ProjParams {
-    CUtensorMap tm_qkv;   // [L * 10240][E] BF16, box 64 x 128, 128-byte swizzle
-    CUtensorMap tm_gate;  // [L * 6144][E]
+    CUtensorMap tm_qkv;    // [L * 10240][E] BF16, box 64 x 128, 128-byte swizzle
+    CUtensorMap tm_gate;   // [L * 6144][E]
+    CUtensorMap tm_alpha;  // [L * 48][E], box 64 x 48 (used when n_ct is 129)
+    CUtensorMap tm_beta;   // [L * 48][E]
+    const float* dt;       // [L][48]
+    const float* ssm_a;    // [L][48]
+    float* gate;           // [B][L][T][48]
+    float* beta;           // [B][L][T][48]
+    int n_ct;              // channel tiles per layer: 128, or 129 with the alpha/beta tile
     const uint16_t* xs;   // split x: [L][n_tb][n_ks][2][n_blk][64] BF16, swizzled
     float* qkv;           // [B][L][T][10240]
     float* z;             // [B][L][T][6144]
@@ -266,6 +282,10 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
         fence_mbar_init();
         prefetch_tensormap(&p.tm_qkv);
         prefetch_tensormap(&p.tm_gate);
+        if (p.n_ct > kChTiles) {
+            prefetch_tensormap(&p.tm_alpha);
+            prefetch_tensormap(&p.tm_beta);
+        }
     }
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tc_fence_before();
@@ -279,10 +299,11 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
             const uint64_t pol = evict_first_policy();
             uint32_t it = 0;
             for (long long tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
-                const int ct = static_cast<int>(tile % kChTiles);
-                const long long rest = tile / kChTiles;
+                const int ct = static_cast<int>(tile % p.n_ct);
+                const long long rest = tile / p.n_ct;
                 const int tb = static_cast<int>(rest % p.n_tb);
                 const int l = static_cast<int>(rest / p.n_tb);
+                const bool is_ab = ct == kChTiles;
                 const bool is_qkv = ct < kQkvTiles;
                 const CUtensorMap* tm = is_qkv ? &p.tm_qkv : &p.tm_gate;
                 const int row = is_qkv ? l * kConvChannels + ct * kBM : l * kValueDim + (ct - kQkvTiles) * kBM;
@@ -297,8 +318,14 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
                         break;
                     }
                     const uint32_t st = base + s * stage_bytes;
-                    mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-                    tma_load_2d(st, tm, ks * kBK, row, full_bar(s), pol);
+                    if (is_ab) {
+                        mbar_arrive_expect_tx(full_bar(s), 2u * kAbRows * 128u + x_bytes);
+                        tma_load_2d(st, &p.tm_alpha, ks * kBK, l * kAbRows, full_bar(s), pol);
+                        tma_load_2d(st + kAbRows * 128u, &p.tm_beta, ks * kBK, l * kAbRows, full_bar(s), pol);
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(s), stage_bytes);
+                        tma_load_2d(st, tm, ks * kBK, row, full_bar(s), pol);
+                    }
                     bulk_load(st + kWBytes, xsrc + static_cast<size_t>(ks) * x_bytes, x_bytes, full_bar(s));
                     ++it;
                 }
@@ -365,22 +392,39 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
         for (long long tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++local) {
             const int a = static_cast<int>(local & 1u);
             const uint32_t aph = (local >> 1) & 1u;
-            const int ct = static_cast<int>(tile % kChTiles);
-            const long long rest = tile / kChTiles;
+            const int ct = static_cast<int>(tile % p.n_ct);
+            const long long rest = tile / p.n_ct;
             const int tb = static_cast<int>(rest % p.n_tb);
             const int l = static_cast<int>(rest / p.n_tb);
             const int m0 = tb * kMaxTok;
             const int P = min(kMaxTok, M - m0);
+            // Output of this lane: a qkv or z channel, or in the alpha/beta tile a
+            // gate (lanes 0-47) or beta (lanes 48-95) head; lanes 96-127 store nothing.
             float* out;
             int width, ch;
+            int kind = 0;  // 0: plain, 1: gate, 2: beta, 3: none
+            float dt = 0.f, sa = 0.f;
             if (ct < kQkvTiles) {
                 out = p.qkv;
                 width = kConvChannels;
                 ch = ct * kBM + chan;
-            } else {
+            } else if (ct < kChTiles) {
                 out = p.z;
                 width = kValueDim;
                 ch = (ct - kQkvTiles) * kBM + chan;
+            } else {
+                width = kVHeads;
+                if (chan < kAbRows) {
+                    kind = 1;
+                    out = p.gate;
+                    ch = chan;
+                    dt = __ldg(p.dt + static_cast<size_t>(l) * kVHeads + ch);
+                    sa = __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + ch);
+                } else {
+                    kind = chan < 2 * kAbRows ? 2 : 3;
+                    out = p.beta;
+                    ch = chan < 2 * kAbRows ? chan - kAbRows : 0;
+                }
             }
             if (!wait_or_abort(accf_bar(a), aph, abort_flag)) break;
             tc_fence_after();
@@ -392,11 +436,13 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = j0 + jj;
-                    if (j < P) {
+                    if (j < P && kind != 3) {
                         const int m = m0 + j;
                         const int sb = m / p.T, t = m - (m / p.T) * p.T;
-                        out[((static_cast<size_t>(sb) * p.L + l) * p.T + t) * width + ch] =
-                            __uint_as_float(hi[jj]) + __uint_as_float(lo[jj]);
+                        float v = __uint_as_float(hi[jj]) + __uint_as_float(lo[jj]);
+                        if (kind == 1) v = softplusf_(v + dt) * sa;
+                        else if (kind == 2) v = sigmoidf_(v);
+                        out[((static_cast<size_t>(sb) * p.L + l) * p.T + t) * width + ch] = v;
                     }
                 }
             }
@@ -447,10 +493,10 @@ cudaError_t setup(int dev, int* sms) {
     return cudaSuccess;
 }
 
-cudaError_t encode_weights(CUtensorMap* tm, const uint16_t* w, long long rows, int E) {
+cudaError_t encode_weights(CUtensorMap* tm, const uint16_t* w, long long rows, int E, int box_rows) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(E), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(E) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(w), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -505,10 +551,23 @@ cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
 
     ProjParams p;
-    e = encode_weights(&p.tm_qkv, a.w_qkv, static_cast<long long>(a.L) * kConvChannels, a.n_embd);
+    memset(&p, 0, sizeof(p));
+    e = encode_weights(&p.tm_qkv, a.w_qkv, static_cast<long long>(a.L) * kConvChannels, a.n_embd, kBM);
     if (e != cudaSuccess) return e;
-    e = encode_weights(&p.tm_gate, a.w_gate, static_cast<long long>(a.L) * kValueDim, a.n_embd);
+    e = encode_weights(&p.tm_gate, a.w_gate, static_cast<long long>(a.L) * kValueDim, a.n_embd, kBM);
     if (e != cudaSuccess) return e;
+    p.n_ct = kChTiles;
+    if (a.w_alpha != nullptr) {
+        e = encode_weights(&p.tm_alpha, a.w_alpha, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
+        if (e != cudaSuccess) return e;
+        e = encode_weights(&p.tm_beta, a.w_beta, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
+        if (e != cudaSuccess) return e;
+        p.dt = a.dt;
+        p.ssm_a = a.ssm_a;
+        p.gate = a.gate;
+        p.beta = a.beta;
+        p.n_ct = kChTiles + 1;
+    }
     p.xs = sp.xs;
     p.qkv = a.qkv;
     p.z = a.z;
@@ -519,7 +578,7 @@ cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream) {
     p.n_blk = g.n_blk;
     p.n_tb = g.n_tb;
     p.n_stages = g.n_stages;
-    p.n_tiles = static_cast<long long>(a.L) * g.n_tb * kChTiles;
+    p.n_tiles = static_cast<long long>(a.L) * g.n_tb * p.n_ct;
     const long long grid = p.n_tiles < sms ? p.n_tiles : sms;
     gdn_in_proj_kernel<<<static_cast<unsigned>(grid), kProjThreads, kProjSmem, stream>>>(p);
     return cudaGetLastError();

@@ -210,6 +210,28 @@ gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_
                        void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream);
 
 /*
+ * gdn_step_inputs - all four inputs of the decode step from the layer input
+ * x in one pass of the tensor cores: qkv and z as gdn_in_proj computes them,
+ * and gate and beta as gdn_ab_gates computes them (fused_gdn_ab in gdn_layer
+ * step 5 on the page src/core/layer.cpp), with the alpha/beta rows as one
+ * more 128-row tile per layer of the same kernel.
+ *
+ *   w_alpha, w_beta  [L][48][n_embd] BF16 bit patterns (input)
+ *   dt, ssm_a        [L][48] (input)
+ *   gate, beta       [B][L][T][48] (outputs; feed gdn_decode_step_ex with
+ *                    GDN_FLAG_GATES_READY)
+ *   the other arguments as gdn_in_proj; the workspace size is
+ *   gdn_in_proj_workspace_size().
+ *
+ * The alpha and beta sums use the same hi + lo split of x as qkv and z.
+ * Same conventions as gdn_in_proj; no output overlaps any other buffer.
+ */
+gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, const uint16_t* w_alpha,
+                           const uint16_t* w_beta, const float* dt, const float* ssm_a, float* qkv, float* z,
+                           float* gate, float* beta, void* workspace, size_t workspace_bytes, int B, int L, int T,
+                           int n_embd, void* stream);
+
+/*
  * gdn_in_proj_noalloc - gdn_in_proj without a caller workspace: the split of
  * x goes to a fixed 48 MiB scratch array compiled into the library, one per
  * device, so the call needs no allocation by anyone. The Winery-Strata pages

@@ -39,6 +39,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
                "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_workspace_size",
+               "gdn_in_proj_noalloc", "gdn_step_inputs",
                "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
         assert fn in names
 
@@ -193,3 +194,21 @@ def test_in_proj_argument_checks(lib):
     assert lib.gdn_in_proj(*args(dict(ptr, z=ptr["qkv"] + 16)), ws, B, L, T, E, None) == 4
     assert lib.gdn_in_proj(*args(dict(ptr, ws=ptr["wq"] + 32)), ws, B, L, T, E, None) == 4
     assert lib.gdn_in_proj(*args(dict(ptr, qkv=ptr["qkv"] + 8)), ws, B, L, T, E, None) == 3
+
+
+@no_gpu
+def test_step_inputs_argument_checks(lib):
+    base = 1 << 41
+    E, B, L, T = 128, 2, 3, 1
+    ws = lib.gdn_in_proj_workspace_size(B, L, T, E)
+    keys = ("x", "wq", "wg", "wa", "wb", "dt", "sa", "qkv", "z", "gate", "beta", "ws")
+    ptr = {k: base + (i << 32) for i, k in enumerate(keys)}
+    args = lambda p: [p[k] for k in keys]  # noqa: E731
+    assert lib.gdn_step_inputs(*args(ptr), ws, B, L, T, 100, None) == 2
+    assert lib.gdn_step_inputs(*args(ptr), ws - 16, B, L, T, E, None) == 2
+    for k in keys:
+        assert lib.gdn_step_inputs(*args(dict(ptr, **{k: None})), ws, B, L, T, E, None) == 1, k
+        assert lib.gdn_step_inputs(*args(dict(ptr, **{k: ptr[k] + 4})), ws, B, L, T, E, None) == 3, k
+    assert lib.gdn_step_inputs(*args(dict(ptr, gate=ptr["beta"] + 16)), ws, B, L, T, E, None) == 4
+    assert lib.gdn_step_inputs(*args(dict(ptr, beta=ptr["wa"] + 64)), ws, B, L, T, E, None) == 4
+    assert lib.gdn_step_inputs(*args(dict(ptr, ws=ptr["qkv"] + 64)), ws, B, L, T, E, None) == 4

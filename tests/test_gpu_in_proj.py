@@ -130,11 +130,45 @@ def test_in_proj_full_size_sampled(cuda_device):
         assert _rows_rel_err(gq_, rq) <= SPLIT_TOL and _rows_rel_err(gz_, rz) <= SPLIT_TOL
 
 
-@pytest.mark.parametrize("T", [1, 3])
-def test_mixer_step_fed_by_the_projections(cuda_device, T):
-    """x -> gdn_in_proj -> gdn_ab_gates -> gdn_decode_step_ex(GATES_READY) against the
-    oracle's chain in_proj -> ab_gates -> gdn_decode. The conv history then holds
-    projected values, which differ from the oracle's by the projection's rounding,
+@pytest.mark.parametrize("B,L,T,E", [(3, 2, 5, 128), (150, 1, 1, 64), (16, 1, 8, 2560), (64, 2, 1, 2560)])
+def test_step_inputs_match_oracle(cuda_device, B, L, T, E):
+    """gdn_step_inputs: qkv and z as the oracle's in_proj, gate and beta as its ab_gates."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
+    x = _x(w, E)
+    wq, wg = _weights(w, E)
+    ha = W.host_ab_inputs(w, E)
+    d = cuda_device
+    outs = {}
+    bufs = {}
+    for name, width in (("qkv", W.CONV_CHANNELS), ("z", W.VALUE_DIM), ("gate", 48), ("beta", 48)):
+        bufs[name], outs[name], gd = _guarded((B, L, T, width), d)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=d)
+    g.gdn_step_inputs(torch.from_numpy(x).to(d), _bf16(wq, d), _bf16(wg, d), _bf16(ha["w_alpha"], d),
+                      _bf16(ha["w_beta"], d), torch.from_numpy(ha["dt"]).to(d), torch.from_numpy(ha["ssm_a"]).to(d),
+                      outs["qkv"], outs["z"], outs["gate"], outs["beta"], ws)
+    assert g.gdn_read_device_error() == 0
+    for name in outs:
+        assert torch.isnan(bufs[name][:gd]).all() and torch.isnan(bufs[name][-gd:]).all(), name
+        assert not torch.isnan(outs[name]).any().item(), name
+    rq, rz = _oracle(x, wq, wg)
+    assert _rows_rel_err(outs["qkv"].cpu().numpy(), rq) <= SPLIT_TOL
+    assert _rows_rel_err(outs["z"].cpu().numpy(), rz) <= SPLIT_TOL
+    rg = np.empty((B, L, T, 48))
+    rb = np.empty((B, L, T, 48))
+    for l in range(L):
+        rg[:, l], rb[:, l] = oracle.ab_gates(x[:, l], ha["w_alpha_f32"][l], ha["w_beta_f32"][l], ha["dt"][l],
+                                             ha["ssm_a"][l])
+    assert _rows_rel_err(outs["gate"].cpu().numpy(), rg) <= U.TOL
+    assert _rows_rel_err(outs["beta"].cpu().numpy(), rb) <= U.TOL
+
+
+@pytest.mark.parametrize("T,fused", [(1, False), (3, False), (1, True), (3, True)])
+def test_mixer_step_fed_by_the_projections(cuda_device, T, fused):
+    """x -> gdn_in_proj + gdn_ab_gates (or gdn_step_inputs) -> gdn_decode_step_ex(GATES_READY)
+    against the oracle's chain in_proj -> ab_gates -> gdn_decode. The conv history then
+    holds projected values, which differ from the oracle's by the projection's rounding,
     so it is compared within the tolerance rather than bit for bit."""
     import gated_deltanet_linear_step_gb300 as g
 
@@ -148,11 +182,15 @@ def test_mixer_step_fed_by_the_projections(cuda_device, T):
     qkv = torch.empty(t["qkv"].shape, device=cuda_device)
     z = torch.empty(t["z"].shape, device=cuda_device)
     ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=cuda_device)
-    g.gdn_in_proj(tx, _bf16(wq, cuda_device), _bf16(wg, cuda_device), qkv, z, ws)
     gate = torch.empty(t["alpha"].shape, device=cuda_device)
     beta = torch.empty(t["beta"].shape, device=cuda_device)
-    g.gdn_ab_gates(tx, _bf16(ha["w_alpha"], cuda_device), _bf16(ha["w_beta"], cuda_device), t["dt"], t["ssm_a"],
-                   gate, beta)
+    wa, wb = _bf16(ha["w_alpha"], cuda_device), _bf16(ha["w_beta"], cuda_device)
+    if fused:
+        g.gdn_step_inputs(tx, _bf16(wq, cuda_device), _bf16(wg, cuda_device), wa, wb, t["dt"], t["ssm_a"], qkv, z,
+                          gate, beta, ws)
+    else:
+        g.gdn_in_proj(tx, _bf16(wq, cuda_device), _bf16(wg, cuda_device), qkv, z, ws)
+        g.gdn_ab_gates(tx, wa, wb, t["dt"], t["ssm_a"], gate, beta)
     y = torch.empty(t["z"].shape, device=cuda_device)
     g.gdn_decode_step_ex(qkv, z, gate, beta, t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"], t["conv_state"],
                          t["state"], y, flags=g.FLAG_GATES_READY)
