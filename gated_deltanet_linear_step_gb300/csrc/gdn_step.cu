@@ -63,7 +63,7 @@ constexpr int kRecQ = 0;
 constexpr int kRecK = kS;
 constexpr int kRecV = 2 * kS;          // v, then o
 constexpr int kRecZ = 3 * kS;          // z of the CTA's head, by bulk copy
-constexpr int kRecG = 4 * kS;          // beta, decay, pad
+constexpr int kRecG = 4 * kS;          // beta, decay, 1 / decay, pad
 constexpr int kRecFloats = kRecG + 8;  // 520 floats = 2080 bytes
 
 constexpr size_t kOffRecs = kTileBytes;
@@ -141,6 +141,87 @@ __device__ __forceinline__ void store_history(const Params& p, long long bl, int
     cs[2] = hist[2];
 }
 
+// The same step with the decay deferred into a per-tile scale: the tile is
+// S = P s, so S *= decay only scales P, and the update is s += k (d / P)^T
+// (three FP32 operations per element instead of four). invP tracks 1/P from
+// the per-token 1/decay, so no division sits between the two passes. When P
+// falls below 2^-64 (decay underflow included) s is rescaled to S and P
+// restarts at 1; the branch is uniform over the CTA, which holds one tile.
+// Returns o = S_new^T q.
+constexpr float kDeferMin = 5.421010862427522e-20f;  // 2^-64
+
+__device__ __forceinline__ float4 delta_step_octet_deferred(float (&s)[64], float& P, float& invP, const float* qv,
+                                                            const float* kv, const Octet& q, float4 v4, float beta,
+                                                            float decay, float inv_decay) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            a0 = fmaf(s[i + 0], kk[e], a0);
+            a1 = fmaf(s[i + 1], kk[e], a1);
+            a2 = fmaf(s[i + 2], kk[e], a2);
+            a3 = fmaf(s[i + 3], kk[e], a3);
+        }
+    }
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
+        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
+        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
+        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
+    }
+    const float pn = P * decay;  // S_old * decay = pn * s
+    float d0 = beta * (v4.x - pn * a0);
+    float d1 = beta * (v4.y - pn * a1);
+    float d2 = beta * (v4.z - pn * a2);
+    float d3 = beta * (v4.w - pn * a3);
+    if (pn < kDeferMin) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[i] *= pn;
+        P = 1.0f;
+        invP = 1.0f;
+    } else {
+        P = pn;
+        invP *= inv_decay;
+        d0 *= invP;
+        d1 *= invP;
+        d2 *= invP;
+        d3 *= invP;
+    }
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; r += 4) {
+        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
+        const float4 q4 = *reinterpret_cast<const float4*>(qv + q.row0 + r);
+        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = 4 * (r + e);
+            s[i + 0] = fmaf(kk[e], d0, s[i + 0]);
+            s[i + 1] = fmaf(kk[e], d1, s[i + 1]);
+            s[i + 2] = fmaf(kk[e], d2, s[i + 2]);
+            s[i + 3] = fmaf(kk[e], d3, s[i + 3]);
+            o0 = fmaf(s[i + 0], qq[e], o0);
+            o1 = fmaf(s[i + 1], qq[e], o1);
+            o2 = fmaf(s[i + 2], qq[e], o2);
+            o3 = fmaf(s[i + 3], qq[e], o3);
+        }
+    }
+#pragma unroll
+    for (int m = 4; m <= 16; m <<= 1) {
+        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
+        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
+        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
+        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
+    }
+    return make_float4(P * o0, P * o1, P * o2, P * o3);
+}
+
 __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float* tile = reinterpret_cast<float*>(smem);
@@ -180,6 +261,8 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
     }
     tile_pending = cid < p.n_units;
     float s[64];
+    float scale = 1.0f;  // the tile in registers is scale * s
+    float inv_scale = 1.0f;
 
     for (long long u = cid; u < p.n_units; u += n_clusters) {
         const long long bl = u / kKHeads;
@@ -224,6 +307,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                                    __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
                         rec[t * kRecFloats + kRecG + 0] = bt;
                         rec[t * kRecFloats + kRecG + 1] = dc;
+                        rec[t * kRecFloats + kRecG + 2] = 1.0f / dc;
                     }
                 }
             }
@@ -251,6 +335,8 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                     tile_par ^= 1u;
                     tile_pending = false;
                     if (n > 0) tile_load_octet(s, tile, oc);
+                    scale = 1.0f;
+                    inv_scale = 1.0f;
                 }
             }
 
@@ -260,7 +346,9 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                     float* r = rec + t * kRecFloats;
                     float* vo = r + kRecV + oc.col0;
                     const float4 v4 = *reinterpret_cast<const float4*>(vo);
-                    const float4 o4 = delta_step_octet(s, r + kRecQ, r + kRecK, oc, v4, r[kRecG], r[kRecG + 1]);
+                    const float4 o4 =
+                        delta_step_octet_deferred(s, scale, inv_scale, r + kRecQ, r + kRecK, oc, v4, r[kRecG],
+                                                  r[kRecG + 1], r[kRecG + 2]);
                     __syncwarp();
                     if (oc.rb == 0) *reinterpret_cast<float4*>(vo) = o4;
                 }
@@ -269,6 +357,8 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             // ---- after the last token the tile returns through its slot
             const bool store_tile = last_chunk && write_state && !failed;
             if (store_tile) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) s[i] *= scale;
                 tile_save_octet(s, tile, oc);
                 fence_proxy_async_smem();
             }
