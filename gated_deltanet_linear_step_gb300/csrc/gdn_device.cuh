@@ -1,7 +1,8 @@
 // gdn_device.cuh - device-side pieces shared by the decode-step kernels:
 // inline PTX for mbarriers, bulk async copies and clusters, bounded waits,
-// warp reductions, the scalar activations of the GDN step, and the two forms of
-// the gated delta rule (tile in shared memory, tile in registers).
+// warp reductions, the scalar activations of the GDN step, the gated delta rule
+// on a tile in shared memory, and the register mapping of a tile held by a
+// 256-thread CTA (its step lives with the multi-token kernel).
 #pragma once
 
 #include <cstdint>
@@ -119,11 +120,6 @@ __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wai
 
 // Waits until all of this thread's committed cp.async groups have landed.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// Pulls [src, src + bytes) into L2 without waiting (16-byte aligned, 16-byte multiple).
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -331,34 +327,6 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
     return r;
 }
 
-// Arrives on an mbarrier of another CTA of the cluster, releasing this thread's
-// earlier memory accesses (and those it has observed) at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait_bounded with acquire at cluster scope (arrivals come from other CTAs).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    for (;;) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
 // ------------------------------------------------------------------------
 // The state tile in registers, 64 values per thread ("octet" mapping) for a
 // 256-thread CTA that owns one 128x128 tile. Lane 4 rb + qd of warp w holds
@@ -397,67 +365,6 @@ __device__ __forceinline__ void tile_save_octet(const float (&s)[64], float* til
     for (int r = 0; r < 16; ++r)
         *reinterpret_cast<float4*>(tile + (q.row0 + r) * kHeadDim + q.col0) =
             make_float4(s[4 * r + 0], s[4 * r + 1], s[4 * r + 2], s[4 * r + 3]);
-}
-
-// The gated delta rule on the thread's 16x4 block, with the same two passes as
-// delta_step_smem (pass 1: a = S^T k and d; pass 2: S += k d^T after the
-// decay, o = S_new^T q), the block in registers, and 16-row partial sums
-// reduced over the 8 row blocks of the warp.
-__device__ __forceinline__ float4 delta_step_octet(float (&s)[64], const float* qv, const float* kv, const Octet& q,
-                                                   float4 v4, float beta, float decay) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int r = 0; r < 16; r += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 4 * (r + e);
-            a0 = fmaf(s[i + 0], kk[e], a0);
-            a1 = fmaf(s[i + 1], kk[e], a1);
-            a2 = fmaf(s[i + 2], kk[e], a2);
-            a3 = fmaf(s[i + 3], kk[e], a3);
-        }
-    }
-#pragma unroll
-    for (int m = 4; m <= 16; m <<= 1) {
-        a0 += __shfl_xor_sync(0xffffffffu, a0, m);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, m);
-        a2 += __shfl_xor_sync(0xffffffffu, a2, m);
-        a3 += __shfl_xor_sync(0xffffffffu, a3, m);
-    }
-    const float d0 = beta * (v4.x - decay * a0);
-    const float d1 = beta * (v4.y - decay * a1);
-    const float d2 = beta * (v4.z - decay * a2);
-    const float d3 = beta * (v4.w - decay * a3);
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-#pragma unroll
-    for (int r = 0; r < 16; r += 4) {
-        const float4 k4 = *reinterpret_cast<const float4*>(kv + q.row0 + r);
-        const float4 q4 = *reinterpret_cast<const float4*>(qv + q.row0 + r);
-        const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-        const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = 4 * (r + e);
-            s[i + 0] = fmaf(kk[e], d0, decay * s[i + 0]);
-            s[i + 1] = fmaf(kk[e], d1, decay * s[i + 1]);
-            s[i + 2] = fmaf(kk[e], d2, decay * s[i + 2]);
-            s[i + 3] = fmaf(kk[e], d3, decay * s[i + 3]);
-            o0 = fmaf(s[i + 0], qq[e], o0);
-            o1 = fmaf(s[i + 1], qq[e], o1);
-            o2 = fmaf(s[i + 2], qq[e], o2);
-            o3 = fmaf(s[i + 3], qq[e], o3);
-        }
-    }
-#pragma unroll
-    for (int m = 4; m <= 16; m <<= 1) {
-        o0 += __shfl_xor_sync(0xffffffffu, o0, m);
-        o1 += __shfl_xor_sync(0xffffffffu, o1, m);
-        o2 += __shfl_xor_sync(0xffffffffu, o2, m);
-        o3 += __shfl_xor_sync(0xffffffffu, o3, m);
-    }
-    return make_float4(o0, o1, o2, o3);
 }
 
 }  // namespace gdn

@@ -141,9 +141,12 @@ __device__ __forceinline__ void store_history(const Params& p, long long bl, int
     cs[2] = hist[2];
 }
 
-// The same step with the decay deferred into a per-tile scale: the tile is
-// S = P s, so S *= decay only scales P, and the update is s += k (d / P)^T
-// (three FP32 operations per element instead of four). invP tracks 1/P from
+// The gated delta rule on the thread's 16x4 block of the tile in registers
+// (octet mapping), with two passes: a = S^T k, then the update and o = S_new^T q,
+// 16-row partial sums reduced over the warp's 8 row blocks. The decay is
+// deferred into a per-tile scale: the tile is S = P s, so S *= decay only
+// scales P, and the update is s += k (d / P)^T (three FP32 operations per
+// element instead of four). invP tracks 1/P from
 // the per-token 1/decay, so no division sits between the two passes. When P
 // falls below 2^-64 (decay underflow included) s is rescaled to S and P
 // restarts at 1; the branch is uniform over the CTA, which holds one tile.

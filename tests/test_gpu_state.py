@@ -26,7 +26,8 @@ def test_every_v_head_of_a_k_head_sees_the_old_conv_history(cuda_device, T):
     t = U.to_device(h, cuda_device)
     y = U.run_step(g, t)
     assert g.gdn_read_device_error() == 0
-    ry, rs, rc = U.oracle_full(h)
+    with np.errstate(over="ignore"):  # SiLU of conv outputs near -1e4: exp overflows to inf, the limit is exact
+        ry, rs, rc = U.oracle_full(h)
     gy = y.cpu().numpy()
     for vh in range(48):  # every v head on its own, all three of each k head
         sl = slice(vh * 128, (vh + 1) * 128)
