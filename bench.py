@@ -378,9 +378,9 @@ def run_gdn(args, w_global, world, rank, local):
     max_ms = max_over_ranks(elapsed_ms, world, dev)
     value = total_updates / (max_ms / 1000.0)
 
-    # end to end through the public API: every step's activations come from pinned host
-    # memory and its y goes back to it; the copies of neighbouring steps overlap the
-    # step's kernel on separate streams (HostDecodePipeline).
+    # end to end through the C ABI with host buffers: every step's activations come from
+    # pinned host memory and its y goes back to it (gdn_host_pipeline_*); the copies of
+    # neighbouring steps overlap the step's kernel on separate streams.
     e2e = None
     if not args.no_e2e:
         from gated_deltanet_linear_step_gb300.host_pipeline import HostDecodePipeline
@@ -404,7 +404,8 @@ def run_gdn(args, w_global, world, rank, local):
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1000.0, world, dev)
         e2e = {"value": total_updates / (e2e_ms / 1000.0), "unit": UNIT, "h2d_bytes_per_step": pipe.in_bytes,
                "d2h_bytes_per_step": pipe.out_bytes,
-               "method": "wall clock over K steps; copies of neighbouring steps overlap the kernel on separate streams"}
+               "method": "wall clock over K steps through the C-ABI host pipeline (gdn_host_pipeline_submit with "
+                         "pinned host buffers); copies of neighbouring steps overlap the kernel on separate streams"}
         del pipe
 
     # roofline of the (only) kernel

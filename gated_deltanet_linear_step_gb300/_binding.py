@@ -63,9 +63,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_in_proj_noalloc.argtypes = [_P] * 5 + [_I, _I, _I, _I, _P]
         lib.gdn_step_inputs.argtypes = [_P] * 12 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
         lib.gdn_in_proj_workspace_size.argtypes = [_I, _I, _I, _I]
+        lib.gdn_host_pipeline_slot_bytes.argtypes = [_I, _I, _I]
+        lib.gdn_host_pipeline_slot_bytes.restype = ctypes.c_size_t
+        lib.gdn_host_pipeline_create.argtypes = [ctypes.POINTER(ctypes.c_void_p)] + [_P] * 8 + [ctypes.c_size_t, _I,
+                                                                                               _I, _I, _I]
+        lib.gdn_host_pipeline_submit.argtypes = [_P] * 6
+        lib.gdn_host_pipeline_synchronize.argtypes = [_P]
+        lib.gdn_host_pipeline_destroy.argtypes = [_P]
+        lib.gdn_host_pipeline_destroy.restype = None
         lib.gdn_in_proj_workspace_size.restype = ctypes.c_size_t
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_get_geometry",
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_host_pipeline_create",
+                   "gdn_host_pipeline_submit", "gdn_host_pipeline_synchronize", "gdn_get_geometry",
                    "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.gdn_get_geometry.argtypes = [ctypes.POINTER(ctypes.c_int32)]

@@ -131,6 +131,15 @@ gdn_status run(const float* qkv, const float* z, const float* alpha, const float
 
 }  // namespace
 
+namespace gdn {
+// Status reporting for the other host files of the ABI: records the message
+// gdn_last_error() returns on this thread (an empty message clears it).
+gdn_status report_status(gdn_status s, const char* msg) {
+    t_last_error = msg;
+    return s;
+}
+}  // namespace gdn
+
 extern "C" {
 
 gdn_status gdn_decode_step(const float* qkv, const float* z, const float* alpha, const float* beta,

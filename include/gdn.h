@@ -248,6 +248,45 @@ gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t
 gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                                int B, int L, int T, int n_embd, void* stream);
 
+/*
+ * Host-fed decode steps with overlapped copies. A pipeline runs
+ * gdn_decode_step (or its varlen form when seq_len is given) on activations
+ * that live in HOST memory: each gdn_host_pipeline_submit queues the copies of
+ * one step's qkv, z, alpha and beta to the device, the step, and the copy of
+ * its y back to the host. Two device slots alternate and three streams carry
+ * the three stages, ordered by events, so step k + 1's inputs and step
+ * k - 1's y move while step k computes. Steps run in submission order and
+ * update state and conv_state in place, as direct calls would. The pages have
+ * no counterpart to this part of the library.
+ *
+ * gdn_host_pipeline_slot_bytes: device bytes the two slots need (0 if the
+ *   sizes are out of range).
+ * gdn_host_pipeline_create: dt, ssm_a, conv_w, ssm_norm, conv_state, state
+ *   and seq_len (may be NULL; DEVICE int32 [B]) as for gdn_decode_step, all
+ *   on `device` and kept by the pipeline until destroy; slots is caller-owned
+ *   device memory of at least gdn_host_pipeline_slot_bytes(), 256-byte
+ *   aligned. Creates the streams and events; *out receives the pipeline.
+ * gdn_host_pipeline_submit: HOST pointers to one step's qkv [B][L][T][10240],
+ *   z [B][L][T][6144], alpha and beta [B][L][T][48] (inputs) and y
+ *   [B][L][T][6144] (output). Returns once the work is queued; the host
+ *   buffers must stay untouched until gdn_host_pipeline_synchronize returns.
+ *   Page-locked (pinned) host memory lets the copies overlap the kernels.
+ * gdn_host_pipeline_synchronize: waits for everything submitted.
+ * gdn_host_pipeline_destroy: waits, then frees the streams, events and the
+ *   pipeline (not the caller's buffers).
+ */
+typedef struct gdn_host_pipeline gdn_host_pipeline;
+
+size_t gdn_host_pipeline_slot_bytes(int B, int L, int T);
+gdn_status gdn_host_pipeline_create(gdn_host_pipeline** out, const float* dt, const float* ssm_a,
+                                    const float* conv_w, const float* ssm_norm, float* conv_state, float* state,
+                                    const int32_t* seq_len, void* slots, size_t slots_bytes, int B, int L, int T,
+                                    int device);
+gdn_status gdn_host_pipeline_submit(gdn_host_pipeline* p, const float* qkv, const float* z, const float* alpha,
+                                    const float* beta, float* y);
+gdn_status gdn_host_pipeline_synchronize(gdn_host_pipeline* p);
+void gdn_host_pipeline_destroy(gdn_host_pipeline* p);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char* gdn_last_error(void);
 

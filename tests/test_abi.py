@@ -32,7 +32,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*|size_t)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*|size_t|void)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -212,3 +212,27 @@ def test_step_inputs_argument_checks(lib):
     assert lib.gdn_step_inputs(*args(dict(ptr, gate=ptr["beta"] + 16)), ws, B, L, T, E, None) == 4
     assert lib.gdn_step_inputs(*args(dict(ptr, beta=ptr["wa"] + 64)), ws, B, L, T, E, None) == 4
     assert lib.gdn_step_inputs(*args(dict(ptr, ws=ptr["qkv"] + 64)), ws, B, L, T, E, None) == 4
+
+
+@no_gpu
+def test_host_pipeline_argument_checks(lib):
+    import ctypes
+
+    base = 1 << 41
+    B, L, T = 2, 3, 1
+    n = lib.gdn_host_pipeline_slot_bytes(B, L, T)
+    assert n > 0 and lib.gdn_host_pipeline_slot_bytes(0, L, T) == 0
+    dev = [base + (i << 32) for i in range(6)]  # dt, ssm_a, conv_w, ssm_norm, conv_state, state
+    slots = base + (7 << 32)
+    h = ctypes.c_void_p()
+    assert lib.gdn_host_pipeline_create(None, *dev, None, slots, n, B, L, T, 0) == 1
+    assert lib.gdn_host_pipeline_create(ctypes.byref(h), *dev[:5], None, None, slots, n, B, L, T, 0) == 1
+    assert lib.gdn_host_pipeline_create(ctypes.byref(h), *dev, None, slots + 16, n, B, L, T, 0) == 3
+    assert lib.gdn_host_pipeline_create(ctypes.byref(h), *dev, base + 2, slots, n, B, L, T, 0) == 3
+    assert lib.gdn_host_pipeline_create(ctypes.byref(h), *dev, None, slots, n - 256, B, L, T, 0) == 2
+    assert lib.gdn_host_pipeline_create(ctypes.byref(h), *dev, None, slots, n, B, L, 0, 0) == 2
+    assert b"slots" in lib.gdn_last_error() or b"range" in lib.gdn_last_error()
+    assert h.value is None
+    assert lib.gdn_host_pipeline_submit(None, base, base, base, base, base) == 1
+    assert lib.gdn_host_pipeline_synchronize(None) == 1
+    lib.gdn_host_pipeline_destroy(None)
