@@ -56,10 +56,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
-    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj", "step_inputs"],
+    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj", "step_inputs", "mixer"],
                     help="step: the decode step (the default bench line); ab_gates: the fused alpha/beta projection; "
                          "in_proj: the qkv and z input projections on the tensor cores; step_inputs: qkv, z and "
-                         "the alpha/beta gates in one tensor-core pass")
+                         "the alpha/beta gates in one tensor-core pass; mixer: step_inputs then the decode step "
+                         "on its outputs, from the layer input x to y")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
@@ -588,6 +589,78 @@ def run_in_proj(args, w, with_ab=False):
     }), flush=True)
 
 
+def run_mixer(args, w):
+    """Times the mixer from the layer input to y: gdn_step_inputs (qkv, z and the gates on the
+    tensor cores) then gdn_decode_step_ex with GDN_FLAG_GATES_READY, K steps in one graph."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import gated_deltanet_linear_step_gb300 as g
+
+    g.load_library()
+    dev = torch.device("cuda", 0)
+    E = W.N_EMBD
+    B, L, T = w.B, w.L, w.T
+    t = W.device_inputs(w, dev, threads=16)
+    h = W.host_ab_inputs(w, E)
+    x = torch.from_numpy(h["x"]).to(dev)
+    wa = torch.from_numpy(h["w_alpha"].view(np.int16)).to(dev).view(torch.bfloat16)
+    wb = torch.from_numpy(h["w_beta"].view(np.int16)).to(dev).view(torch.bfloat16)
+    wq = torch.empty((L, W.CONV_CHANNELS, E), dtype=torch.bfloat16, device=dev)
+    wg = torch.empty((L, W.VALUE_DIM, E), dtype=torch.bfloat16, device=dev)
+    with ThreadPoolExecutor(16) as ex:
+        for l, d in ex.map(lambda l: (l, W.proj_weights(w, l, E)), range(L)):
+            wq[l] = torch.from_numpy(d["w_qkv"].view(np.int16)).view(torch.bfloat16).to(dev)
+            wg[l] = torch.from_numpy(d["w_gate"].view(np.int16)).view(torch.bfloat16).to(dev)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=dev)
+    gate = torch.empty(t["alpha"].shape, device=dev)
+    beta = torch.empty(t["beta"].shape, device=dev)
+    y = torch.empty(t["z"].shape, device=dev)
+
+    def step():
+        g.gdn_step_inputs(x, wq, wg, wa, wb, t["dt"], t["ssm_a"], t["qkv"], t["z"], gate, beta, ws)
+        g.gdn_decode_step_ex(t["qkv"], t["z"], gate, beta, t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"],
+                             t["conv_state"], t["state"], y, seq_len=t["seq_len"], flags=g.FLAG_GATES_READY)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clocks:
+        clocks.mark_start()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+    assert g.gdn_read_device_error(device=dev) == 0, "a kernel reported a device error"
+    ms = a.elapsed_time(b) / args.steps
+    lens = W.seq_lens(w)
+    updates = valid_tokens(w, lens)
+    rows = B * L * T
+    n_out = W.CONV_CHANNELS + W.VALUE_DIM + 2 * W.V_HEADS
+    proj_bytes = L * n_out * E * 2 + rows * E * 4 + rows * n_out * 4
+    step_bytes = algorithmic_bytes(w, lens)["total"]
+    peak, peak_kind = measured_peaks()
+    gbs = (proj_bytes + step_bytes) / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "mixer steps from the layer input x to y (projections + decode step), state-updates/s",
+        "op": "mixer", "value": updates / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 (bf16 weights)",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "L": L, "T": T, "n_embd": E,
+                   "timing": f"{args.steps} x (gdn_step_inputs + gdn_decode_step_ex) in one captured CUDA graph"},
+        "clocks": clocks.summary(), "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": peak_kind, "bytes_per_step": proj_bytes + step_bytes,
+                     "note": "the projections' bytes (weights, x, qkv/z/gate/beta written) plus the decode "
+                             "step's algorithmic bytes; qkv and z cross HBM twice between the two calls"},
+    }), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -605,6 +678,9 @@ def main():
     elif args.op in ("in_proj", "step_inputs"):
         if rank == 0:
             run_in_proj(args, base, with_ab=args.op == "step_inputs")
+    elif args.op == "mixer":
+        if rank == 0:
+            run_mixer(args, base)
     elif args.impl == "reference":
         run_reference(args, base, world, rank)
     else:
