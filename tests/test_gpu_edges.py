@@ -1,0 +1,69 @@
+"""Edge cases of the decode step on the GPU: the longest window, lengths that are
+negative, zero for every sequence, or zero in a single-token call."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from tests import parity_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(B, L, T, name="verify_b16_l36_t8_ragged"):
+    w = W.WORKLOADS[name].scaled(B=B, L=L, T=T)
+    return w, W.host_inputs(w, threads=8)
+
+
+def test_longest_window_matches_oracle(cuda_device):
+    """T at its maximum (1024 tokens, 64 chunks of the multi-token kernel) against the oracle."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    T = g.gdn_get_geometry()["max_t"]
+    w, h = _case(1, 1, T, name="decode_b1_l36_t64_zero_state")
+    t = U.to_device(h, cuda_device)
+    y = U.run_step(g, t)
+    assert g.gdn_read_device_error() == 0
+    ry, rs, rc = U.oracle_full(h)
+    assert U.y_errors(y.cpu().numpy(), ry) <= U.TOL
+    assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_negative_and_all_zero_lengths_change_nothing(cuda_device, T):
+    import gated_deltanet_linear_step_gb300 as g
+
+    w, h = _case(3, 2, T)
+    t = U.to_device(h, cuda_device)
+    for lens in ([-7, 0, -1], [0, 0, 0]):
+        t["seq_len"] = torch.tensor(lens, dtype=torch.int32, device=cuda_device)
+        sentinel = torch.full(t["z"].shape, 777.0, device=cuda_device)
+        y = U.run_step(g, t, y=sentinel.clone())
+        torch.cuda.synchronize()
+        assert g.gdn_read_device_error() == 0
+        assert torch.equal(y, sentinel)
+        assert torch.equal(t["state"].cpu(), torch.from_numpy(h["state"]))
+        assert torch.equal(t["conv_state"].cpu(), torch.from_numpy(h["conv_state"]))
+
+
+def test_single_token_call_with_lengths(cuda_device):
+    """T = 1 runs the batched-decode kernel; a length of 0 leaves its sequence untouched and the
+    others match the oracle."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    w, h = _case(4, 2, 1, name="decode_b64_l36_t1")
+    h["seq_len"] = np.array([1, 0, 1, 0], np.int32)
+    t = U.to_device(h, cuda_device)
+    sentinel = torch.full(t["z"].shape, -3.0, device=cuda_device)
+    y = U.run_step(g, t, y=sentinel.clone())
+    assert g.gdn_read_device_error() == 0
+    ry, rs, rc = U.oracle_full(h)
+    gy = y.cpu().numpy()
+    for b in (1, 3):
+        assert np.all(gy[b] == -3.0)
+        assert np.array_equal(t["state"][b].cpu().numpy(), h["state"][b])
+    keep = [0, 2]
+    assert U.y_errors(gy[keep], ry[keep]) <= U.TOL
+    assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
