@@ -236,3 +236,35 @@ def test_host_pipeline_argument_checks(lib):
     assert lib.gdn_host_pipeline_submit(None, base, base, base, base, base) == 1
     assert lib.gdn_host_pipeline_synchronize(None) == 1
     lib.gdn_host_pipeline_destroy(None)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """Without the compiled library every call raises; nothing falls back to another path."""
+    import gated_deltanet_linear_step_gb300 as g
+    from gated_deltanet_linear_step_gb300 import _binding
+
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _binding.load_library(str(tmp_path / "libgdn.so"))
+    monkeypatch.setattr(_binding, "LIB_PATH", str(tmp_path / "libgdn.so"))
+    monkeypatch.setattr(_binding.load_library, "__defaults__", (str(tmp_path / "libgdn.so"),))
+    t = torch.zeros(1, 1, 1, 10240)
+    with pytest.raises(RuntimeError, match="missing"):
+        g.gdn_decode_step(t, t, t, t, t, t, t, t, t, t, t)
+    with pytest.raises(RuntimeError, match="missing"):
+        g.gdn_get_geometry()
+
+
+def test_oracle_is_not_imported_by_the_product():
+    """The library binding and its package never import the oracle."""
+    import ast
+
+    pkg = os.path.join(ROOT, "gated_deltanet_linear_step_gb300")
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            tree = ast.parse(open(os.path.join(pkg, name)).read())
+            for node in ast.walk(tree):
+                if isinstance(node, ast.Import):
+                    assert all(not a.name.startswith("oracle") for a in node.names), name
+                elif isinstance(node, ast.ImportFrom):
+                    assert not (node.module or "").startswith("oracle"), name
