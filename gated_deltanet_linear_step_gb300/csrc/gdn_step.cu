@@ -134,6 +134,59 @@ __device__ __forceinline__ void conv_slot(const Params& p, float* rec, int cc, i
     hist[2] = h2;
 }
 
+// conv_slot for a whole short window (at most kShortWindow tokens) on both slots
+// of a thread at once: every load of slot A and slot B is issued before either
+// is used, so the two slots cost one round trip to memory instead of two.
+constexpr int kShortWindow = 8;
+
+__device__ __forceinline__ void conv_pair_first(const Params& p, float* rec, int tid, int cA, int cB, long long bl,
+                                                int l, int tc, float (&histA)[3], float (&histB)[3]) {
+    const bool has_b = tid < kS;
+    const float4 wA =
+        __ldg(reinterpret_cast<const float4*>(p.conv_w + (static_cast<size_t>(l) * kConvChannels + cA) * kDConv));
+    float4 wB = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (has_b)
+        wB = __ldg(reinterpret_cast<const float4*>(p.conv_w + (static_cast<size_t>(l) * kConvChannels + cB) * kDConv));
+    const float* csA = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + cA) * (kDConv - 1);
+    const float* csB = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + cB) * (kDConv - 1);
+    float a0 = csA[0], a1 = csA[1], a2 = csA[2];
+    float b0 = 0.f, b1 = 0.f, b2 = 0.f;
+    if (has_b) {
+        b0 = csB[0];
+        b1 = csB[1];
+        b2 = csB[2];
+    }
+    const float* xA = p.qkv + static_cast<size_t>(bl) * p.T * kConvChannels + cA;
+    const float* xB = p.qkv + static_cast<size_t>(bl) * p.T * kConvChannels + cB;
+    float xa[kShortWindow], xb[kShortWindow];
+#pragma unroll
+    for (int t = 0; t < kShortWindow; ++t) {
+        xa[t] = (t < tc) ? __ldg(xA + static_cast<size_t>(t) * kConvChannels) : 0.0f;
+        xb[t] = (has_b && t < tc) ? __ldg(xB + static_cast<size_t>(t) * kConvChannels) : 0.0f;
+    }
+#pragma unroll
+    for (int t = 0; t < kShortWindow; ++t) {
+        if (t < tc) {
+            rec[t * kRecFloats + tid] = siluf_(conv4(wA, a0, a1, a2, xa[t]));
+            a0 = a1;
+            a1 = a2;
+            a2 = xa[t];
+            if (has_b) {
+                rec[t * kRecFloats + 2 * kS + tid] = siluf_(conv4(wB, b0, b1, b2, xb[t]));
+                b0 = b1;
+                b1 = b2;
+                b2 = xb[t];
+            }
+        }
+    }
+    histA[0] = a0;
+    histA[1] = a1;
+    histA[2] = a2;
+    histB[0] = b0;
+    histB[1] = b1;
+    histB[2] = b2;
+}
+
 __device__ __forceinline__ void store_history(const Params& p, long long bl, int c, const float (&hist)[3]) {
     float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + c) * (kDConv - 1);
     cs[0] = hist[0];
@@ -225,6 +278,10 @@ __device__ __forceinline__ float4 delta_step_octet_deferred(float (&s)[64], floa
     return make_float4(P * o0, P * o1, P * o2, P * o3);
 }
 
+// kShort: the call's window has at most kShortWindow tokens, so every unit is one
+// chunk and the tile never stays in registers from one chunk to the next. That
+// leaves room to issue both conv slots' loads at once (conv_pair_first).
+template <bool kShort>
 __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) unsigned char smem[];
     float* tile = reinterpret_cast<float*>(smem);
@@ -278,6 +335,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
         int n = p.T;
         if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + b), 0), p.T);
 
+        if (kShort) {
+            // The previous unit's tile is dead here; clearing the registers tells the compiler so.
+#pragma unroll
+            for (int i = 0; i < 64; ++i) s[i] = 0.0f;
+        }
+
         int c0 = 0;
         do {
             const int tc = min(kChunk, n - c0);
@@ -298,8 +361,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             // ---- conv + SiLU of the CTA's 384 channels; the gates of its head
             float histA[3], histB[3];
             if (work) {
-                conv_slot(p, rec, tid, cA, bl, l, c0, tc, histA);
-                if (tid < kS) conv_slot(p, rec, 2 * kS + tid, cB, bl, l, c0, tc, histB);
+                if (kShort) {
+                    conv_pair_first(p, rec, tid, cA, cB, bl, l, tc, histA, histB);
+                } else {
+                    conv_slot(p, rec, tid, cA, bl, l, c0, tc, histA);
+                    if (tid < kS) conv_slot(p, rec, 2 * kS + tid, cB, bl, l, c0, tc, histB);
+                }
                 if (tid >= kCtaThreads - kChunk) {
                     const int t = tid - (kCtaThreads - kChunk);
                     if (t < tc) {
@@ -450,7 +517,10 @@ cudaError_t device_setup(int* clusters) {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceSetup& d = g_setup[dev];
     if (!d.ready) {
-        e = cudaFuncSetAttribute(gdn_window_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gdn_window_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gdn_window_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kSmemBytes));
         if (e != cudaSuccess) return e;
         int sms = 0;
@@ -459,7 +529,7 @@ cudaError_t device_setup(int* clusters) {
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t cfg = window_config(static_cast<unsigned>(kGroup * sms), nullptr, attr);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, gdn_window_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, gdn_window_kernel<false>, &cfg);
         if (e != cudaSuccess || n <= 0) {
             (void)cudaGetLastError();
             n = (2 * sms) / kGroup;  // two CTAs per SM
@@ -499,7 +569,8 @@ cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long n_cl = p.n_units < clusters ? p.n_units : clusters;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = window_config(static_cast<unsigned>(n_cl * kGroup), stream, attr);
-    e = cudaLaunchKernelEx(&cfg, gdn_window_kernel, p);
+    e = a.T <= kShortWindow ? cudaLaunchKernelEx(&cfg, gdn_window_kernel<true>, p)
+                            : cudaLaunchKernelEx(&cfg, gdn_window_kernel<false>, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
