@@ -360,6 +360,17 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
 
             // ---- conv + SiLU of the CTA's 384 channels; the gates of its head
             float histA[3], histB[3];
+            // Short windows: the gate inputs are loaded with the conv inputs, not after them.
+            const int tg = tid - (kCtaThreads - kChunk);
+            const bool gate_thread = work && tg >= 0 && tg < tc;
+            float g_a = 0.f, g_b = 0.f, g_dt = 0.f, g_sa = 0.f;
+            if (kShort && gate_thread) {
+                const size_t row = (static_cast<size_t>(bl) * p.T + c0 + tg) * kVHeads + vh;
+                g_a = __ldg(p.alpha + row);
+                g_b = __ldg(p.beta + row);
+                g_dt = __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh);
+                g_sa = __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh);
+            }
             if (work) {
                 if (kShort) {
                     conv_pair_first(p, rec, tid, cA, cB, bl, l, tc, histA, histB);
@@ -367,18 +378,19 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                     conv_slot(p, rec, tid, cA, bl, l, c0, tc, histA);
                     if (tid < kS) conv_slot(p, rec, 2 * kS + tid, cB, bl, l, c0, tc, histB);
                 }
-                if (tid >= kCtaThreads - kChunk) {
-                    const int t = tid - (kCtaThreads - kChunk);
-                    if (t < tc) {
-                        const size_t row = (static_cast<size_t>(bl) * p.T + c0 + t) * kVHeads + vh;
-                        float bt, dc;
-                        head_gates_in((p.flags & kGatesReady) != 0, __ldg(p.alpha + row), __ldg(p.beta + row),
-                                   __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh),
-                                   __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
-                        rec[t * kRecFloats + kRecG + 0] = bt;
-                        rec[t * kRecFloats + kRecG + 1] = dc;
-                        rec[t * kRecFloats + kRecG + 2] = 1.0f / dc;
+                if (gate_thread) {
+                    if (!kShort) {
+                        const size_t row = (static_cast<size_t>(bl) * p.T + c0 + tg) * kVHeads + vh;
+                        g_a = __ldg(p.alpha + row);
+                        g_b = __ldg(p.beta + row);
+                        g_dt = __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh);
+                        g_sa = __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh);
                     }
+                    float bt, dc;
+                    head_gates_in((p.flags & kGatesReady) != 0, g_a, g_b, g_dt, g_sa, bt, dc);
+                    rec[tg * kRecFloats + kRecG + 0] = bt;
+                    rec[tg * kRecFloats + kRecG + 1] = dc;
+                    rec[tg * kRecFloats + kRecG + 2] = 1.0f / dc;
                 }
             }
             // All three CTAs have read this unit's old q/k history (first chunk).
