@@ -21,7 +21,10 @@
 // a unit's first chunk; a cluster barrier follows, and only after it does
 // rank 0 write the new q/k history (in the unit's last chunk). Each CTA writes
 // the history of its own v channels. The barrier also keeps the three CTAs on
-// the same unit.
+// the same unit. In the short-window instance (one chunk per unit) the barrier
+// is split: each CTA arrives once it has read the old history and waits only at
+// the unit's end, where rank 0 writes the new q/k history, so no CTA stalls on
+// the others between its conv and its recurrence.
 //
 // Tokens. The conv, norms and gates of up to kChunk tokens are computed into
 // shared-memory records, the recurrence walks them with the tile in
@@ -278,6 +281,13 @@ __device__ __forceinline__ float4 delta_step_octet_deferred(float (&s)[64], floa
     return make_float4(P * o0, P * o1, P * o2, P * o3);
 }
 
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // kShort: the call's window has at most kShortWindow tokens, so every unit is one
 // chunk and the tile never stays in registers from one chunk to the next. That
 // leaves room to issue both conv slots' loads at once (conv_pair_first).
@@ -341,6 +351,9 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             for (int i = 0; i < 64; ++i) s[i] = 0.0f;
         }
 
+        float qk_hist[3] = {0.f, 0.f, 0.f};
+        bool qk_store = false;  // short windows: rank 0 writes the q/k history at the unit's end
+
         int c0 = 0;
         do {
             const int tc = min(kChunk, n - c0);
@@ -393,13 +406,25 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                     rec[tg * kRecFloats + kRecG + 2] = 1.0f / dc;
                 }
             }
-            // All three CTAs have read this unit's old q/k history (first chunk).
-            if (c0 == 0) cluster_sync();
-            else __syncthreads();
-            // The new history: q/k by rank 0 only, v by each CTA.
-            if (last_chunk && write_state && !failed) {
-                if (hh == 0) store_history(p, bl, cA, histA);
-                if (tid < kS) store_history(p, bl, cB, histB);
+            if (kShort) {
+                // This CTA has read the unit's old q/k history: it arrives now and waits for the
+                // other two only at the unit's end, before rank 0 writes the new history.
+                cluster_arrive_release();
+                __syncthreads();
+                if (last_chunk && write_state && !failed && tid < kS) store_history(p, bl, cB, histB);
+                qk_hist[0] = histA[0];
+                qk_hist[1] = histA[1];
+                qk_hist[2] = histA[2];
+                qk_store = last_chunk && write_state && hh == 0;
+            } else {
+                // All three CTAs have read this unit's old q/k history (first chunk).
+                if (c0 == 0) cluster_sync();
+                else __syncthreads();
+                // The new history: q/k by rank 0 only, v by each CTA.
+                if (last_chunk && write_state && !failed) {
+                    if (hh == 0) store_history(p, bl, cA, histA);
+                    if (tid < kS) store_history(p, bl, cB, histB);
+                }
             }
 
             // ---- L2 norm of q and k (one warp per token) and the q scale
@@ -473,6 +498,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             c0 += kChunk;
             __syncthreads();  // the records are rewritten by the next chunk
         } while (c0 < n);
+        if (kShort) {
+            cluster_wait_acquire();
+            if (qk_store && !failed) store_history(p, bl, cA, qk_hist);
+        }
 
         // The slot takes the next unit's tile once the store has read it.
         const long long next = u + n_clusters;
