@@ -28,14 +28,16 @@
 //
 // Tokens. The conv, norms and gates of up to kChunk tokens are computed into
 // shared-memory records, the recurrence walks them with the tile in
-// registers, then y is produced for the chunk. z arrives in the records by
-// bulk copy while the chunk computes. The conv history of a later chunk is
+// registers, then y is produced for the chunk. z arrives in the records, and
+// the layer's ssm_norm beside them, by bulk copy while the chunk computes. The conv history of a later chunk is
 // re-read from the previous chunk's qkv rows.
 //
 // Tiles. A unit's tile arrives in the CTA's slot by bulk copy, moves to
 // registers, and after the last token returns to the slot and leaves with one
 // bulk store; the slot then takes the next unit's tile. The other CTA on the
-// SM computes while one waits.
+// SM computes while one waits. Warps 4-7 convolve one channel slot to warps
+// 0-3's two, so single threads of warps 4 and 5 issue the copies (z, and the
+// tile's store and refill) that would otherwise delay a two-slot warp.
 //
 // Waits are bounded; a wait that gives up marks the CTA failed, after which it
 // computes and writes nothing but still takes part in every cluster barrier,
@@ -70,9 +72,12 @@ constexpr int kRecG = 4 * kS;          // beta, decay, 1 / decay, pad
 constexpr int kRecFloats = kRecG + 8;  // 520 floats = 2080 bytes
 
 constexpr size_t kOffRecs = kTileBytes;
-constexpr size_t kOffBars = kOffRecs + size_t(kChunk) * kRecFloats * 4;  // 98816
+constexpr size_t kOffNorm = kOffRecs + size_t(kChunk) * kRecFloats * 4;  // 98816: the layer's ssm_norm
+constexpr size_t kOffBars = kOffNorm + kS * 4;                             // 99328
 constexpr int kBarTile = 0, kBarZ = 1, kNumBars = 2;
-constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;  // 98832
+constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;  // 99344
+constexpr int kCopyIssuer = 128;  // issues the z and ssm_norm copies (warp 4)
+constexpr int kTileIssuer = 160;  // stores and refills the tile slot (warp 5)
 
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit in one SM's shared memory");
 static_assert((kRecFloats * 4) % 16 == 0 && (kRecZ * 4) % 16 == 0, "records must stay 16-byte aligned");
@@ -281,8 +286,14 @@ __device__ __forceinline__ float4 delta_step_octet_deferred(float (&s)[64], floa
     return make_float4(P * o0, P * o1, P * o2, P * o3);
 }
 
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// In the short-window instance the per-unit cluster barrier orders one thing:
+// the old q/k history loads of ranks 1 and 2 before rank 0's stores of the new
+// history (a CTA barrier publishes the records). Each thread's loads have
+// returned by the time it arrives (their values feed the conv, which it issues
+// before the arrive), so the arrive needs no release fence; a release would
+// also stall on the thread's earlier y and history stores.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -296,6 +307,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
     extern __shared__ __align__(128) unsigned char smem[];
     float* tile = reinterpret_cast<float*>(smem);
     float* rec = reinterpret_cast<float*>(smem + kOffRecs);
+    float* norm_w = reinterpret_cast<float*>(smem + kOffNorm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
 
     const int tid = threadIdx.x;
@@ -318,6 +330,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
         fence_mbar_init();
         fence_proxy_async_smem();
     }
+    __syncthreads();  // the barriers are initialized before any thread uses them
 
     uint32_t tile_par = 0, z_par = 0;
     bool tile_pending = false, z_pending = false;  // copies issued and not yet waited for
@@ -360,10 +373,11 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             const bool last_chunk = (c0 + tc == n) && n > 0;
             const bool work = !failed && tc > 0;
 
-            // ---- z of the chunk's tokens by bulk copy, read in the epilogue
+            // ---- z of the chunk's tokens and the layer's ssm_norm by bulk copy, read in the epilogue
             if (work && write_y) {
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(z_bar, tc * kS * 4);
+                if (tid == kCopyIssuer) {
+                    mbar_arrive_expect_tx(z_bar, (tc + 1) * kS * 4);
+                    bulk_load(smem_addr(norm_w), p.ssm_norm + static_cast<size_t>(l) * kS, kS * 4, z_bar);
                     for (int t = 0; t < tc; ++t)
                         bulk_load(smem_addr(rec + t * kRecFloats + kRecZ),
                                   p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, z_bar);
@@ -409,7 +423,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             if (kShort) {
                 // This CTA has read the unit's old q/k history: it arrives now and waits for the
                 // other two only at the unit's end, before rank 0 writes the new history.
-                cluster_arrive_release();
+                cluster_arrive_relaxed();
                 __syncthreads();
                 if (last_chunk && write_state && !failed && tid < kS) store_history(p, bl, cB, histB);
                 qk_hist[0] = histA[0];
@@ -418,6 +432,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                 qk_store = last_chunk && write_state && hh == 0;
             } else {
                 // All three CTAs have read this unit's old q/k history (first chunk).
+                // (Here the barrier also publishes the records, so it keeps its release.)
                 if (c0 == 0) cluster_sync();
                 else __syncthreads();
                 // The new history: q/k by rank 0 only, v by each CTA.
@@ -470,7 +485,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                 fence_proxy_async_smem();
             }
             __syncthreads();
-            if (tid == 0 && store_tile) {
+            if (tid == kTileIssuer && store_tile) {
                 bulk_store(p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile, tile_s, kTileBytes);
                 bulk_commit();
             }
@@ -487,8 +502,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
                         const float* r = rec + t * kRecFloats;
                         const float4 o4 = *reinterpret_cast<const float4*>(r + kRecV + lane * 4);
                         const float4 z4 = *reinterpret_cast<const float4*>(r + kRecZ + lane * 4);
-                        const float4 w4 = __ldg(
-                            reinterpret_cast<const float4*>(p.ssm_norm + static_cast<size_t>(l) * kS + lane * 4));
+                        const float4 w4 = *reinterpret_cast<const float4*>(norm_w + lane * 4);
                         __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim +
                                                          vh * kS + lane * 4),
                                gated_rms_norm4(o4, z4, w4, silu_gate));
@@ -506,7 +520,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
         // The slot takes the next unit's tile once the store has read it.
         const long long next = u + n_clusters;
         if (next < p.n_units && !failed) {
-            if (tid == 0) {
+            if (tid == kTileIssuer) {
                 const long long nbl = next / kKHeads;
                 const int ng = static_cast<int>(next - nbl * kKHeads);
                 bulk_wait_read();
@@ -518,7 +532,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
         }
     }
 
-    if (tid == 0) {
+    if (tid == kTileIssuer) {
         // Copies still in flight land before the CTA leaves (bounded), and so do the stores.
         if (tile_pending) (void)mbar_wait_bounded(tile_bar, tile_par);
         if (z_pending) (void)mbar_wait_bounded(z_bar, z_par);
