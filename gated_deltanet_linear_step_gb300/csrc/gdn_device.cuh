@@ -131,8 +131,14 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
-__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+// sigmoid and SiLU through the __expf and __fdividef intrinsics: relative error
+// near 1e-6 over the inputs' range, far inside the 1e-4 parity bar, at about a
+// fifth of the instructions of expf and an IEEE division. For x below about -88,
+// 1 + e^-x is infinite and both return 0 (signed), their limit. The multi-token
+// kernel evaluates one SiLU per conv channel and token, and one sigmoid per y
+// element. softplus keeps expf and log1pf: it feeds the decay exponent.
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
 
 // Global conv channel of the unit's channel slot cc (k head g): q of head g at
