@@ -1,5 +1,6 @@
 """Edge cases of the decode step on the GPU: the longest window, lengths that are
-negative, zero for every sequence, or zero in a single-token call."""
+negative, zero for every sequence, or zero in a single-token call, and activations
+driven far into saturation."""
 import numpy as np
 import pytest
 import torch
@@ -66,4 +67,39 @@ def test_single_token_call_with_lengths(cuda_device):
     keep = [0, 2]
     assert U.y_errors(gy[keep], ry[keep]) <= U.TOL
     assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
+    assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("T,name", [(1, "decode_b64_l36_t1"), (5, "verify_b16_l36_t8_ragged"),
+                                    (20, "verify_b16_l36_t8_ragged")])
+@pytest.mark.parametrize("gate", ["sigmoid", "silu"])
+def test_saturated_activations_match_oracle(cuda_device, T, name, gate):
+    """Inputs scaled so that SiLU, sigmoid and softplus see arguments far beyond +-88, where e^-x
+    overflows or underflows in fp32: SiLU must go to x or 0, sigmoid to 1 or 0, beta to 0 or 1 and
+    decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel and both instances of
+    the multi-token kernel."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    w, h = _case(3, 2, T, name=name)
+    for k, f in (("qkv", 120.0), ("conv_state", 120.0), ("z", 150.0), ("alpha", 60.0), ("beta", 60.0)):
+        h[k] = (h[k] * np.float32(f)).astype(np.float32)
+    t = U.to_device(h, cuda_device)
+    flags = g.FLAG_SILU_GATE if gate == "silu" else 0
+    y = U.run_step(g, t, flags=flags)
+    torch.cuda.synchronize()
+    assert g.gdn_read_device_error() == 0
+    with np.errstate(over="ignore"):
+        ry, rs, rc = U.oracle_full(h, gate=gate)
+    gy = y.cpu().numpy()
+    assert np.all(np.isfinite(gy[~np.isnan(ry)]))
+    assert U.y_errors(gy, ry) <= U.TOL
+    # With beta and decay both driven to zero the fp64 oracle keeps tiles near 1e-50, which fp32
+    # cannot hold: 1e-4 relative needs 14 significant bits, which fp32 has only above about 2^-112.
+    # Tiles whose oracle magnitude is below 2^-100 must come out below 2^-100; the rest meet the bar.
+    gs = t["state"].cpu().numpy().reshape(-1, 128 * 128).astype(np.float64)
+    rt = rs.reshape(-1, 128 * 128)
+    floor = 2.0 ** -100
+    tiny = np.abs(rt).max(axis=1) < floor
+    assert np.all(np.abs(gs[tiny]).max(axis=1) < floor)
+    assert U.state_errors(gs[~tiny], rt[~tiny]) <= U.TOL
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
