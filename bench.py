@@ -70,6 +70,9 @@ def parse():
     ap.add_argument("--timing", default="graph", choices=["graph", "direct"],
                     help="graph: the K timed steps are one captured CUDA graph (no host gaps between launches); "
                          "direct: K calls from Python")
+    ap.add_argument("--packed", action="store_true",
+                    help="in_proj, step_inputs and mixer: weights packed once by gdn_pack_proj_weights before the "
+                         "timed region, the calls on the packed weights timed")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -542,10 +545,18 @@ def run_in_proj(args, w, with_ab=False):
         sa = torch.from_numpy(h["ssm_a"]).to(dev)
         gate = torch.empty((B, L, T, 48), device=dev)
         beta = torch.empty_like(gate)
+    packed = None
+    if args.packed:
+        packed = torch.empty(g.gdn_proj_pack_bytes(L, E), dtype=torch.uint8, device=dev)
+        g.gdn_pack_proj_weights(wq, wg, packed, wa if with_ab else None, wb if with_ab else None)
 
     def step():
-        if with_ab:
+        if with_ab and packed is not None:
+            g.gdn_step_inputs_packed(x, packed, dt, sa, qkv, z, gate, beta, ws)
+        elif with_ab:
             g.gdn_step_inputs(x, wq, wg, wa, wb, dt, sa, qkv, z, gate, beta, ws)
+        elif packed is not None:
+            g.gdn_in_proj_packed(x, packed, qkv, z, ws)
         else:
             g.gdn_in_proj(x, wq, wg, qkv, z, ws)
 
@@ -579,7 +590,7 @@ def run_in_proj(args, w, with_ab=False):
         "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16 x (bf16 hi + lo of f32), f32 accumulate",
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "L": L, "T": T, "n_embd": E, "outputs": n_out,
-                   "weights_bytes": L * n_out * E * 2,
+                   "weights_bytes": L * n_out * E * 2, "weights": "packed" if args.packed else "row-major",
                    "l2": "weights far larger than the 129 MB L2, streamed once per step",
                    "timing": f"{args.steps} calls (2 launches each) in one captured CUDA graph"},
         "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
@@ -615,9 +626,16 @@ def run_mixer(args, w):
     gate = torch.empty(t["alpha"].shape, device=dev)
     beta = torch.empty(t["beta"].shape, device=dev)
     y = torch.empty(t["z"].shape, device=dev)
+    packed = None
+    if args.packed:
+        packed = torch.empty(g.gdn_proj_pack_bytes(L, E), dtype=torch.uint8, device=dev)
+        g.gdn_pack_proj_weights(wq, wg, packed, wa, wb)
 
     def step():
-        g.gdn_step_inputs(x, wq, wg, wa, wb, t["dt"], t["ssm_a"], t["qkv"], t["z"], gate, beta, ws)
+        if packed is not None:
+            g.gdn_step_inputs_packed(x, packed, t["dt"], t["ssm_a"], t["qkv"], t["z"], gate, beta, ws)
+        else:
+            g.gdn_step_inputs(x, wq, wg, wa, wb, t["dt"], t["ssm_a"], t["qkv"], t["z"], gate, beta, ws)
         g.gdn_decode_step_ex(t["qkv"], t["z"], gate, beta, t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"],
                              t["conv_state"], t["state"], y, seq_len=t["seq_len"], flags=g.FLAG_GATES_READY)
 
@@ -652,6 +670,7 @@ def run_mixer(args, w):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 (bf16 weights)",
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "L": L, "T": T, "n_embd": E,
+                   "weights": "packed" if args.packed else "row-major",
                    "timing": f"{args.steps} x (gdn_step_inputs + gdn_decode_step_ex) in one captured CUDA graph"},
         "clocks": clocks.summary(), "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,

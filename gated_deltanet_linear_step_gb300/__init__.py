@@ -19,9 +19,13 @@ from ._binding import (  # noqa: F401
     gdn_in_proj,
     gdn_in_proj_noalloc,
     gdn_in_proj_workspace_size,
+    gdn_in_proj_packed,
+    gdn_pack_proj_weights,
+    gdn_proj_pack_bytes,
     gdn_last_error,
     gdn_read_device_error,
     gdn_step_inputs,
+    gdn_step_inputs_packed,
     gdn_verify_commit,
     gdn_verify_window,
     load_library,

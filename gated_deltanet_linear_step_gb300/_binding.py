@@ -63,6 +63,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_in_proj_noalloc.argtypes = [_P] * 5 + [_I, _I, _I, _I, _P]
         lib.gdn_step_inputs.argtypes = [_P] * 12 + [ctypes.c_size_t, _I, _I, _I, _I, _P]
         lib.gdn_in_proj_workspace_size.argtypes = [_I, _I, _I, _I]
+        lib.gdn_proj_pack_bytes.argtypes = [_I, _I]
+        lib.gdn_proj_pack_bytes.restype = ctypes.c_size_t
+        lib.gdn_pack_proj_weights.argtypes = [_P] * 5 + [ctypes.c_size_t, _I, _I, _P]
+        lib.gdn_in_proj_packed.argtypes = [_P, _P, ctypes.c_size_t, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _P]
+        lib.gdn_step_inputs_packed.argtypes = [_P, _P, ctypes.c_size_t] + [_P] * 7 + [ctypes.c_size_t, _I, _I, _I,
+                                                                                        _I, _P]
         lib.gdn_host_pipeline_slot_bytes.argtypes = [_I, _I, _I]
         lib.gdn_host_pipeline_slot_bytes.restype = ctypes.c_size_t
         lib.gdn_host_pipeline_create.argtypes = [ctypes.POINTER(ctypes.c_void_p)] + [_P] * 8 + [ctypes.c_size_t, _I,
@@ -73,7 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_host_pipeline_destroy.restype = None
         lib.gdn_in_proj_workspace_size.restype = ctypes.c_size_t
         for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
-                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_host_pipeline_create",
+                   "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_noalloc", "gdn_step_inputs",
+                   "gdn_pack_proj_weights", "gdn_in_proj_packed", "gdn_step_inputs_packed", "gdn_host_pipeline_create",
                    "gdn_host_pipeline_submit", "gdn_host_pipeline_synchronize", "gdn_get_geometry",
                    "gdn_read_device_error"):
             getattr(lib, fn).restype = ctypes.c_int
@@ -314,6 +321,93 @@ def gdn_in_proj_noalloc(x, w_qkv, w_gate, qkv, z, stream=None):
     ]
     with torch.cuda.device(dev):
         _check(lib.gdn_in_proj_noalloc(*p, B, L, T, E, _stream_handle(stream, dev)))
+
+
+def gdn_proj_pack_bytes(L: int, n_embd: int) -> int:
+    """Bytes of the packed projection weights of L layers (0 for sizes out of range)."""
+    return int(load_library().gdn_proj_pack_bytes(int(L), int(n_embd)))
+
+
+def _bf16_weight(w, name):
+    if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    return w
+
+
+def _packed(packed, dev):
+    if not isinstance(packed, torch.Tensor) or packed.dtype != torch.uint8 or packed.dim() != 1:
+        raise TypeError("packed must be a 1-D torch.uint8 tensor written by gdn_pack_proj_weights")
+    return _ptr(packed, "packed", tuple(packed.shape), dtype=torch.uint8, device=dev), int(packed.numel())
+
+
+def gdn_pack_proj_weights(w_qkv, w_gate, packed, w_alpha=None, w_beta=None, stream=None):
+    """Rearranges the projection weights into ``packed`` (a 1-D uint8 CUDA tensor of at least
+    gdn_proj_pack_bytes(L, n_embd) bytes), the order gdn_in_proj_packed and
+    gdn_step_inputs_packed read. w_alpha and w_beta are optional (zero rows without them)."""
+    lib = load_library()
+    _bf16_weight(w_qkv, "w_qkv")
+    if w_qkv.dim() != 3:
+        raise ValueError("w_qkv must be [L][10240][n_embd]")
+    L, E = int(w_qkv.shape[0]), int(w_qkv.shape[2])
+    dev = w_qkv.device
+    if (w_alpha is None) != (w_beta is None):
+        raise ValueError("give both w_alpha and w_beta, or neither")
+    p = [
+        _ptr(w_qkv, "w_qkv", (L, CONV_CHANNELS, E), dtype=w_qkv.dtype, device=dev),
+        _ptr(_bf16_weight(w_gate, "w_gate"), "w_gate", (L, VALUE_DIM, E), dtype=w_gate.dtype, device=dev),
+        None if w_alpha is None else _ptr(_bf16_weight(w_alpha, "w_alpha"), "w_alpha", (L, V_HEADS, E),
+                                          dtype=w_alpha.dtype, device=dev),
+        None if w_beta is None else _ptr(_bf16_weight(w_beta, "w_beta"), "w_beta", (L, V_HEADS, E),
+                                         dtype=w_beta.dtype, device=dev),
+    ]
+    pp, nbytes = _packed(packed, dev)
+    with torch.cuda.device(dev):
+        _check(lib.gdn_pack_proj_weights(*p, pp, nbytes, L, E, _stream_handle(stream, dev)))
+
+
+def gdn_in_proj_packed(x, packed, qkv, z, workspace, stream=None):
+    """gdn_in_proj on weights packed by gdn_pack_proj_weights; bit-identical outputs."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
+        raise TypeError("workspace must be a 1-D torch.uint8 tensor")
+    pp, nbytes = _packed(packed, dev)
+    p = [
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev),
+        _ptr(workspace, "workspace", tuple(workspace.shape), dtype=torch.uint8, device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_in_proj_packed(_ptr(x, "x", (B, L, T, E), device=dev), pp, nbytes, *p,
+                                      int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
+
+
+def gdn_step_inputs_packed(x, packed, dt, ssm_a, qkv, z, gate, beta, workspace, stream=None):
+    """gdn_step_inputs on weights packed by gdn_pack_proj_weights (with w_alpha and w_beta);
+    bit-identical outputs."""
+    lib = load_library()
+    if not isinstance(x, torch.Tensor) or x.dim() != 4:
+        raise ValueError("x must be a [B][L][T][n_embd] tensor")
+    B, L, T, E = (int(v) for v in x.shape)
+    dev = x.device
+    if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
+        raise TypeError("workspace must be a 1-D torch.uint8 tensor")
+    pp, nbytes = _packed(packed, dev)
+    p = [
+        _ptr(dt, "dt", (L, V_HEADS), device=dev),
+        _ptr(ssm_a, "ssm_a", (L, V_HEADS), device=dev),
+        _ptr(qkv, "qkv", (B, L, T, CONV_CHANNELS), device=dev),
+        _ptr(z, "z", (B, L, T, VALUE_DIM), device=dev),
+        _ptr(gate, "gate", (B, L, T, V_HEADS), device=dev),
+        _ptr(beta, "beta", (B, L, T, V_HEADS), device=dev),
+        _ptr(workspace, "workspace", tuple(workspace.shape), dtype=torch.uint8, device=dev),
+    ]
+    with torch.cuda.device(dev):
+        _check(lib.gdn_step_inputs_packed(_ptr(x, "x", (B, L, T, E), device=dev), pp, nbytes, *p,
+                                          int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
 
 
 def gdn_get_geometry() -> dict:

@@ -129,6 +129,77 @@ gdn_status run(const float* qkv, const float* z, const float* alpha, const float
     return GDN_OK;
 }
 
+// Checks and launches a projection on packed weights: gdn_in_proj_packed
+// (dt, ssm_a, gate and beta NULL) or gdn_step_inputs_packed (all four set).
+gdn_status run_packed(const char* fn, const float* x, const void* packed, size_t packed_bytes, const float* dt,
+                      const float* ssm_a, float* qkv, float* z, float* gate, float* beta, void* workspace,
+                      size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream, bool with_ab) {
+    const struct {
+        const char* name;
+        const void* p;
+        bool required;
+    } ptrs[] = {{"x", x, true},         {"packed", packed, true}, {"qkv", qkv, true},
+                {"z", z, true},         {"workspace", workspace, true}, {"dt", dt, with_ab},
+                {"ssm_a", ssm_a, with_ab}, {"gate", gate, with_ab}, {"beta", beta, with_ab}};
+    for (const auto& q : ptrs) {
+        if (!q.required) continue;
+        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
+    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
+    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
+    const unsigned long long b = B, l = L, t = T, e = n_embd;
+    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
+    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
+    const size_t pack = gdn::proj_pack_bytes(L, n_embd);
+    if (packed_bytes < pack)
+        return fail(GDN_ERR_SHAPE, "%s: packed weights of %zu bytes, %zu needed", fn, packed_bytes, pack);
+    const Span spans[] = {
+        {"x", x, b * l * t * e * 4, false},
+        {"packed", packed, pack, false},
+        {"dt", dt, with_ab ? l * gdn::kVHeads * 4 : 0, false},
+        {"ssm_a", ssm_a, with_ab ? l * gdn::kVHeads * 4 : 0, false},
+        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
+        {"z", z, b * l * t * gdn::kValueDim * 4, true},
+        {"gate", gate, with_ab ? b * l * t * gdn::kVHeads * 4 : 0, true},
+        {"beta", beta, with_ab ? b * l * t * gdn::kVHeads * 4 : 0, true},
+        {"workspace", workspace, need, true},
+    };
+    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
+    for (int i = 0; i < n; ++i) {
+        if (!spans[i].output) continue;
+        for (int k = 0; k < n; ++k)
+            if (k != i && overlaps(spans[i], spans[k]))
+                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
+    }
+    gdn::ProjArgs a;
+    a.x = x;
+    a.w_qkv = nullptr;
+    a.w_gate = nullptr;
+    a.qkv = qkv;
+    a.z = z;
+    a.workspace = workspace;
+    a.B = B;
+    a.L = L;
+    a.T = T;
+    a.n_embd = n_embd;
+    a.packed = packed;
+    if (with_ab) {
+        a.dt = dt;
+        a.ssm_a = ssm_a;
+        a.gate = gate;
+        a.beta = beta;
+    }
+    const cudaError_t err = gdn::launch_in_proj(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
+    return GDN_OK;
+}
+
 }  // namespace
 
 namespace gdn {
@@ -438,6 +509,75 @@ gdn_status gdn_read_device_error(void* stream, uint32_t* out) {
     const cudaError_t e = gdn::read_device_error(static_cast<cudaStream_t>(stream), out);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "gdn_read_device_error: %s", cudaGetErrorString(e));
     return GDN_OK;
+}
+
+size_t gdn_proj_pack_bytes(int L, int n_embd) {
+    if (L < 1 || L > 65535 || n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0) return 0;
+    return gdn::proj_pack_bytes(L, n_embd);
+}
+
+gdn_status gdn_pack_proj_weights(const uint16_t* w_qkv, const uint16_t* w_gate, const uint16_t* w_alpha,
+                                 const uint16_t* w_beta, void* packed, size_t packed_bytes, int L, int n_embd,
+                                 void* stream) {
+    t_last_error.clear();
+    const char* fn = "gdn_pack_proj_weights";
+    if ((w_alpha == nullptr) != (w_beta == nullptr))
+        return fail(GDN_ERR_NULL, "%s: w_alpha and w_beta must both be given or both be NULL", fn);
+    const struct {
+        const char* name;
+        const void* p;
+        bool required;
+    } ptrs[] = {{"w_qkv", w_qkv, true}, {"w_gate", w_gate, true}, {"packed", packed, true},
+                {"w_alpha", w_alpha, w_alpha != nullptr}, {"w_beta", w_beta, w_beta != nullptr}};
+    for (const auto& q : ptrs) {
+        if (!q.required) continue;
+        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
+        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
+            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
+    }
+    if (L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: L=%d out of range", fn, L);
+    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
+    const size_t need = gdn::proj_pack_bytes(L, n_embd);
+    if (packed_bytes < need)
+        return fail(GDN_ERR_SHAPE, "%s: packed buffer of %zu bytes, %zu needed", fn, packed_bytes, need);
+    const unsigned long long l = L, e = n_embd;
+    const Span out = {"packed", packed, need, true};
+    const Span ins[] = {
+        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
+        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
+        {"w_alpha", w_alpha, w_alpha != nullptr ? l * gdn::kVHeads * e * 2 : 0, false},
+        {"w_beta", w_beta, w_beta != nullptr ? l * gdn::kVHeads * e * 2 : 0, false},
+    };
+    for (const Span& in : ins)
+        if (overlaps(out, in)) return fail(GDN_ERR_ALIAS, "%s: packed overlaps %s", fn, in.name);
+    gdn::PackArgs a;
+    a.w_qkv = w_qkv;
+    a.w_gate = w_gate;
+    a.w_alpha = w_alpha;
+    a.w_beta = w_beta;
+    a.packed = packed;
+    a.L = L;
+    a.n_embd = n_embd;
+    const cudaError_t err = gdn::launch_pack_proj(a, static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
+    return GDN_OK;
+}
+
+gdn_status gdn_in_proj_packed(const float* x, const void* packed, size_t packed_bytes, float* qkv, float* z,
+                              void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd,
+                              void* stream) {
+    t_last_error.clear();
+    return run_packed("gdn_in_proj_packed", x, packed, packed_bytes, nullptr, nullptr, qkv, z, nullptr, nullptr,
+                      workspace, workspace_bytes, B, L, T, n_embd, stream, false);
+}
+
+gdn_status gdn_step_inputs_packed(const float* x, const void* packed, size_t packed_bytes, const float* dt,
+                                  const float* ssm_a, float* qkv, float* z, float* gate, float* beta, void* workspace,
+                                  size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream) {
+    t_last_error.clear();
+    return run_packed("gdn_step_inputs_packed", x, packed, packed_bytes, dt, ssm_a, qkv, z, gate, beta, workspace,
+                      workspace_bytes, B, L, T, n_embd, stream, true);
 }
 
 }  // extern "C"

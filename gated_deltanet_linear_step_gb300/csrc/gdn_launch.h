@@ -71,6 +71,20 @@ struct ProjArgs {
     const float* ssm_a = nullptr;
     float* gate = nullptr;
     float* beta = nullptr;
+    // Optional: weights packed by launch_pack_proj; then w_qkv, w_gate, w_alpha and
+    // w_beta are not read, and gate != NULL selects the alpha/beta tile.
+    const void* packed = nullptr;
+};
+
+// The weights of the input projections, rearranged once into the blocks the
+// tensor cores read (gdn_proj.cu). w_alpha and w_beta may be NULL (zero rows).
+struct PackArgs {
+    const uint16_t* w_qkv;
+    const uint16_t* w_gate;
+    const uint16_t* w_alpha;
+    const uint16_t* w_beta;
+    void* packed;
+    int L, n_embd;
 };
 
 // Blocking of the input projections: token blocks, rows per block (a multiple
@@ -84,6 +98,10 @@ size_t proj_workspace_bytes(int B, int L, int T, int n_embd);
 
 // The split of x, then the tensor-core projection (gdn_proj.cu).
 cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream);
+
+// Bytes of the packed weights of L layers, and the packing kernel.
+size_t proj_pack_bytes(int L, int n_embd);
+cudaError_t launch_pack_proj(const PackArgs& a, cudaStream_t stream);
 
 // launch_in_proj with the workspace in the library's static scratch array
 // (gdn_proj_noalloc.cu); the caller checks the size against

@@ -25,7 +25,16 @@
 // 96-127 of that tile hold whatever the stage held before; each accumulator
 // lane depends on its own row only, and those lanes are not stored.
 //
-// Two kernels:
+// Packed weights. gdn_pack_proj_kernel rearranges the weights once, ahead of
+// the calls, into the blocks the MMA reads: per layer 129 tiles (80 of w_qkv,
+// 48 of w_gate, then the 48 alpha rows, the 48 beta rows and 32 zero rows),
+// per tile n_embd / 64 blocks of [128][64] BF16 (16 KB) in the 128-byte
+// swizzled K-major order a tensor-map load with that swizzle would leave in
+// shared memory. With packed weights the producer fetches each block with one
+// contiguous bulk copy instead of a 128-row tensor-map load whose rows lie
+// n_embd x 2 bytes apart in HBM.
+//
+// Two kernels per call:
 // * gdn_x_split_kernel writes hi and lo of every (layer, token block, 64-wide
 //   slice of n_embd) as two [N][64] BF16 blocks, already in the 128-byte
 //   swizzled K-major layout the MMA reads, into the caller's workspace.
@@ -66,6 +75,7 @@ constexpr int kMaxTok = 128;                   // tokens per block (MMA N <= 128
 constexpr int kQkvTiles = kConvChannels / kBM;  // 80
 constexpr int kGateTiles = kValueDim / kBM;     // 48
 constexpr int kChTiles = kQkvTiles + kGateTiles;  // 128; the alpha/beta tile is number 128
+constexpr int kPackTiles = kChTiles + 1;           // tiles per layer in the packed weights
 constexpr int kAbRows = kVHeads;                   // 48 alpha rows, then 48 beta rows
 constexpr int kProjThreads = 192;
 constexpr int kMaxStages = 8;
@@ -88,6 +98,7 @@ struct ProjParams {
     float* gate;           // [B][L][T][48]
     float* beta;           // [B][L][T][48]
     int n_ct;              // channel tiles per layer: 128, or 129 with the alpha/beta tile
+    const uint8_t* wp;     // packed weights [L][129][E / 64][16 KB], or NULL: the tensor maps above
     const uint16_t* xs;   // split x: [L][n_tb][n_ks][2][n_blk][64] BF16, swizzled
     float* qkv;           // [B][L][T][10240]
     float* z;             // [B][L][T][6144]
@@ -96,6 +107,16 @@ struct ProjParams {
     int n_tb;             // token blocks
     int n_stages;
     long long n_tiles;
+};
+
+struct PackParams {
+    const uint16_t* w_qkv;    // [L][10240][E]
+    const uint16_t* w_gate;   // [L][6144][E]
+    const uint16_t* w_alpha;  // [L][48][E], or NULL: zero rows
+    const uint16_t* w_beta;   // [L][48][E], or NULL: zero rows
+    uint8_t* out;             // [L][129][E / 64][16 KB]
+    int L, E;
+    long long n_blocks;
 };
 
 struct SplitParams {
@@ -217,6 +238,35 @@ __device__ __forceinline__ uint32_t lo_pair(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// One 16 KB block per iteration: 128 rows x 64 BF16, the 16-byte chunk c of
+// row r stored at r * 128 + (c XOR r mod 8) * 16.
+__global__ void __launch_bounds__(256) gdn_pack_proj_kernel(const __grid_constant__ PackParams p) {
+    const int n_ks = p.E / kBK;
+    for (long long blk = blockIdx.x; blk < p.n_blocks; blk += gridDim.x) {
+        const int ks = static_cast<int>(blk % n_ks);
+        const long long rest = blk / n_ks;
+        const int ct = static_cast<int>(rest % kPackTiles);
+        const int l = static_cast<int>(rest / kPackTiles);
+        uint8_t* dst = p.out + static_cast<size_t>(blk) * kWBytes;
+        for (int i = threadIdx.x; i < kBM * 8; i += blockDim.x) {
+            const int r = i >> 3, c = i & 7;
+            const uint16_t* row = nullptr;
+            if (ct < kQkvTiles) {
+                row = p.w_qkv + (static_cast<size_t>(l) * kConvChannels + ct * kBM + r) * p.E;
+            } else if (ct < kChTiles) {
+                row = p.w_gate + (static_cast<size_t>(l) * kValueDim + (ct - kQkvTiles) * kBM + r) * p.E;
+            } else if (r < kAbRows) {
+                if (p.w_alpha != nullptr) row = p.w_alpha + (static_cast<size_t>(l) * kAbRows + r) * p.E;
+            } else if (r < 2 * kAbRows) {
+                if (p.w_beta != nullptr) row = p.w_beta + (static_cast<size_t>(l) * kAbRows + r - kAbRows) * p.E;
+            }
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (row != nullptr) v = __ldg(reinterpret_cast<const uint4*>(row + ks * kBK + c * 8));
+            *reinterpret_cast<uint4*>(dst + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) gdn_x_split_kernel(const __grid_constant__ SplitParams p) {
     const int n_ks = p.E / kBK;
     const int M = p.B * p.T;
@@ -280,9 +330,9 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
         }
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tensormap(&p.tm_qkv);
-        prefetch_tensormap(&p.tm_gate);
-        if (p.n_ct > kChTiles) {
+        if (p.wp == nullptr) prefetch_tensormap(&p.tm_qkv);
+        if (p.wp == nullptr) prefetch_tensormap(&p.tm_gate);
+        if (p.wp == nullptr && p.n_ct > kChTiles) {
             prefetch_tensormap(&p.tm_alpha);
             prefetch_tensormap(&p.tm_beta);
         }
@@ -318,7 +368,12 @@ __global__ void __launch_bounds__(kProjThreads, 1) gdn_in_proj_kernel(const __gr
                         break;
                     }
                     const uint32_t st = base + s * stage_bytes;
-                    if (is_ab) {
+                    if (p.wp != nullptr) {
+                        mbar_arrive_expect_tx(full_bar(s), stage_bytes);
+                        bulk_load_stream(
+                            st, p.wp + ((static_cast<size_t>(l) * kPackTiles + ct) * n_ks + ks) * kWBytes, kWBytes,
+                            full_bar(s));
+                    } else if (is_ab) {
                         mbar_arrive_expect_tx(full_bar(s), 2u * kAbRows * 128u + x_bytes);
                         tma_load_2d(st, &p.tm_alpha, ks * kBK, l * kAbRows, full_bar(s), pol);
                         tma_load_2d(st + kAbRows * 128u, &p.tm_beta, ks * kBK, l * kAbRows, full_bar(s), pol);
@@ -552,16 +607,23 @@ cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream) {
 
     ProjParams p;
     memset(&p, 0, sizeof(p));
-    e = encode_weights(&p.tm_qkv, a.w_qkv, static_cast<long long>(a.L) * kConvChannels, a.n_embd, kBM);
-    if (e != cudaSuccess) return e;
-    e = encode_weights(&p.tm_gate, a.w_gate, static_cast<long long>(a.L) * kValueDim, a.n_embd, kBM);
-    if (e != cudaSuccess) return e;
+    const bool with_ab = a.gate != nullptr;
+    if (a.packed != nullptr) {
+        p.wp = static_cast<const uint8_t*>(a.packed);
+    } else {
+        e = encode_weights(&p.tm_qkv, a.w_qkv, static_cast<long long>(a.L) * kConvChannels, a.n_embd, kBM);
+        if (e != cudaSuccess) return e;
+        e = encode_weights(&p.tm_gate, a.w_gate, static_cast<long long>(a.L) * kValueDim, a.n_embd, kBM);
+        if (e != cudaSuccess) return e;
+        if (with_ab) {
+            e = encode_weights(&p.tm_alpha, a.w_alpha, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
+            if (e != cudaSuccess) return e;
+            e = encode_weights(&p.tm_beta, a.w_beta, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
+            if (e != cudaSuccess) return e;
+        }
+    }
     p.n_ct = kChTiles;
-    if (a.w_alpha != nullptr) {
-        e = encode_weights(&p.tm_alpha, a.w_alpha, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
-        if (e != cudaSuccess) return e;
-        e = encode_weights(&p.tm_beta, a.w_beta, static_cast<long long>(a.L) * kAbRows, a.n_embd, kAbRows);
-        if (e != cudaSuccess) return e;
+    if (with_ab) {
         p.dt = a.dt;
         p.ssm_a = a.ssm_a;
         p.gate = a.gate;
@@ -581,6 +643,32 @@ cudaError_t launch_in_proj(const ProjArgs& a, cudaStream_t stream) {
     p.n_tiles = static_cast<long long>(a.L) * g.n_tb * p.n_ct;
     const long long grid = p.n_tiles < sms ? p.n_tiles : sms;
     gdn_in_proj_kernel<<<static_cast<unsigned>(grid), kProjThreads, kProjSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+size_t proj_pack_bytes(int L, int E) {
+    return static_cast<size_t>(L) * kPackTiles * (E / kBK) * kWBytes;
+}
+
+cudaError_t launch_pack_proj(const PackArgs& a, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int sms = 0;
+    e = setup(dev, &sms);
+    if (e != cudaSuccess) return e;
+    PackParams p;
+    p.w_qkv = a.w_qkv;
+    p.w_gate = a.w_gate;
+    p.w_alpha = a.w_alpha;
+    p.w_beta = a.w_beta;
+    p.out = static_cast<uint8_t*>(a.packed);
+    p.L = a.L;
+    p.E = a.n_embd;
+    p.n_blocks = static_cast<long long>(a.L) * kPackTiles * (a.n_embd / kBK);
+    const long long cap = static_cast<long long>(sms) * 16;
+    gdn_pack_proj_kernel<<<static_cast<unsigned>(p.n_blocks < cap ? p.n_blocks : cap), 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -249,6 +249,55 @@ gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint
                                int B, int L, int T, int n_embd, void* stream);
 
 /*
+ * gdn_proj_pack_bytes - bytes of device memory the packed projection weights
+ * of L layers take (0 if the sizes are out of range):
+ * L x 129 tiles x (n_embd / 64) blocks x 16384 bytes, about the size of the
+ * four weight tensors together.
+ */
+size_t gdn_proj_pack_bytes(int L, int n_embd);
+
+/*
+ * gdn_pack_proj_weights - rearranges the projection weights once, ahead of
+ * the calls that use them, into the order the tensor cores read. For each
+ * layer there are 129 tiles of 128 output rows: 80 of w_qkv, 48 of w_gate,
+ * then one with the 48 rows of w_alpha, the 48 rows of w_beta and 32 rows of
+ * zeros. Each tile is n_embd / 64 blocks of 128 rows x 64 BF16 values
+ * (16384 bytes). Within a block, the 16-byte chunk c (8 values) of row r
+ * sits at byte r * 128 + (c XOR (r mod 8)) * 16: the 128-byte swizzled
+ * K-major order. The pages have no counterpart; it is a layout of this
+ * library, read by gdn_in_proj_packed and gdn_step_inputs_packed.
+ *
+ *   w_qkv, w_gate    as for gdn_in_proj (input)
+ *   w_alpha, w_beta  as for gdn_step_inputs (input), or both NULL: the
+ *                    alpha/beta tile is then zeros
+ *   packed           device memory of at least gdn_proj_pack_bytes() bytes,
+ *                    16-byte aligned, owned by the caller (output); it must
+ *                    not overlap the weights (GDN_ERR_ALIAS)
+ *
+ * One kernel runs on `stream`. Other conventions as gdn_in_proj.
+ */
+gdn_status gdn_pack_proj_weights(const uint16_t* w_qkv, const uint16_t* w_gate, const uint16_t* w_alpha,
+                                 const uint16_t* w_beta, void* packed, size_t packed_bytes, int L, int n_embd,
+                                 void* stream);
+
+/*
+ * gdn_in_proj_packed, gdn_step_inputs_packed - gdn_in_proj and
+ * gdn_step_inputs with the weights given as one buffer written by
+ * gdn_pack_proj_weights (packed_bytes: its size, at least
+ * gdn_proj_pack_bytes()). The tensor cores read the same values in the same
+ * order, so the outputs are bit-identical to the calls on the unpacked
+ * weights; each 16 KB block arrives by one contiguous copy instead of 128
+ * rows lying n_embd x 2 bytes apart. The other arguments, the workspace and
+ * the conventions are those of gdn_in_proj and gdn_step_inputs.
+ */
+gdn_status gdn_in_proj_packed(const float* x, const void* packed, size_t packed_bytes, float* qkv, float* z,
+                              void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd,
+                              void* stream);
+gdn_status gdn_step_inputs_packed(const float* x, const void* packed, size_t packed_bytes, const float* dt,
+                                  const float* ssm_a, float* qkv, float* z, float* gate, float* beta, void* workspace,
+                                  size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream);
+
+/*
  * Host-fed decode steps with overlapped copies. A pipeline runs
  * gdn_decode_step (or its varlen form when seq_len is given) on activations
  * that live in HOST memory: each gdn_host_pipeline_submit queues the copies of

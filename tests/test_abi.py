@@ -39,7 +39,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for fn in ("gdn_decode_step", "gdn_decode_step_varlen", "gdn_verify_window", "gdn_verify_commit",
                "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_workspace_size",
-               "gdn_in_proj_noalloc", "gdn_step_inputs",
+               "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_proj_pack_bytes", "gdn_pack_proj_weights",
+               "gdn_in_proj_packed", "gdn_step_inputs_packed",
                "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
         assert fn in names
 
@@ -212,6 +213,60 @@ def test_step_inputs_argument_checks(lib):
     assert lib.gdn_step_inputs(*args(dict(ptr, gate=ptr["beta"] + 16)), ws, B, L, T, E, None) == 4
     assert lib.gdn_step_inputs(*args(dict(ptr, beta=ptr["wa"] + 64)), ws, B, L, T, E, None) == 4
     assert lib.gdn_step_inputs(*args(dict(ptr, ws=ptr["qkv"] + 64)), ws, B, L, T, E, None) == 4
+
+
+def test_proj_pack_bytes(lib):
+    """129 tiles per layer (qkv, gate, alpha/beta) x n_embd / 64 blocks of 16 KB."""
+    assert lib.gdn_proj_pack_bytes(36, 2560) == 36 * 129 * 40 * 16384
+    assert lib.gdn_proj_pack_bytes(1, 64) == 129 * 16384
+    assert lib.gdn_proj_pack_bytes(0, 64) == 0
+    assert lib.gdn_proj_pack_bytes(2, 100) == 0
+    assert lib.gdn_proj_pack_bytes(2, 65536 + 64) == 0
+
+
+@no_gpu
+def test_pack_and_packed_argument_checks(lib):
+    base = 1 << 41
+    E, B, L, T = 128, 2, 3, 1
+    ws = lib.gdn_in_proj_workspace_size(B, L, T, E)
+    pb = lib.gdn_proj_pack_bytes(L, E)
+    w = {k: base + (i << 32) for i, k in enumerate(("wq", "wg", "wa", "wb", "pk"))}
+    pack = lambda p, n=pb, l=L, e=E: lib.gdn_pack_proj_weights(  # noqa: E731
+        p["wq"], p["wg"], p["wa"], p["wb"], p["pk"], n, l, e, None)
+    assert pack(dict(w, wq=None)) == 1
+    assert pack(dict(w, wa=None)) == 1                  # alpha without beta
+    assert lib.gdn_pack_proj_weights(w["wq"], w["wg"], None, None, None, pb, L, E, None) == 1
+    assert pack(dict(w, pk=w["pk"] + 8)) == 3
+    assert pack(dict(w, wb=w["wb"] + 4)) == 3
+    assert pack(w, n=pb - 16) == 2
+    assert pack(w, l=0) == 2
+    assert pack(w, e=100) == 2
+    assert pack(dict(w, pk=w["wg"] + 4096)) == 4        # packed overlaps w_gate
+    assert b"overlaps" in lib.gdn_last_error()
+
+    keys = ("x", "pk", "qkv", "z", "ws")
+    ptr = {k: base + (i << 32) for i, k in enumerate(keys)}
+    proj = lambda p, n=pb, w_=ws, e=E: lib.gdn_in_proj_packed(  # noqa: E731
+        p["x"], p["pk"], n, p["qkv"], p["z"], p["ws"], w_, B, L, T, e, None)
+    for k in keys:
+        assert proj(dict(ptr, **{k: None})) == 1, k
+        assert proj(dict(ptr, **{k: ptr[k] + 4})) == 3, k
+    assert proj(ptr, n=pb - 16) == 2
+    assert proj(ptr, w_=ws - 16) == 2
+    assert proj(ptr, e=100) == 2
+    assert proj(dict(ptr, qkv=ptr["pk"] + 64)) == 4
+    assert proj(dict(ptr, z=ptr["qkv"] + 16)) == 4
+
+    keys = ("x", "pk", "dt", "sa", "qkv", "z", "gate", "beta", "ws")
+    ptr = {k: base + (i << 32) for i, k in enumerate(keys)}
+    step = lambda p, n=pb: lib.gdn_step_inputs_packed(  # noqa: E731
+        p["x"], p["pk"], n, p["dt"], p["sa"], p["qkv"], p["z"], p["gate"], p["beta"], p["ws"], ws, B, L, T, E, None)
+    for k in keys:
+        assert step(dict(ptr, **{k: None})) == 1, k
+        assert step(dict(ptr, **{k: ptr[k] + 4})) == 3, k
+    assert step(ptr, n=pb - 16) == 2
+    assert step(dict(ptr, gate=ptr["beta"] + 16)) == 4
+    assert step(dict(ptr, beta=ptr["pk"] + 64)) == 4
 
 
 @no_gpu

@@ -207,3 +207,83 @@ def test_mixer_step_fed_by_the_projections(cuda_device, T, fused):
     assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
     gc = t["conv_state"].cpu().numpy().astype(np.float64)
     assert float(np.abs(gc - rc).max() / np.abs(rc).max()) <= U.TOL
+
+
+def _packed_expected(wq, wg, wa, wb):
+    """The packed layout restated in numpy: per layer 129 tiles of 128 rows (80 of w_qkv,
+    48 of w_gate, then alpha, beta and 32 zero rows), per tile n_embd / 64 blocks of
+    [128][64] BF16 where the 16-byte chunk c of row r sits at chunk position c XOR (r mod 8)."""
+    L, _, E = wq.shape
+    ab = np.zeros((L, 128, E), np.uint16)
+    if wa is not None:
+        ab[:, :48], ab[:, 48:96] = wa, wb
+    rows = np.concatenate([wq, wg, ab], axis=1)              # [L][129 * 128][E]
+    blocks = rows.reshape(L, 129, 128, E // 64, 8, 8)          # l, tile, r, ks, chunk, value
+    blocks = blocks.transpose(0, 1, 3, 2, 4, 5).copy()         # l, tile, ks, r, chunk, value
+    out = np.empty_like(blocks)
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    out[:, :, :, r, c ^ (r & 7)] = blocks[:, :, :, r, c]
+    return out.reshape(-1).view(np.uint8)
+
+
+@pytest.mark.parametrize("with_ab", [True, False])
+def test_packed_weights_layout(cuda_device, with_ab):
+    import gated_deltanet_linear_step_gb300 as g
+
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=1, L=2, T=1)
+    E = 128
+    wq, wg = _weights(w, E)
+    ha = W.host_ab_inputs(w, E)
+    d = cuda_device
+    n = g.gdn_proj_pack_bytes(2, E)
+    buf = torch.full((n + 2 * 4096,), 0xA5, dtype=torch.uint8, device=d)
+    packed = buf[4096:4096 + n]
+    wa = _bf16(ha["w_alpha"], d) if with_ab else None
+    wb = _bf16(ha["w_beta"], d) if with_ab else None
+    g.gdn_pack_proj_weights(_bf16(wq, d), _bf16(wg, d), packed, wa, wb)
+    torch.cuda.synchronize()
+    want = _packed_expected(wq.view(np.uint16), wg.view(np.uint16),
+                            ha["w_alpha"].view(np.uint16) if with_ab else None,
+                            ha["w_beta"].view(np.uint16) if with_ab else None)
+    assert np.array_equal(packed.cpu().numpy(), want)
+    assert (buf[:4096] == 0xA5).all() and (buf[-4096:] == 0xA5).all()
+
+
+@pytest.mark.parametrize("B,L,T,E", [(3, 2, 5, 128), (150, 1, 1, 64), (64, 2, 1, 2560)])
+def test_packed_projections_equal_unpacked_bit_for_bit(cuda_device, B, L, T, E):
+    """gdn_in_proj_packed and gdn_step_inputs_packed feed the tensor cores the same values in
+    the same order as the calls on the row-major weights: identical bits."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
+    x = torch.from_numpy(_x(w, E)).to(cuda_device)
+    wq, wg = _weights(w, E)
+    ha = W.host_ab_inputs(w, E)
+    d = cuda_device
+    wq_d, wg_d = _bf16(wq, d), _bf16(wg, d)
+    wa_d, wb_d = _bf16(ha["w_alpha"], d), _bf16(ha["w_beta"], d)
+    dt, sa = torch.from_numpy(ha["dt"]).to(d), torch.from_numpy(ha["ssm_a"]).to(d)
+    packed = torch.empty(g.gdn_proj_pack_bytes(L, E), dtype=torch.uint8, device=d)
+    g.gdn_pack_proj_weights(wq_d, wg_d, packed, wa_d, wb_d)
+    ws = torch.empty(g.gdn_in_proj_workspace_size(B, L, T, E), dtype=torch.uint8, device=d)
+
+    def outs():
+        return {name: torch.full((B, L, T, width), float("nan"), device=d)
+                for name, width in (("qkv", W.CONV_CHANNELS), ("z", W.VALUE_DIM), ("gate", 48), ("beta", 48))}
+
+    a, b = outs(), outs()
+    g.gdn_in_proj(x, wq_d, wg_d, a["qkv"], a["z"], ws)
+    g.gdn_in_proj_packed(x, packed, b["qkv"], b["z"], ws)
+    torch.cuda.synchronize()
+    assert g.gdn_read_device_error() == 0
+    assert torch.equal(a["qkv"], b["qkv"]) and torch.equal(a["z"], b["z"])
+
+    a, b = outs(), outs()
+    g.gdn_step_inputs(x, wq_d, wg_d, wa_d, wb_d, dt, sa, a["qkv"], a["z"], a["gate"], a["beta"], ws)
+    g.gdn_step_inputs_packed(x, packed, dt, sa, b["qkv"], b["z"], b["gate"], b["beta"], ws)
+    torch.cuda.synchronize()
+    assert g.gdn_read_device_error() == 0
+    for name in a:
+        assert not torch.isnan(b[name]).any().item(), name
+        assert torch.equal(a[name], b[name]), name
