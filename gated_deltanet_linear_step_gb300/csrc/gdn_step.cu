@@ -59,7 +59,6 @@ constexpr uint32_t kTileBytes = kTile * 4;  // 65536
 constexpr int kCtaThreads = 256;            // one tile per CTA
 constexpr int kWarps = kCtaThreads / 32;    // 8
 constexpr int kChunk = 16;                  // tokens whose inputs are staged at once
-constexpr int kCtaChannels = 3 * kS;        // 384 conv channels per CTA: q, k of head g, v of its head
 
 // Per-token record in shared memory (floats): channel slot cc of the CTA maps
 // to offset cc (q at [0,128), k at [128,256), v at [256,384)); the recurrence
