@@ -129,24 +129,61 @@ gdn_status run(const float* qkv, const float* z, const float* alpha, const float
     return GDN_OK;
 }
 
-// Checks and launches a projection on packed weights: gdn_in_proj_packed
-// (dt, ssm_a, gate and beta NULL) or gdn_step_inputs_packed (all four set).
-gdn_status run_packed(const char* fn, const float* x, const void* packed, size_t packed_bytes, const float* dt,
-                      const float* ssm_a, float* qkv, float* z, float* gate, float* beta, void* workspace,
-                      size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream, bool with_ab) {
+// One input-projection call. The weights are row-major (w_qkv, w_gate, and with the
+// gates w_alpha, w_beta) or packed; the gate arguments (dt, ssm_a, gate, beta) come
+// all together or not at all; the split of x goes to the caller's workspace or, with
+// `scratch`, to the library's static scratch array.
+struct ProjCall {
+    const char* fn = "";
+    const float* x = nullptr;
+    const uint16_t* w_qkv = nullptr;
+    const uint16_t* w_gate = nullptr;
+    const uint16_t* w_alpha = nullptr;
+    const uint16_t* w_beta = nullptr;
+    const void* packed = nullptr;
+    size_t packed_bytes = 0;
+    const float* dt = nullptr;
+    const float* ssm_a = nullptr;
+    float* qkv = nullptr;
+    float* z = nullptr;
+    float* gate = nullptr;
+    float* beta = nullptr;
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
+    int B = 0, L = 0, T = 0, n_embd = 0;
+    bool with_ab = false;
+    bool use_packed = false;
+    bool scratch = false;
+};
+
+// Checks a projection call and launches it.
+gdn_status run_proj(const ProjCall& c, void* stream) {
+    const char* fn = c.fn;
+    const bool rowmajor = !c.use_packed;
     const struct {
         const char* name;
         const void* p;
         bool required;
-    } ptrs[] = {{"x", x, true},         {"packed", packed, true}, {"qkv", qkv, true},
-                {"z", z, true},         {"workspace", workspace, true}, {"dt", dt, with_ab},
-                {"ssm_a", ssm_a, with_ab}, {"gate", gate, with_ab}, {"beta", beta, with_ab}};
+    } ptrs[] = {{"x", c.x, true},
+                {"w_qkv", c.w_qkv, rowmajor},
+                {"w_gate", c.w_gate, rowmajor},
+                {"w_alpha", c.w_alpha, rowmajor && c.with_ab},
+                {"w_beta", c.w_beta, rowmajor && c.with_ab},
+                {"packed", c.packed, c.use_packed},
+                {"dt", c.dt, c.with_ab},
+                {"ssm_a", c.ssm_a, c.with_ab},
+                {"qkv", c.qkv, true},
+                {"z", c.z, true},
+                {"gate", c.gate, c.with_ab},
+                {"beta", c.beta, c.with_ab},
+                {"workspace", c.workspace, !c.scratch}};
     for (const auto& q : ptrs) {
         if (!q.required) continue;
         if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
         if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
             return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
     }
+    const int B = c.B, L = c.L, T = c.T, n_embd = c.n_embd;
     if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
     if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
     if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
@@ -154,21 +191,29 @@ gdn_status run_packed(const char* fn, const float* x, const void* packed, size_t
     const unsigned long long b = B, l = L, t = T, e = n_embd;
     if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
     const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
-    if (workspace_bytes < need)
-        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
-    const size_t pack = gdn::proj_pack_bytes(L, n_embd);
-    if (packed_bytes < pack)
-        return fail(GDN_ERR_SHAPE, "%s: packed weights of %zu bytes, %zu needed", fn, packed_bytes, pack);
+    if (c.scratch && need > gdn::proj_static_scratch_bytes())
+        return fail(GDN_ERR_SHAPE, "%s: these sizes need %zu bytes of scratch, the library holds %zu", fn, need,
+                    gdn::proj_static_scratch_bytes());
+    if (!c.scratch && c.workspace_bytes < need)
+        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, c.workspace_bytes, need);
+    const size_t pack = c.use_packed ? gdn::proj_pack_bytes(L, n_embd) : 0;
+    if (c.use_packed && c.packed_bytes < pack)
+        return fail(GDN_ERR_SHAPE, "%s: packed weights of %zu bytes, %zu needed", fn, c.packed_bytes, pack);
+    const unsigned long long ab = c.with_ab ? 1 : 0, rm = rowmajor ? 1 : 0;
     const Span spans[] = {
-        {"x", x, b * l * t * e * 4, false},
-        {"packed", packed, pack, false},
-        {"dt", dt, with_ab ? l * gdn::kVHeads * 4 : 0, false},
-        {"ssm_a", ssm_a, with_ab ? l * gdn::kVHeads * 4 : 0, false},
-        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
-        {"z", z, b * l * t * gdn::kValueDim * 4, true},
-        {"gate", gate, with_ab ? b * l * t * gdn::kVHeads * 4 : 0, true},
-        {"beta", beta, with_ab ? b * l * t * gdn::kVHeads * 4 : 0, true},
-        {"workspace", workspace, need, true},
+        {"x", c.x, b * l * t * e * 4, false},
+        {"w_qkv", c.w_qkv, rm * l * gdn::kConvChannels * e * 2, false},
+        {"w_gate", c.w_gate, rm * l * gdn::kValueDim * e * 2, false},
+        {"w_alpha", c.w_alpha, rm * ab * l * gdn::kVHeads * e * 2, false},
+        {"w_beta", c.w_beta, rm * ab * l * gdn::kVHeads * e * 2, false},
+        {"packed", c.packed, pack, false},
+        {"dt", c.dt, ab * l * gdn::kVHeads * 4, false},
+        {"ssm_a", c.ssm_a, ab * l * gdn::kVHeads * 4, false},
+        {"qkv", c.qkv, b * l * t * gdn::kConvChannels * 4, true},
+        {"z", c.z, b * l * t * gdn::kValueDim * 4, true},
+        {"gate", c.gate, ab * b * l * t * gdn::kVHeads * 4, true},
+        {"beta", c.beta, ab * b * l * t * gdn::kVHeads * 4, true},
+        {"workspace", c.workspace, c.scratch ? 0 : need, true},
     };
     const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
     for (int i = 0; i < n; ++i) {
@@ -178,24 +223,27 @@ gdn_status run_packed(const char* fn, const float* x, const void* packed, size_t
                 return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
     }
     gdn::ProjArgs a;
-    a.x = x;
-    a.w_qkv = nullptr;
-    a.w_gate = nullptr;
-    a.qkv = qkv;
-    a.z = z;
-    a.workspace = workspace;
+    a.x = c.x;
+    a.w_qkv = rowmajor ? c.w_qkv : nullptr;
+    a.w_gate = rowmajor ? c.w_gate : nullptr;
+    a.qkv = c.qkv;
+    a.z = c.z;
+    a.workspace = c.scratch ? nullptr : c.workspace;
     a.B = B;
     a.L = L;
     a.T = T;
     a.n_embd = n_embd;
-    a.packed = packed;
-    if (with_ab) {
-        a.dt = dt;
-        a.ssm_a = ssm_a;
-        a.gate = gate;
-        a.beta = beta;
+    a.packed = c.use_packed ? c.packed : nullptr;
+    if (c.with_ab) {
+        a.w_alpha = rowmajor ? c.w_alpha : nullptr;
+        a.w_beta = rowmajor ? c.w_beta : nullptr;
+        a.dt = c.dt;
+        a.ssm_a = c.ssm_a;
+        a.gate = c.gate;
+        a.beta = c.beta;
     }
-    const cudaError_t err = gdn::launch_in_proj(a, static_cast<cudaStream_t>(stream));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t err = c.scratch ? gdn::launch_in_proj_static(a, st) : gdn::launch_in_proj(a, st);
     if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
     return GDN_OK;
 }
@@ -316,54 +364,20 @@ size_t gdn_in_proj_workspace_size(int B, int L, int T, int n_embd) {
 gdn_status gdn_in_proj(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                        void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream) {
     t_last_error.clear();
-    const char* fn = "gdn_in_proj";
-    const struct {
-        const char* name;
-        const void* p;
-    } ptrs[] = {{"x", x}, {"w_qkv", w_qkv}, {"w_gate", w_gate}, {"qkv", qkv}, {"z", z}, {"workspace", workspace}};
-    for (const auto& q : ptrs) {
-        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
-        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
-            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
-    }
-    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
-    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
-    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
-        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
-    const unsigned long long b = B, l = L, t = T, e = n_embd;
-    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
-    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
-    if (workspace_bytes < need)
-        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
-    const Span spans[] = {
-        {"x", x, b * l * t * e * 4, false},
-        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
-        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
-        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
-        {"z", z, b * l * t * gdn::kValueDim * 4, true},
-        {"workspace", workspace, need, true},
-    };
-    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
-    for (int i = 0; i < n; ++i) {
-        if (!spans[i].output) continue;
-        for (int k = 0; k < n; ++k)
-            if (k != i && overlaps(spans[i], spans[k]))
-                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
-    }
-    gdn::ProjArgs a;
-    a.x = x;
-    a.w_qkv = w_qkv;
-    a.w_gate = w_gate;
-    a.qkv = qkv;
-    a.z = z;
-    a.workspace = workspace;
-    a.B = B;
-    a.L = L;
-    a.T = T;
-    a.n_embd = n_embd;
-    const cudaError_t err = gdn::launch_in_proj(a, static_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
-    return GDN_OK;
+    ProjCall c;
+    c.fn = "gdn_in_proj";
+    c.x = x;
+    c.w_qkv = w_qkv;
+    c.w_gate = w_gate;
+    c.qkv = qkv;
+    c.z = z;
+    c.workspace = workspace;
+    c.workspace_bytes = workspace_bytes;
+    c.B = B;
+    c.L = L;
+    c.T = T;
+    c.n_embd = n_embd;
+    return run_proj(c, stream);
 }
 
 gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, const uint16_t* w_alpha,
@@ -371,121 +385,45 @@ gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t
                            float* gate, float* beta, void* workspace, size_t workspace_bytes, int B, int L, int T,
                            int n_embd, void* stream) {
     t_last_error.clear();
-    const char* fn = "gdn_step_inputs";
-    const struct {
-        const char* name;
-        const void* p;
-    } ptrs[] = {{"x", x},     {"w_qkv", w_qkv}, {"w_gate", w_gate}, {"w_alpha", w_alpha},      {"w_beta", w_beta},
-                {"dt", dt},   {"ssm_a", ssm_a}, {"qkv", qkv},       {"z", z},                  {"gate", gate},
-                {"beta", beta}, {"workspace", workspace}};
-    for (const auto& q : ptrs) {
-        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
-        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
-            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
-    }
-    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
-    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
-    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
-        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
-    const unsigned long long b = B, l = L, t = T, e = n_embd;
-    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
-    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
-    if (workspace_bytes < need)
-        return fail(GDN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
-    const Span spans[] = {
-        {"x", x, b * l * t * e * 4, false},
-        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
-        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
-        {"w_alpha", w_alpha, l * gdn::kVHeads * e * 2, false},
-        {"w_beta", w_beta, l * gdn::kVHeads * e * 2, false},
-        {"dt", dt, l * gdn::kVHeads * 4, false},
-        {"ssm_a", ssm_a, l * gdn::kVHeads * 4, false},
-        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
-        {"z", z, b * l * t * gdn::kValueDim * 4, true},
-        {"gate", gate, b * l * t * gdn::kVHeads * 4, true},
-        {"beta", beta, b * l * t * gdn::kVHeads * 4, true},
-        {"workspace", workspace, need, true},
-    };
-    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
-    for (int i = 0; i < n; ++i) {
-        if (!spans[i].output) continue;
-        for (int k = 0; k < n; ++k)
-            if (k != i && overlaps(spans[i], spans[k]))
-                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
-    }
-    gdn::ProjArgs a;
-    a.x = x;
-    a.w_qkv = w_qkv;
-    a.w_gate = w_gate;
-    a.qkv = qkv;
-    a.z = z;
-    a.workspace = workspace;
-    a.B = B;
-    a.L = L;
-    a.T = T;
-    a.n_embd = n_embd;
-    a.w_alpha = w_alpha;
-    a.w_beta = w_beta;
-    a.dt = dt;
-    a.ssm_a = ssm_a;
-    a.gate = gate;
-    a.beta = beta;
-    const cudaError_t err = gdn::launch_in_proj(a, static_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
-    return GDN_OK;
+    ProjCall c;
+    c.fn = "gdn_step_inputs";
+    c.x = x;
+    c.w_qkv = w_qkv;
+    c.w_gate = w_gate;
+    c.w_alpha = w_alpha;
+    c.w_beta = w_beta;
+    c.dt = dt;
+    c.ssm_a = ssm_a;
+    c.qkv = qkv;
+    c.z = z;
+    c.gate = gate;
+    c.beta = beta;
+    c.workspace = workspace;
+    c.workspace_bytes = workspace_bytes;
+    c.B = B;
+    c.L = L;
+    c.T = T;
+    c.n_embd = n_embd;
+    c.with_ab = true;
+    return run_proj(c, stream);
 }
 
 gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                                int B, int L, int T, int n_embd, void* stream) {
     t_last_error.clear();
-    const char* fn = "gdn_in_proj_noalloc";
-    const struct {
-        const char* name;
-        const void* p;
-    } ptrs[] = {{"x", x}, {"w_qkv", w_qkv}, {"w_gate", w_gate}, {"qkv", qkv}, {"z", z}};
-    for (const auto& q : ptrs) {
-        if (q.p == nullptr) return fail(GDN_ERR_NULL, "%s: %s is NULL", fn, q.name);
-        if ((reinterpret_cast<unsigned long long>(q.p) & 15ull) != 0)
-            return fail(GDN_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, q.name);
-    }
-    if (B < 1 || L < 1 || L > 65535) return fail(GDN_ERR_SHAPE, "%s: B=%d and L=%d out of range", fn, B, L);
-    if (T < 1 || T > gdn::kMaxT) return fail(GDN_ERR_SHAPE, "%s: T=%d must be in [1, %d]", fn, T, gdn::kMaxT);
-    if (n_embd < 64 || n_embd > 65536 || n_embd % 64 != 0)
-        return fail(GDN_ERR_SHAPE, "%s: n_embd=%d must be a multiple of 64 in [64, 65536]", fn, n_embd);
-    const unsigned long long b = B, l = L, t = T, e = n_embd;
-    if (b * t > (1ull << 30)) return fail(GDN_ERR_SHAPE, "%s: B*T is too large", fn);
-    const size_t need = gdn::proj_workspace_bytes(B, L, T, n_embd);
-    if (need > gdn::proj_static_scratch_bytes())
-        return fail(GDN_ERR_SHAPE, "%s: these sizes need %zu bytes of scratch, the library holds %zu", fn, need,
-                    gdn::proj_static_scratch_bytes());
-    const Span spans[] = {
-        {"x", x, b * l * t * e * 4, false},
-        {"w_qkv", w_qkv, l * gdn::kConvChannels * e * 2, false},
-        {"w_gate", w_gate, l * gdn::kValueDim * e * 2, false},
-        {"qkv", qkv, b * l * t * gdn::kConvChannels * 4, true},
-        {"z", z, b * l * t * gdn::kValueDim * 4, true},
-    };
-    const int n = static_cast<int>(sizeof(spans) / sizeof(spans[0]));
-    for (int i = 0; i < n; ++i) {
-        if (!spans[i].output) continue;
-        for (int k = 0; k < n; ++k)
-            if (k != i && overlaps(spans[i], spans[k]))
-                return fail(GDN_ERR_ALIAS, "%s: output %s overlaps %s", fn, spans[i].name, spans[k].name);
-    }
-    gdn::ProjArgs a;
-    a.x = x;
-    a.w_qkv = w_qkv;
-    a.w_gate = w_gate;
-    a.qkv = qkv;
-    a.z = z;
-    a.workspace = nullptr;
-    a.B = B;
-    a.L = L;
-    a.T = T;
-    a.n_embd = n_embd;
-    const cudaError_t err = gdn::launch_in_proj_static(a, static_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return fail(GDN_ERR_CUDA, "%s: CUDA error: %s", fn, cudaGetErrorString(err));
-    return GDN_OK;
+    ProjCall c;
+    c.fn = "gdn_in_proj_noalloc";
+    c.x = x;
+    c.w_qkv = w_qkv;
+    c.w_gate = w_gate;
+    c.qkv = qkv;
+    c.z = z;
+    c.B = B;
+    c.L = L;
+    c.T = T;
+    c.n_embd = n_embd;
+    c.scratch = true;
+    return run_proj(c, stream);
 }
 
 const char* gdn_last_error(void) { return t_last_error.c_str(); }
@@ -568,16 +506,47 @@ gdn_status gdn_in_proj_packed(const float* x, const void* packed, size_t packed_
                               void* workspace, size_t workspace_bytes, int B, int L, int T, int n_embd,
                               void* stream) {
     t_last_error.clear();
-    return run_packed("gdn_in_proj_packed", x, packed, packed_bytes, nullptr, nullptr, qkv, z, nullptr, nullptr,
-                      workspace, workspace_bytes, B, L, T, n_embd, stream, false);
+    ProjCall c;
+    c.fn = "gdn_in_proj_packed";
+    c.x = x;
+    c.packed = packed;
+    c.packed_bytes = packed_bytes;
+    c.qkv = qkv;
+    c.z = z;
+    c.workspace = workspace;
+    c.workspace_bytes = workspace_bytes;
+    c.B = B;
+    c.L = L;
+    c.T = T;
+    c.n_embd = n_embd;
+    c.use_packed = true;
+    return run_proj(c, stream);
 }
 
 gdn_status gdn_step_inputs_packed(const float* x, const void* packed, size_t packed_bytes, const float* dt,
                                   const float* ssm_a, float* qkv, float* z, float* gate, float* beta, void* workspace,
                                   size_t workspace_bytes, int B, int L, int T, int n_embd, void* stream) {
     t_last_error.clear();
-    return run_packed("gdn_step_inputs_packed", x, packed, packed_bytes, dt, ssm_a, qkv, z, gate, beta, workspace,
-                      workspace_bytes, B, L, T, n_embd, stream, true);
+    ProjCall c;
+    c.fn = "gdn_step_inputs_packed";
+    c.x = x;
+    c.packed = packed;
+    c.packed_bytes = packed_bytes;
+    c.dt = dt;
+    c.ssm_a = ssm_a;
+    c.qkv = qkv;
+    c.z = z;
+    c.gate = gate;
+    c.beta = beta;
+    c.workspace = workspace;
+    c.workspace_bytes = workspace_bytes;
+    c.B = B;
+    c.L = L;
+    c.T = T;
+    c.n_embd = n_embd;
+    c.with_ab = true;
+    c.use_packed = true;
+    return run_proj(c, stream);
 }
 
 }  // extern "C"
