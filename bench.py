@@ -56,11 +56,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
-    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj", "step_inputs", "mixer"],
+    ap.add_argument("--op", default="step", choices=["step", "ab_gates", "in_proj", "step_inputs", "mixer", "verify"],
                     help="step: the decode step (the default bench line); ab_gates: the fused alpha/beta projection; "
                          "in_proj: the qkv and z input projections on the tensor cores; step_inputs: qkv, z and "
                          "the alpha/beta gates in one tensor-core pass; mixer: step_inputs then the decode step "
-                         "on its outputs, from the layer input x to y")
+                         "on its outputs, from the layer input x to y; verify: a two-phase verify window "
+                         "(gdn_verify_window over every sequence's draft tokens, then gdn_verify_commit of a "
+                         "seeded number of accepted tokens)")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(W.WORKLOADS))
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
@@ -680,6 +682,74 @@ def run_mixer(args, w):
     }), flush=True)
 
 
+def run_verify(args, w):
+    """Times the two-phase verify window: gdn_verify_window (y for every sequence's draft tokens,
+    the state read only) then gdn_verify_commit (the state advanced by n_keep[b] accepted tokens,
+    drawn per sequence from U{0..len[b]} with a fixed seed), K pairs in one captured graph."""
+    import gated_deltanet_linear_step_gb300 as g
+
+    g.load_library()
+    dev = torch.device("cuda", 0)
+    B, L, T = w.B, w.L, w.T
+    t = W.device_inputs(w, dev, threads=16)
+    lens = W.seq_lens(w)
+    lens = np.full(B, T, np.int32) if lens is None else lens
+    keep = np.random.default_rng(w.seed + 1).integers(0, lens + 1).astype(np.int32)
+    seq_len = torch.from_numpy(lens).to(dev)
+    n_keep = torch.from_numpy(keep).to(dev)
+    y = torch.empty(t["z"].shape, device=dev)
+
+    def step():
+        g.gdn_verify_window(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"],
+                            t["conv_state"], t["state"], y, seq_len=seq_len)
+        g.gdn_verify_commit(t["qkv"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"], t["conv_state"],
+                            t["state"], n_keep)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clocks:
+        clocks.mark_start()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize(dev)
+        clocks.mark_end()
+    assert g.gdn_read_device_error(device=dev) == 0, "a kernel reported a device error"
+    ms = a.elapsed_time(b) / args.steps
+    drafted = int(lens.sum()) * L
+    kept = int(keep.sum()) * L
+    tile = 48 * 128 * 128 * 4
+    conv = 10240 * 3 * 4
+    weights = L * (10240 * 4 + 48 + 48 + 128) * 4
+    # window: every tile and conv history read, the drafted tokens' inputs read and their y written;
+    # commit: the tiles and histories of sequences that keep a token read and written, the kept
+    # tokens' qkv, alpha and beta read.
+    advanced = int((keep > 0).sum()) * L
+    window_bytes = B * L * (tile + conv) + drafted * (10240 + 6144 + 48 + 48 + 6144) * 4 + weights
+    commit_bytes = advanced * 2 * (tile + conv) + kept * (10240 + 48 + 48) * 4 + weights
+    peak, peak_kind = measured_peaks()
+    gbs = (window_bytes + commit_bytes) / (ms / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "verified draft tokens (seq*layer*token) per second, window + commit",
+        "op": "verify", "value": drafted / (ms / 1e3), "unit": "draft-tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "L": L, "T": T, "drafted_per_layer": int(lens.sum()),
+                   "kept_per_layer": int(keep.sum()),
+                   "n_keep": "per sequence from U{0..len[b]}, numpy default_rng(seed + 1)",
+                   "timing": f"{args.steps} x (gdn_verify_window + gdn_verify_commit) in one captured CUDA graph"},
+        "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": peak_kind, "bytes_per_step": window_bytes + commit_bytes,
+                     "window_bytes": window_bytes, "commit_bytes": commit_bytes},
+    }), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -697,6 +767,9 @@ def main():
     elif args.op in ("in_proj", "step_inputs"):
         if rank == 0:
             run_in_proj(args, base, with_ab=args.op == "step_inputs")
+    elif args.op == "verify":
+        if rank == 0:
+            run_verify(args, base)
     elif args.op == "mixer":
         if rank == 0:
             run_mixer(args, base)
