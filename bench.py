@@ -68,7 +68,7 @@ def parse():
                     help="sequences per GPU (default: the workload's B); smaller values are for profiling")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers (default: the workload's L); smaller values are for profiling")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--timing", default="graph", choices=["graph", "direct"],
                     help="graph: the K timed steps are one captured CUDA graph (no host gaps between launches); "
                          "direct: K calls from Python")
@@ -270,8 +270,8 @@ class ClockSampler:
 
 # ----------------------------------------------------------- cpu legs ----
 def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None):
-    """Times the oracle on (sequence, layer) slices of the workload until the budget
-    is spent. Returns (updates done, oracle seconds, slices)."""
+    """Times the oracle on (sequence, layer) slices of the workload until `seconds` of oracle time
+    have passed. Returns (updates done, oracle seconds, slices)."""
     import oracle
 
     lens = W.seq_lens(w)
