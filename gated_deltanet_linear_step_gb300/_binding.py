@@ -222,8 +222,7 @@ def gdn_ab_gates(x, w_alpha, w_beta, dt, ssm_a, gate, beta, stream=None):
     B, L, T, E = (int(v) for v in x.shape)
     dev = x.device
     for name, w in (("w_alpha", w_alpha), ("w_beta", w_beta)):
-        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+        _bf16_weight(w, name)
     p = [
         _ptr(x, "x", (B, L, T, E), device=dev),
         _ptr(w_alpha, "w_alpha", (L, V_HEADS, E), dtype=w_alpha.dtype, device=dev),
@@ -235,6 +234,12 @@ def gdn_ab_gates(x, w_alpha, w_beta, dt, ssm_a, gate, beta, stream=None):
     ]
     with torch.cuda.device(dev):
         _check(lib.gdn_ab_gates(*p, B, L, T, E, _stream_handle(stream, dev)))
+
+
+def _bf16_weight(w, name):
+    if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+    return w
 
 
 def gdn_in_proj_workspace_size(B: int, L: int, T: int, n_embd: int) -> int:
@@ -253,8 +258,7 @@ def gdn_in_proj(x, w_qkv, w_gate, qkv, z, workspace, stream=None):
     B, L, T, E = (int(v) for v in x.shape)
     dev = x.device
     for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate)):
-        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+        _bf16_weight(w, name)
     if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
         raise TypeError("workspace must be a 1-D torch.uint8 tensor")
     p = [
@@ -279,8 +283,7 @@ def gdn_step_inputs(x, w_qkv, w_gate, w_alpha, w_beta, dt, ssm_a, qkv, z, gate, 
     B, L, T, E = (int(v) for v in x.shape)
     dev = x.device
     for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate), ("w_alpha", w_alpha), ("w_beta", w_beta)):
-        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+        _bf16_weight(w, name)
     if not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8 or workspace.dim() != 1:
         raise TypeError("workspace must be a 1-D torch.uint8 tensor")
     p = [
@@ -310,8 +313,7 @@ def gdn_in_proj_noalloc(x, w_qkv, w_gate, qkv, z, stream=None):
     B, L, T, E = (int(v) for v in x.shape)
     dev = x.device
     for name, w in (("w_qkv", w_qkv), ("w_gate", w_gate)):
-        if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-            raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
+        _bf16_weight(w, name)
     p = [
         _ptr(x, "x", (B, L, T, E), device=dev),
         _ptr(w_qkv, "w_qkv", (L, CONV_CHANNELS, E), dtype=w_qkv.dtype, device=dev),
@@ -326,12 +328,6 @@ def gdn_in_proj_noalloc(x, w_qkv, w_gate, qkv, z, stream=None):
 def gdn_proj_pack_bytes(L: int, n_embd: int) -> int:
     """Bytes of the packed projection weights of L layers (0 for sizes out of range)."""
     return int(load_library().gdn_proj_pack_bytes(int(L), int(n_embd)))
-
-
-def _bf16_weight(w, name):
-    if not isinstance(w, torch.Tensor) or w.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
-        raise TypeError(f"{name} must hold BF16 values (torch.bfloat16) or their 16-bit patterns")
-    return w
 
 
 def _packed(packed, dev):
