@@ -9,13 +9,15 @@
 //
 // x is read once for both projections. Per layer this is a small GEMM:
 // [rows = B*T] x [n_embd] times [n_embd] x [96]. A cluster of kSplit CTAs takes
-// 16 rows of one layer, each CTA a contiguous share of n_embd. x and both
+// 32 rows of one layer, each CTA a contiguous share of n_embd. x and both
 // weight blocks stream through double-buffered shared memory in 64-wide
 // slices by 16-byte asynchronous copies (weight rows padded to 144 bytes, so a
 // thread reads eight weights of an output with one 16-byte load), and each of
-// the 128 threads accumulates 2 rows x 6 outputs in fp32 registers. Rank 0 then
-// adds the other ranks' partial sums, read from their shared memory across
-// the cluster, and applies the gate epilogue; no global workspace is involved.
+// the 128 threads accumulates 4 rows x 6 outputs in fp32 registers, so every
+// weight load feeds 32 FMAs. The partial sums then go to the weight buffers,
+// which the main loop no longer needs; rank 0 adds the other ranks' sums, read
+// from their shared memory across the cluster, and applies the gate epilogue.
+// No global workspace is involved.
 
 #include <cuda_bf16.h>
 
@@ -26,7 +28,7 @@ namespace gdn {
 namespace {
 
 constexpr int kAbThreads = 128;
-constexpr int kRowsPerCta = 16;
+constexpr int kRowsPerCta = 32;
 constexpr int kOut = 2 * kVHeads;  // 96: alpha heads, then beta heads
 constexpr int kKSlice = 64;        // n_embd elements per shared-memory slice
 constexpr int kSplit = 4;          // CTAs per cluster, each summing a share of n_embd
@@ -45,7 +47,9 @@ struct AbParams {
 __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_constant__ AbParams p) {
     __shared__ __align__(16) float xs[2][kRowsPerCta][kKSlice];          // 8 KB, double-buffered
     __shared__ __align__(16) __nv_bfloat16 ws[2][kOut][kKSlice + 8];    // 27 KB, rows padded to 144 bytes
-    __shared__ __align__(16) float part[kAbThreads][12];               // 6 KB: this CTA's partial sums
+    // This CTA's partial sums, in the weight buffers once the main loop is done with them.
+    float (*part)[24] = reinterpret_cast<float (*)[24]>(&ws[0][0][0]);
+    static_assert(sizeof(ws) >= sizeof(float) * kAbThreads * 24, "partial sums fit in the weight buffers");
 
     const int tid = threadIdx.x;
     const int l = blockIdx.y;
@@ -54,7 +58,7 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
     const int m0 = (blockIdx.x / kSplit) * kRowsPerCta;
     const int n_slices = p.E / kKSlice;
     const int s_begin = n_slices * rank / kSplit, s_end = n_slices * (rank + 1) / kSplit;
-    const int mp = tid >> 4;                 // row pair 0..7 -> rows 2 mp, 2 mp + 1
+    const int mp = tid >> 4;                 // row quad 0..7 -> rows 4 mp .. 4 mp + 3
     const int n0 = (tid & 15) * 6;           // first of six outputs
 
     // Global row of layer-local row m (m = b * T + t).
@@ -63,9 +67,9 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
         return p.x + ((static_cast<size_t>(b) * p.L + l) * p.T + t) * p.E;
     };
 
-    float acc[2][6];
+    float acc[4][6];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 6; ++j) acc[i][j] = 0.f;
 
@@ -99,11 +103,11 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
         __syncthreads();
 #pragma unroll 2
         for (int k = 0; k < kKSlice; k += 8) {
-            float xv[2][8];
+            float xv[4][8];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float4 a = *reinterpret_cast<const float4*>(&xs[buf][2 * mp + i][k]);
-                const float4 b = *reinterpret_cast<const float4*>(&xs[buf][2 * mp + i][k + 4]);
+            for (int i = 0; i < 4; ++i) {
+                const float4 a = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k]);
+                const float4 b = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k + 4]);
                 xv[i][0] = a.x; xv[i][1] = a.y; xv[i][2] = a.z; xv[i][3] = a.w;
                 xv[i][4] = b.x; xv[i][5] = b.y; xv[i][6] = b.z; xv[i][7] = b.w;
             }
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
                 for (int e = 0; e < 4; ++e) {
                     const float2 w = __bfloat1622float2(w2[e]);
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
+                    for (int i = 0; i < 4; ++i) {
                         acc[i][j] = fmaf(xv[i][2 * e], w.x, acc[i][j]);
                         acc[i][j] = fmaf(xv[i][2 * e + 1], w.y, acc[i][j]);
                     }
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
 
     // Partial sums meet on rank 0.
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 6; ++j) part[tid][6 * i + j] = acc[i][j];
     cluster_sync();
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
         for (int r = 1; r < kSplit; ++r) {
             const uint32_t remote = cluster_map(smem_addr(&part[tid][0]), r);
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 6; ++j) {
                     float v;
@@ -148,8 +152,8 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
     if (rank != 0) return;
 
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int m = m0 + 2 * mp + i;
+    for (int i = 0; i < 4; ++i) {
+        const int m = m0 + 4 * mp + i;
         if (m >= M) continue;
         const int b = m / p.T, t = m - (m / p.T) * p.T;
         const size_t row = ((static_cast<size_t>(b) * p.L + l) * p.T + t) * kVHeads;
