@@ -15,9 +15,11 @@
 // thread reads eight weights of an output with one 16-byte load), and each of
 // the 128 threads accumulates 4 rows x 6 outputs in fp32 registers, so every
 // weight load feeds 32 FMAs. The partial sums then go to the weight buffers,
-// which the main loop no longer needs; rank 0 adds the other ranks' sums, read
-// from their shared memory across the cluster, and applies the gate epilogue.
-// No global workspace is involved.
+// which the main loop no longer needs, and meet in a reduce-scatter: rank r of
+// the cluster adds the other ranks' sums for row r of each thread's four rows,
+// read from their shared memory across the cluster with every load issued
+// before any sum uses it, and applies the gate epilogue to that row. No global
+// workspace is involved.
 
 #include <cuda_bf16.h>
 
@@ -44,7 +46,7 @@ struct AbParams {
     int B, L, T, E;
 };
 
-__global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_constant__ AbParams p) {
+__global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __grid_constant__ AbParams p) {
     __shared__ __align__(16) float xs[2][kRowsPerCta][kKSlice];          // 8 KB, double-buffered
     __shared__ __align__(16) __nv_bfloat16 ws[2][kOut][kKSlice + 8];    // 27 KB, rows padded to 144 bytes
     // This CTA's partial sums, in the weight buffers once the main loop is done with them.
@@ -129,45 +131,51 @@ __global__ void __launch_bounds__(kAbThreads) gdn_ab_gates_kernel(const __grid_c
         __syncthreads();  // the buffer is refilled two slices later
     }
 
-    // Partial sums meet on rank 0.
+    // Partial sums meet across the cluster.
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 6; ++j) part[tid][6 * i + j] = acc[i][j];
     cluster_sync();
-    if (rank == 0) {
-        for (int r = 1; r < kSplit; ++r) {
-            const uint32_t remote = cluster_map(smem_addr(&part[tid][0]), r);
+    // Reduce-scatter: rank r finishes row 4 mp + r of each thread's four rows, adding the
+    // other ranks' partial sums (two floats per load, all issued before any sum uses them).
+    static_assert(kSplit == 4, "one row of a thread's four per rank");
+    float2 rv[kSplit - 1][3];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+    for (int o = 1; o < kSplit; ++o) {
+        const uint32_t remote = cluster_map(smem_addr(&part[tid][6 * rank]), (rank + o) % kSplit);
 #pragma unroll
-                for (int j = 0; j < 6; ++j) {
-                    float v;
-                    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote + 4 * (6 * i + j)));
-                    acc[i][j] += v;
-                }
-        }
+        for (int q = 0; q < 3; ++q)
+            asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                         : "=f"(rv[o - 1][q].x), "=f"(rv[o - 1][q].y)
+                         : "r"(remote + 8 * q));
     }
-    cluster_sync();  // the other ranks' partial sums stay in place until rank 0 has read them
-    if (rank != 0) return;
-
+    float sum[6];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int m = m0 + 4 * mp + i;
-        if (m >= M) continue;
+    for (int j = 0; j < 6; ++j) sum[j] = part[tid][6 * rank + j];
+#pragma unroll
+    for (int o = 0; o < kSplit - 1; ++o)
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            sum[2 * q] += rv[o][q].x;
+            sum[2 * q + 1] += rv[o][q].y;
+        }
+    const int m = m0 + 4 * mp + rank;
+    if (m < M) {
         const int b = m / p.T, t = m - (m / p.T) * p.T;
         const size_t row = ((static_cast<size_t>(b) * p.L + l) * p.T + t) * kVHeads;
 #pragma unroll
         for (int j = 0; j < 6; ++j) {
             const int n = n0 + j;
             if (n < kVHeads) {
-                p.gate[row + n] = softplusf_(acc[i][j] + p.dt[static_cast<size_t>(l) * kVHeads + n]) *
+                p.gate[row + n] = softplusf_(sum[j] + p.dt[static_cast<size_t>(l) * kVHeads + n]) *
                                   p.ssm_a[static_cast<size_t>(l) * kVHeads + n];
             } else {
-                p.beta[row + n - kVHeads] = sigmoidf_(acc[i][j]);
+                p.beta[row + n - kVHeads] = sigmoidf_(sum[j]);
             }
         }
     }
+    cluster_sync();  // no CTA leaves while another may still read its partial sums
 }
 
 }  // namespace
