@@ -24,7 +24,7 @@ def _rows_rel_err(g, r):
     return float(np.max(np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)))
 
 
-@pytest.mark.parametrize("B,L,T,E", [(3, 2, 1, 2560), (2, 3, 5, 2560), (17, 1, 1, 128), (1, 1, 33, 64)])
+@pytest.mark.parametrize("B,L,T,E", [(3, 2, 1, 2560), (2, 3, 5, 2560), (17, 1, 1, 128), (1, 1, 33, 64), (64, 2, 1, 2560)])
 def test_ab_gates_match_oracle(cuda_device, B, L, T, E):
     import gated_deltanet_linear_step_gb300 as g
 
