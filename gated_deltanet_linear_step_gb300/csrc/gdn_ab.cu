@@ -10,9 +10,11 @@
 // x is read once for both projections. Per layer this is a small GEMM:
 // [rows = B*T] x [n_embd] times [n_embd] x [96]. A cluster of kSplit CTAs takes
 // 32 rows of one layer, each CTA a contiguous share of n_embd. x and both
-// weight blocks stream through double-buffered shared memory in 64-wide
-// slices by 16-byte asynchronous copies (weight rows padded to 144 bytes, so a
-// thread reads eight weights of an output with one 16-byte load), and each of
+// weight blocks stream through double-buffered shared memory (83 KB, dynamic)
+// in 128-wide slices by 16-byte asynchronous copies; a share of an odd number
+// of 64-wide units ends with one 64-wide slice, and both widths are compiled
+// separately. Weight rows are padded by 16 bytes, so a thread reads eight
+// weights of an output with one 16-byte load. Each of
 // the 128 threads accumulates 4 rows x 6 outputs in fp32 registers, so every
 // weight load feeds 32 FMAs. The partial sums then go to the weight buffers,
 // which the main loop no longer needs, and meet in a reduce-scatter: rank r of
@@ -23,6 +25,9 @@
 
 #include <cuda_bf16.h>
 
+#include <mutex>
+#include <type_traits>
+
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
 
@@ -32,8 +37,12 @@ namespace {
 constexpr int kAbThreads = 128;
 constexpr int kRowsPerCta = 32;
 constexpr int kOut = 2 * kVHeads;  // 96: alpha heads, then beta heads
-constexpr int kKSlice = 64;        // n_embd elements per shared-memory slice
+constexpr int kKSlice = 128;       // n_embd elements per shared-memory slice
 constexpr int kSplit = 4;          // CTAs per cluster, each summing a share of n_embd
+
+using XsBuf = float[2][kRowsPerCta][kKSlice];
+using WsBuf = __nv_bfloat16[2][kOut][kKSlice + 8];
+constexpr size_t kAbSmem = sizeof(XsBuf) + sizeof(WsBuf);
 
 struct AbParams {
     const float* x;          // [B][L][T][E]
@@ -47,8 +56,9 @@ struct AbParams {
 };
 
 __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __grid_constant__ AbParams p) {
-    __shared__ __align__(16) float xs[2][kRowsPerCta][kKSlice];          // 8 KB, double-buffered
-    __shared__ __align__(16) __nv_bfloat16 ws[2][kOut][kKSlice + 8];    // 27 KB, rows padded to 144 bytes
+    extern __shared__ __align__(16) unsigned char ab_smem[];
+    auto& xs = *reinterpret_cast<XsBuf*>(ab_smem);                  // double-buffered x slices
+    auto& ws = *reinterpret_cast<WsBuf*>(ab_smem + sizeof(XsBuf));  // weight slices, rows padded by 16 bytes
     // This CTA's partial sums, in the weight buffers once the main loop is done with them.
     float (*part)[24] = reinterpret_cast<float (*)[24]>(&ws[0][0][0]);
     static_assert(sizeof(ws) >= sizeof(float) * kAbThreads * 24, "partial sums fit in the weight buffers");
@@ -58,8 +68,14 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
     const int rank = static_cast<int>(cluster_rank());
     const int M = p.B * p.T;                 // rows of this layer
     const int m0 = (blockIdx.x / kSplit) * kRowsPerCta;
-    const int n_slices = p.E / kKSlice;
-    const int s_begin = n_slices * rank / kSplit, s_end = n_slices * (rank + 1) / kSplit;
+    // This rank's share of n_embd, in 64-wide units, taken kKSlice wide at a time: when the share
+    // is an odd number of units, its last slice is 64 wide.
+    constexpr int kUnit = 64;
+    const int n_units = p.E / kUnit;
+    const int u_begin = n_units * rank / kSplit, u_end = n_units * (rank + 1) / kSplit;
+    const int per = kKSlice / kUnit;
+    const int s_begin = 0, s_end = (u_end - u_begin + per - 1) / per;  // slices of this rank
+    auto slice_width = [&](int sl) { return min(kKSlice, (u_end - u_begin - sl * per) * kUnit); };
     const int mp = tid >> 4;                 // row quad 0..7 -> rows 4 mp .. 4 mp + 3
     const int n0 = (tid & 15) * 6;           // first of six outputs
 
@@ -76,21 +92,26 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
         for (int j = 0; j < 6; ++j) acc[i][j] = 0.f;
 
     // Slice loads: 16-byte asynchronous copies into buffer `buf`.
-    auto load_slice = [&](int sl, int buf) {
-        const int k0 = sl * kKSlice;
-        for (int i = tid; i < kRowsPerCta * kKSlice / 4; i += kAbThreads) {
-            const int r = i / (kKSlice / 4), c = (i % (kKSlice / 4)) * 4;
+    auto load_w = [&](int sl, int buf, auto width_c) {
+        constexpr int width = decltype(width_c)::value;
+        const int k0 = (u_begin + sl * per) * kUnit;
+        for (int i = tid; i < kRowsPerCta * width / 4; i += kAbThreads) {
+            const int r = i / (width / 4), c = (i % (width / 4)) * 4;
             const int m = m0 + r < M ? m0 + r : M - 1;  // rows past M read a valid row; their sums are not stored
             cp_async16(smem_addr(&xs[buf][r][c]), x_row(m) + k0 + c);
         }
-        for (int i = tid; i < kOut * kKSlice / 8; i += kAbThreads) {
-            const int n = i / (kKSlice / 8), c = (i % (kKSlice / 8)) * 8;
+        for (int i = tid; i < kOut * width / 8; i += kAbThreads) {
+            const int n = i / (width / 8), c = (i % (width / 8)) * 8;
             const uint16_t* src = (n < kVHeads ? p.wa + (static_cast<size_t>(l) * kVHeads + n) * p.E
                                                : p.wb + (static_cast<size_t>(l) * kVHeads + n - kVHeads) * p.E) +
                                   k0 + c;
             cp_async16(smem_addr(&ws[buf][n][c]), src);
         }
         cp_async_commit();
+    };
+    auto load_slice = [&](int sl, int buf) {
+        if (slice_width(sl) == kKSlice) load_w(sl, buf, std::integral_constant<int, kKSlice>{});
+        else load_w(sl, buf, std::integral_constant<int, kUnit>{});
     };
 
     if (s_begin < s_end) load_slice(s_begin, 0);
@@ -103,31 +124,36 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
             cp_async_wait_all();
         }
         __syncthreads();
+        auto compute = [&](auto width_c) {
+            constexpr int width = decltype(width_c)::value;
 #pragma unroll 2
-        for (int k = 0; k < kKSlice; k += 8) {
-            float xv[4][8];
+            for (int k = 0; k < width; k += 8) {
+                float xv[4][8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 a = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k]);
-                const float4 b = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k + 4]);
-                xv[i][0] = a.x; xv[i][1] = a.y; xv[i][2] = a.z; xv[i][3] = a.w;
-                xv[i][4] = b.x; xv[i][5] = b.y; xv[i][6] = b.z; xv[i][7] = b.w;
-            }
+                for (int i = 0; i < 4; ++i) {
+                    const float4 a = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k]);
+                    const float4 b = *reinterpret_cast<const float4*>(&xs[buf][4 * mp + i][k + 4]);
+                    xv[i][0] = a.x; xv[i][1] = a.y; xv[i][2] = a.z; xv[i][3] = a.w;
+                    xv[i][4] = b.x; xv[i][5] = b.y; xv[i][6] = b.z; xv[i][7] = b.w;
+                }
 #pragma unroll
-            for (int j = 0; j < 6; ++j) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(&ws[buf][n0 + j][k]);
-                const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                for (int j = 0; j < 6; ++j) {
+                    const uint4 raw = *reinterpret_cast<const uint4*>(&ws[buf][n0 + j][k]);
+                    const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 w = __bfloat1622float2(w2[e]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 w = __bfloat1622float2(w2[e]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[i][j] = fmaf(xv[i][2 * e], w.x, acc[i][j]);
-                        acc[i][j] = fmaf(xv[i][2 * e + 1], w.y, acc[i][j]);
+                        for (int i = 0; i < 4; ++i) {
+                            acc[i][j] = fmaf(xv[i][2 * e], w.x, acc[i][j]);
+                            acc[i][j] = fmaf(xv[i][2 * e + 1], w.y, acc[i][j]);
+                        }
                     }
                 }
             }
-        }
+        };
+        if (slice_width(sl) == kKSlice) compute(std::integral_constant<int, kKSlice>{});
+        else compute(std::integral_constant<int, kUnit>{});
         __syncthreads();  // the buffer is refilled two slices later
     }
 
@@ -181,6 +207,21 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
 }  // namespace
 
 cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream) {
+    {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        static std::mutex mutex;
+        static bool ready[64] = {};
+        std::lock_guard<std::mutex> lock(mutex);
+        if (!ready[dev]) {
+            e = cudaFuncSetAttribute(gdn_ab_gates_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kAbSmem));
+            if (e != cudaSuccess) return e;
+            ready[dev] = true;
+        }
+    }
     AbParams p;
     p.x = a.x;
     p.wa = a.w_alpha;
@@ -197,7 +238,7 @@ cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(((M + kRowsPerCta - 1) / kRowsPerCta) * kSplit, a.L, 1);
     cfg.blockDim = dim3(kAbThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = kAbSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
