@@ -2,14 +2,17 @@
 
 One step is one call of the whole decode path (conv, SiLU, norms, gates, the
 gated delta rule, the gated RMSNorm) over one batch of synthetic input: by
-default the batched-decode workload of 64 sequences x 36 layers x 1 token with
-state ~N(0, 0.05). The metric is GDN state updates per second
-(sequence x layer x valid token) together with the achieved HBM bandwidth
-against the measured GB300 copy peak.
+default the large-batch decode workload of 128 sequences x 36 layers x 1 token
+(beta and decay near 1, state ~N(0, 0.05)), the largest of the five workloads.
+The metric is GDN state updates per second (sequence x layer x valid token)
+together with the achieved HBM bandwidth against the measured GB300 copy peak.
+The same run also measures the other four workloads, each on its own, and
+reports them in the line's ``configs`` object.
 
 Timed regions use CUDA events on the launching stream, bracketed by a barrier
-and a device synchronise. The state (7.3 GB at the default workload) is far
-larger than the 129 MB L2, so no step finds its inputs in L2.
+and a device synchronise. The state (14.5 GB at the default workload) is far
+larger than the 129 MB L2, so no step finds its inputs in L2; the one workload
+that fits in L2 is timed call by call with L2 flushed before each call.
 
 ``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
 the same workload, on this machine's host cores.
@@ -41,12 +44,13 @@ sys.path.insert(0, ROOT)
 
 import workloads as W  # noqa: E402
 
-DEFAULT_WORKLOAD = "decode_b64_l36_t1"
+DEFAULT_WORKLOAD = "decode_b128_l36_t1_beta_hi_decay_hi"
 METRIC = "GDN state-updates/sec (seq*layer*token) and achieved HBM GB/s vs GB300 peak"
 UNIT = "state-updates/s"
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_decode_step_kernel_traffic.txt")
-KERNEL_SOURCES = [os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", f)
-                  for f in ("gdn_decode_t1.cu", "gdn_device.cuh")]
+PROFILES = os.path.join(ROOT, "profiles")
+L2_BYTES = 129e6
+L2_NOTE_LARGE = "inputs larger than L2: the working set is far larger than the 129 MB L2; state updated in place"
+L2_NOTE_FLUSH = "working set fits in L2: L2 flushed (512 MB written) before each timed call"
 
 
 # ------------------------------------------------------------------ args --
@@ -77,6 +81,8 @@ def parse():
                          "timed region, the calls on the packed weights timed")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (the line's configs object), e.g. for profiling")
     return ap.parse_args()
 
 
@@ -163,42 +169,59 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def committed_traffic(workload: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel source and workload."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
-    text = open(TRAFFIC_FILE).read()
-    wm = re.search(r"workload:\s*(\S+)", text)
-    if not wm or wm.group(1) != workload:
-        return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    h = re.search(r"kernel_source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or not h:
-        return None
+def kernel_sources(T: int) -> list:
+    """The sources of the kernel a call with T tokens runs (the single-token kernel or the window kernel)."""
+    names = ("gdn_decode_t1.cu", "gdn_device.cuh") if T == 1 else ("gdn_step.cu", "gdn_device.cuh")
+    return [os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", f) for f in names]
+
+
+def committed_traffic(workload: str, T: int):
+    """Per-launch DRAM bytes from a committed ncu summary (``profiles/*traffic*.txt``) taken on this
+    workload and on the kernel source as it stands (its sha256 must match), else None."""
     digest = hashlib.sha256()
-    for path in KERNEL_SOURCES:
+    for path in kernel_sources(T):
         digest.update(open(path, "rb").read())
-    return float(m.group(1)) if h.group(1) == digest.hexdigest() else None
+    want = digest.hexdigest()
+    if not os.path.isdir(PROFILES):
+        return None
+    for fn in sorted(os.listdir(PROFILES)):
+        if "traffic" not in fn or not fn.endswith(".txt"):
+            continue
+        text = open(os.path.join(PROFILES, fn)).read()
+        wm = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        h = re.search(r"^kernel_source_sha256:\s*([0-9a-f]{64})", text, re.M)
+        if wm and m and h and wm.group(1) == workload and h.group(1) == want:
+            return float(m.group(1))
+    return None
 
 
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
-    """Samples SM clocks, power and throttle reasons with nvidia-smi around the timed region.
+    """Samples the SM clock, power and clock-event (throttle) reasons during the timed region.
 
-    A reader thread stamps each sample with the host clock on arrival, and
-    ``summary`` keeps the samples that fall inside [mark_start, mark_end].
+    NVML is read directly (ctypes on libnvidia-ml, read-only queries) every 5 ms by a
+    thread, so even a timed region of a few tens of milliseconds gets samples of its
+    own; without NVML, ``nvidia-smi -lms 50`` is used. ``summary`` keeps the samples
+    that fall inside [mark_start, mark_end].
     """
 
-    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
-    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    # NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+    SMI_QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+    SMI_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    PERIOD_S = 0.005
 
     def __init__(self, device):
         self.device = device
-        self.proc = None
-        self.samples = []
+        self.samples = []  # (host time, sm MHz, max sm MHz, power W, [reason names])
         self.t0 = self.t1 = None
+        self.source = None
+        self._stop = False
+        self.proc = None
+        self.thread = None
 
     def _gpu_id(self):
         try:
@@ -209,24 +232,69 @@ class ClockSampler:
             ids = [v for v in vis.split(",") if v.strip()]
             return ids[self.device.index] if self.device.index < len(ids) else str(self.device.index)
 
-    def __enter__(self):
+    def _start_nvml(self):
+        import ctypes
         import threading
 
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self._gpu_id()}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, FileNotFoundError):
-            self.proc = None
-            return self
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return False
+        handle = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByUUID(self._gpu_id().encode(), ctypes.byref(handle)) != 0:
+            return False
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) != 0:  # 1 = NVML_CLOCK_SM
+            return False
 
         def reader():
-            for line in self.proc.stdout:
-                self.samples.append((time.time(), line))
+            while not self._stop:
+                ok = nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0
+                ok = ok and nv.nvmlDeviceGetPowerUsage(handle, ctypes.byref(pw)) == 0
+                ok = ok and reasons_fn(handle, ctypes.byref(rs)) == 0
+                if ok:
+                    names = [n for bit, n in self.REASON_BITS.items() if rs.value & bit]
+                    self.samples.append((time.time(), float(clk.value), float(mx.value), pw.value / 1000.0, names))
+                time.sleep(self.PERIOD_S)
+            nv.nvmlShutdown()
 
         self.thread = threading.Thread(target=reader, daemon=True)
         self.thread.start()
-        time.sleep(0.3)
+        self.source = "nvml, every 5 ms"
+        return True
+
+    def _start_smi(self):
+        import threading
+
+        self.proc = subprocess.Popen(["nvidia-smi", f"--id={self._gpu_id()}", f"--query-gpu={self.SMI_QUERY}",
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+        def reader():
+            for line in self.proc.stdout:
+                parts = [q.strip() for q in line.split(",")]
+                try:
+                    names = [self.SMI_NAMES[i] for i, v in enumerate(parts[3:7]) if v.lower() == "active"]
+                    self.samples.append((time.time(), float(parts[0]), float(parts[1]), float(parts[2]), names))
+                except (ValueError, IndexError):
+                    continue
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        self.source = "nvidia-smi -lms 50"
+
+    def __enter__(self):
+        try:
+            started = self._start_nvml()
+        except (OSError, AttributeError):
+            started = False
+        if not started:
+            try:
+                self._start_smi()
+            except (OSError, FileNotFoundError):
+                self.source = None
+        time.sleep(0.2)
         return self
 
     def mark_start(self):
@@ -236,42 +304,40 @@ class ClockSampler:
         self.t1 = time.time()
 
     def __exit__(self, *exc):
+        time.sleep(0.02)
+        self._stop = True
         if self.proc is not None:
-            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            try:
-                rows.append((ts, float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
-            except (ValueError, IndexError):
-                continue
+        rows = list(self.samples)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1 + 0.05]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
         note = None
         if not inside:  # timed region shorter than the sampling period: nearest samples
             inside = sorted(rows, key=lambda r: abs(r[0] - (self.t0 or r[0])))[:2]
-            note = "timed region shorter than the 50 ms sampling period; nearest samples"
-        reasons = sorted({self.NAMES[i] for r in inside for i, v in enumerate(r[4]) if v.lower() == "active"})
+            note = "timed region shorter than the sampling period; nearest samples"
+        reasons = sorted({n for r in inside for n in r[4]})
         out = {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
-               "power_w_max": max(r[3] for r in inside), "samples": len(inside), "reasons": reasons}
+               "power_w_max": max(r[3] for r in inside), "samples": len(inside), "reasons": reasons,
+               "source": self.source}
         if note:
             out["note"] = note
         return out
 
 
 # ----------------------------------------------------------- cpu legs ----
-def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None):
+def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None, wall_seconds: float | None = None):
     """Times the oracle on (sequence, layer) slices of the workload until `seconds` of oracle time
-    have passed. Returns (updates done, oracle seconds, slices)."""
+    have passed (or `wall_seconds` of wall time, input generation included). Returns (updates done,
+    oracle seconds, slices)."""
     import oracle
 
     lens = W.seq_lens(w)
@@ -279,8 +345,11 @@ def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None):
     order = [(b, l) for l in range(w.L) for b in range(w.B)]
     rng = np.random.default_rng(7)
     rng.shuffle(order)
+    wall0 = time.perf_counter()
     for b, l in order:
         if spent >= seconds or (max_slices is not None and slices >= max_slices):
+            break
+        if slices > 0 and wall_seconds is not None and time.perf_counter() - wall0 >= wall_seconds:
             break
         sl = W.sequence_slice(w, b, l)
         wt = W.layer_weights(w, l)
@@ -293,31 +362,125 @@ def oracle_sample(w: W.Workload, seconds: float, max_slices: int | None = None):
     return done, spent, slices
 
 
-def run_reference(args, w, world, rank):
+def step_config(w_global: W.Workload, per_rank: W.Workload, world: int) -> dict:
+    """The workload description printed in `config` by both arms (the same keys and values)."""
+    working = algorithmic_bytes(per_rank, W.seq_lens(per_rank))["total"]
+    return {"workload": w_global.name, "B": w_global.B, "L": w_global.L, "T": w_global.T, "B_per_gpu": per_rank.B,
+            "head_dim": 128, "k_heads": 16, "v_heads": 48, "conv_channels": 10240,
+            "l2": L2_NOTE_LARGE if working > 2 * L2_BYTES else L2_NOTE_FLUSH,
+            "parallelism": f"dp{world} (sequences sharded, no collective)"}
+
+
+def run_reference(args, w_global, per_rank, world, rank):
     if rank != 0:
         return
-    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))  # the whole run stays near two minutes
-    per_step = min(per_step, 6.0)
+    # Bounded by wall time (input generation included) so the whole run stays near two minutes.
+    wall_per_step = min(6.0, max(1.0, 100.0 / max(1, args.steps)))
     for _ in range(args.warmup):
-        oracle_sample(w, min(per_step, 1.0))
+        oracle_sample(per_rank, 0.2, wall_seconds=0.5)
     done_total, spent_total, slices_total = 0, 0.0, 0
     for _ in range(args.steps):
-        d, s, n = oracle_sample(w, per_step)
+        d, s_, n = oracle_sample(per_rank, wall_per_step, wall_seconds=wall_per_step)
         done_total += d
-        spent_total += s
+        spent_total += s_
         slices_total += n
     value = done_total / spent_total
-    sample = (f"{slices_total} (sequence, layer) slices of {w.name} over {args.steps} steps "
-              f"(~{per_step:.1f} s of oracle time each), fp64 numpy, one thread")
+    sample = (f"{slices_total} random (sequence, layer) slices of {per_rank.name} over {args.steps} steps "
+              f"(at most {wall_per_step:.1f} s of wall time each, input generation not timed), fp64 numpy, one thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * spent_total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "L": w.L, "T": w.T, "head_dim": 128, "v_heads": 48},
+        "config": step_config(w_global, per_rank, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def make_step(g, t, y):
+    """One decode call on the device tensors `t` (state and conv_state updated in place)."""
+    def step():
+        if t["seq_len"] is None:
+            g.gdn_decode_step(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
+                              t["ssm_norm"], t["conv_state"], t["state"], y)
+        else:
+            g.gdn_decode_step_varlen(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
+                                     t["ssm_norm"], t["conv_state"], t["state"], y, t["seq_len"])
+    return step
+
+
+def roofline_of(w: W.Workload, lens, mean_launch_s: float, traffic) -> dict:
+    """Roofline of one decode call: HBM against the measured copy peak, or the FP32 ALUs when the
+    recurrence's arithmetic (7 flops per state element per token, FMA = 2) bounds the call more
+    tightly than its bytes."""
+    bytes_alg = algorithmic_bytes(w, lens)
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_alg["total"] / mean_launch_s / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_kind": peak_kind, "state_only_gbs": bytes_alg["state"] / mean_launch_s / 1e9,
+            "state_only_frac": bytes_alg["state"] / mean_launch_s / 1e9 / peak,
+            "algorithmic_bytes_per_launch": bytes_alg["total"]}
+    flops = 7.0 * 128 * 128 * 48 * valid_tokens(w, lens)
+    if flops / (ALU_PEAK_TFLOPS * 1e12) > bytes_alg["total"] / (peak * 1e9):
+        tf = flops / mean_launch_s / 1e12
+        roof.update({"bound": "alu", "achieved": tf, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": tf / ALU_PEAK_TFLOPS, "peak_kind": ALU_PEAK_KIND, "hbm_gbs": achieved,
+                     "hbm_frac": achieved / peak, "flops_per_launch": flops})
+    return roof
+
+
+def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
+    """One workload on its own: device-timed decode calls, with the roofline of its kernel.
+    Working sets larger than L2 run `steps` calls from one captured CUDA graph; the one that fits
+    in L2 runs call by call, each after a write of 512 MB that evicts L2, each timed alone."""
+    w = W.WORKLOADS[name]
+    t = W.device_inputs(w, dev, threads=16)
+    lens = W.seq_lens(w)
+    y = torch.empty(t["z"].shape, device=dev)
+    step = make_step(g, t, y)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    working = algorithmic_bytes(w, lens)["total"]
+    if working > 2 * L2_BYTES:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / steps
+        l2 = L2_NOTE_LARGE
+        del graph
+    else:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        times = []
+        for _ in range(steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            times.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+        l2 = L2_NOTE_FLUSH
+        del flush
+    assert g.gdn_read_device_error(device=dev) == 0, f"a kernel reported a device error on {name}"
+    updates = valid_tokens(w, lens)
+    roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T))
+    out = {"workload": name, "B": w.B, "L": w.L, "T": w.T, "steps": steps, "ms_per_step": ms,
+           "value": updates / (ms / 1e3), "unit": UNIT,
+           "kernel": "gdn_decode_t1_kernel" if w.T == 1 else "gdn_window_kernel", "l2": l2, "roofline": roof}
+    del t, y, step
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------- gpu arm ----
@@ -335,14 +498,7 @@ def run_gdn(args, w_global, world, rank, local):
     lens = None if lens_all is None else lens_all[rows[0]:rows[1]]
     y = torch.empty(t["z"].shape, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        if t["seq_len"] is None:
-            g.gdn_decode_step(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
-                              t["ssm_norm"], t["conv_state"], t["state"], y)
-        else:
-            g.gdn_decode_step_varlen(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"],
-                                     t["ssm_norm"], t["conv_state"], t["state"], y, t["seq_len"])
+    step = make_step(g, t, y)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -367,17 +523,18 @@ def run_gdn(args, w_global, world, rank, local):
         if graph is not None:
             graph.replay()
         else:
-            for s, e in ev:
-                s.record(stream)
+            for s_, e_ in ev:
+                s_.record(stream)
                 step()
-                e.record(stream)
+                e_.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         clocks.mark_end()
     barrier(world)
     elapsed_ms = t_start.elapsed_time(t_end)
-    launch_ms = [elapsed_ms / args.steps] if graph is not None else [s.elapsed_time(e) for s, e in ev]
+    launch_ms = [elapsed_ms / args.steps] if graph is not None else [s_.elapsed_time(e_) for s_, e_ in ev]
     assert g.gdn_read_device_error(device=dev) == 0, "the kernel reported a device error"
+    del graph
 
     updates_rank = valid_tokens(w, lens) * args.steps
     total_updates = sum_over_ranks(updates_rank, world, dev)
@@ -412,51 +569,40 @@ def run_gdn(args, w_global, world, rank, local):
                "d2h_bytes_per_step": pipe.out_bytes,
                "method": "wall clock over K steps through the C-ABI host pipeline (gdn_host_pipeline_submit with "
                          "pinned host buffers); copies of neighbouring steps overlap the kernel on separate streams"}
-        del pipe
+        del pipe, host, y_host
 
-    # roofline of the (only) kernel
-    bytes_alg = algorithmic_bytes(w, lens)
-    working_bytes = bytes_alg["total"]
     mean_launch_s = float(np.mean(launch_ms)) / 1000.0
-    peak, peak_kind = measured_peaks()
-    achieved = bytes_alg["total"] / mean_launch_s / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": committed_traffic(w_global.name) if world == 1 else None, "peak_kind": peak_kind,
-                "state_only_gbs": bytes_alg["state"] / mean_launch_s / 1e9,
-                "algorithmic_bytes_per_launch": bytes_alg["total"]}
-    # The recurrence's FP32 work (7 flops per state element per token, FMA = 2) can bound a
-    # multi-token call more tightly than its bytes: report the tighter of the two floors.
-    flops = 7.0 * 128 * 128 * 48 * valid_tokens(w, lens)
-    alu_peak = ALU_PEAK_TFLOPS
-    if flops / (alu_peak * 1e12) > bytes_alg["total"] / (peak * 1e9):
-        tf = flops / mean_launch_s / 1e12
-        roofline.update({"bound": "alu", "achieved": tf, "peak": alu_peak, "unit": "TFLOP/s", "frac": tf / alu_peak,
-                         "peak_kind": ALU_PEAK_KIND, "hbm_gbs": achieved, "hbm_frac": achieved / peak,
-                         "flops_per_launch": flops})
+    roofline = roofline_of(w, lens, mean_launch_s, committed_traffic(w_global.name, w.T) if world == 1 else None)
+    del t, y, step
+    torch.cuda.empty_cache()
+
+    # The other workloads, each measured on its own in this run (rank 0 of a one-GPU run).
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = {}
+        for name in W.WORKLOADS:
+            if name != w_global.name:
+                configs[name] = measure_workload(g, name, args.steps, args.warmup, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        done, spent, slices = oracle_sample(w, args.cpu_seconds)
+        done, spent, slices = oracle_sample(w, args.cpu_seconds, wall_seconds=2.5 * args.cpu_seconds)
         cpu = {"value": done / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{slices} random (sequence, layer) slices of {w.name}, {done} updates, "
-                         f"{spent:.1f} s, fp64 numpy on one host thread"}
+                         f"{spent:.1f} s of oracle time (input generation not timed), fp64 numpy on one host thread"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w_global.name, "B": w_global.B, "L": w.L, "T": w.T, "B_per_gpu": w.B,
-                       "head_dim": 128, "k_heads": 16, "v_heads": 48, "conv_channels": 10240,
-                       "l2": ("state working set far larger than the 129 MB L2; updated in place every step"
-                              if working_bytes > 2 * 129e6 else
-                              "working set fits in L2 (warm-L2 figure, not an HBM measurement)"),
-                       "timing": f"{args.timing}: {args.steps} steps" + (" in one captured CUDA graph" if graph is not None else ""),
-                       "parallelism": f"dp{world} (sequences sharded, no collective)"},
+            "config": step_config(w_global, w, world),
+            "timing": f"{args.timing}: {args.steps} steps" + (" in one captured CUDA graph" if args.timing == "graph" else ""),
             "clocks": clocks.summary(), "e2e": e2e, "gpu_launches": args.steps, "roofline": roofline,
             "cpu_baseline": cpu,
             "launch_ms": {"mean": float(np.mean(launch_ms)), "min": float(np.min(launch_ms)),
                           "max": float(np.max(launch_ms))},
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
 
@@ -774,7 +920,7 @@ def main():
         if rank == 0:
             run_mixer(args, base)
     elif args.impl == "reference":
-        run_reference(args, base, world, rank)
+        run_reference(args, w_global, base, world, rank)
     else:
         run_gdn(args, w_global, world, rank, local)
     if world > 1:

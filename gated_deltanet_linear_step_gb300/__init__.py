@@ -10,6 +10,7 @@ from ._binding import (  # noqa: F401
     FLAG_NO_STATE_WRITE,
     FLAG_NO_Y,
     FLAG_SILU_GATE,
+    FLAG_TEST_GIVE_UP,
     GdnError,
     gdn_ab_gates,
     gdn_decode_step,

@@ -29,6 +29,7 @@ FLAG_NO_STATE_WRITE = 0x1
 FLAG_NO_Y = 0x2
 FLAG_SILU_GATE = 0x4
 FLAG_GATES_READY = 0x8
+FLAG_TEST_GIVE_UP = 0x10  # tests only: the first wait for a state tile gives up (see gdn.h)
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_ALIGN", 4: "GDN_ERR_ALIAS",
           5: "GDN_ERR_CUDA", 6: "GDN_ERR_FLAGS"}

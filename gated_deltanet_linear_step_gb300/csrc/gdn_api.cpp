@@ -18,7 +18,8 @@ static_assert(GDN_VALUE_DIM == gdn::kValueDim, "geometry mismatch");
 static_assert(GDN_D_CONV == gdn::kDConv, "geometry mismatch");
 static_assert(GDN_MAX_T == gdn::kMaxT, "geometry mismatch");
 static_assert(GDN_FLAG_NO_STATE_WRITE == gdn::kNoStateWrite && GDN_FLAG_NO_Y == gdn::kNoY &&
-                  GDN_FLAG_SILU_GATE == gdn::kSiluGate && GDN_FLAG_GATES_READY == gdn::kGatesReady,
+                  GDN_FLAG_SILU_GATE == gdn::kSiluGate && GDN_FLAG_GATES_READY == gdn::kGatesReady &&
+                  GDN_FLAG_TEST_GIVE_UP == gdn::kTestGiveUp,
               "flag mismatch");
 
 namespace {
@@ -56,7 +57,7 @@ gdn_status run(const float* qkv, const float* z, const float* alpha, const float
                float* y, const int32_t* seq_len, int B, int L, int T, uint32_t flags, void* stream,
                const char* fn) {
     t_last_error.clear();
-    const uint32_t known = gdn::kNoStateWrite | gdn::kNoY | gdn::kSiluGate | gdn::kGatesReady;
+    const uint32_t known = gdn::kNoStateWrite | gdn::kNoY | gdn::kSiluGate | gdn::kGatesReady | gdn::kTestGiveUp;
     if (flags & ~known) return fail(GDN_ERR_FLAGS, "%s: unknown flag bits 0x%x", fn, flags & ~known);
     const bool want_y = (flags & gdn::kNoY) == 0;
     const bool write_state = (flags & gdn::kNoStateWrite) == 0;

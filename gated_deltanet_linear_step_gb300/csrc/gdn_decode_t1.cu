@@ -207,12 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
 
     uint32_t tile_par = 0, stage_par = 0, wt_par = 0;
     bool wt_pending = true;
-    bool failed = false;
+    bool failed = false;         // one of this thread's waits gave up
     bool store_pending = false;  // a bulk store of this group's tile has not yet been waited for
+    // The phase of a copy whose wait gave up in this thread, or -1: the copy may
+    // still land, so it is waited for (bounded) before the CTA leaves.
+    int wt_late = -1, stage_late = -1, tile_late = -1;
+    bool give_up = (p.flags & kTestGiveUp) != 0;  // the first tile wait gives up (tests this path)
 
     for (long long u = u_begin; u < u_end; ++u) {
         const int slot = static_cast<int>((u - u_begin) & 1);
         float* S = stage + slot * kStFloats;
+        const uint32_t stage_bar = smem_addr(&bars[kBarStage + slot]);
         const Unit x = cur;
         const Unit xn = next_unit(p, cur);
         cur = xn;
@@ -227,17 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
             wt_pending = true;
         }
         if (wt_pending) {
-            if (!mbar_wait_bounded(smem_addr(&bars[kBarWt]), wt_par)) failed = true;
+            if (!mbar_wait_bounded(smem_addr(&bars[kBarWt]), wt_par)) {
+                failed = true;
+                wt_late = static_cast<int>(wt_par);
+            }
             wt_par ^= 1u;
             wt_pending = false;
         }
         int n = 1;
         if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + x.b), 0), 1);
-        if (!mbar_wait_bounded(smem_addr(&bars[kBarStage + slot]), (stage_par >> slot) & 1u)) failed = true;
+        if (!mbar_wait_bounded(stage_bar, (stage_par >> slot) & 1u)) {
+            failed = true;
+            stage_late = static_cast<int>((stage_par >> slot) & 1u);
+        }
         stage_par ^= 1u << slot;
 
-        // ---- conv + SiLU (in place over the qkv slice), new conv history, gates
-        if (n > 0) {
+        // ---- conv + SiLU (in place over the qkv slice), new conv history, gates.
+        // A thread whose wait gave up computes and writes nothing from here on.
+        if (n > 0 && !failed) {
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int cc = tid + k * kThreads;
@@ -267,15 +279,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
             }
         }
         __syncthreads();
-        if (n > 0 && warp == 0) normalize_qk(S + kStX, S + kStX + kS, lane);
+        // (the norm's shuffles need the whole warp: the decision is the warp's)
+        if (n > 0 && warp == 0 && !__any_sync(0xffffffffu, failed)) normalize_qk(S + kStX, S + kStX + kS, lane);
         __syncthreads();
 
         // ---- this unit's tile
-        if (!mbar_wait_bounded(my_bar, tile_par)) failed = true;
+        const bool tile_ok = !give_up && mbar_wait_bounded(my_bar, tile_par);
+        give_up = false;
+        if (!tile_ok) {
+            failed = true;
+            tile_late = static_cast<int>(tile_par);
+        }
         tile_par ^= 1u;
 
         // ---- the gated delta rule on the tile in its slot; o replaces v
-        if (n > 0) {
+        if (n > 0 && !__any_sync(0xffffffffu, failed)) {
             float* vo = S + kStX + 2 * kS + hh * kS + q.col0;
             const float4 v4 = *reinterpret_cast<const float4*>(vo);
             const float4 o4 = delta_step_smem(my_tile, S + kStX, S + kStX + kS, q, v4, gates[hh], gates[kGroup + hh]);
@@ -283,14 +301,31 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
             if (q.rb == 0) *reinterpret_cast<float4*>(vo) = o4;
             fence_proxy_async_smem();  // the updated tile is read next by the bulk store
         }
-        named_barrier(1 + hh, kS);
-        if (group_leader && n > 0 && write_state) {
+        const bool group_failed = named_barrier_or(1 + hh, kS, failed);
+        if (group_leader && n > 0 && write_state && !group_failed) {
             bulk_store(p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile, my_tile_s,
                        kTileBytes);
             bulk_commit();
             store_pending = true;
         }
-        __syncthreads();
+
+        if (__syncthreads_or(failed ? 1 : 0)) {
+            // A wait gave up: record it, let every copy still in flight land (each
+            // wait bounded), and stop. Each copy is waited for by the thread that
+            // issued it, on the phase its own wait gave up on.
+            if (tid == 0) {
+                atomicOr(&g_t1_error, kErrWaitTimeout);
+                if (wt_late >= 0) (void)mbar_wait_bounded(smem_addr(&bars[kBarWt]), static_cast<uint32_t>(wt_late));
+                if (stage_late >= 0) (void)mbar_wait_bounded(stage_bar, static_cast<uint32_t>(stage_late));
+                if (has_next)
+                    (void)mbar_wait_bounded(smem_addr(&bars[kBarStage + (slot ^ 1)]), (stage_par >> (slot ^ 1)) & 1u);
+            }
+            if (group_leader) {
+                if (tile_late >= 0) (void)mbar_wait_bounded(my_bar, static_cast<uint32_t>(tile_late));
+                bulk_wait_all();
+            }
+            return;
+        }
 
         // ---- y = rms_norm(o) * ssm_norm * gate(z), one warp per head
         if (n > 0 && write_y && warp < kGroup) {
@@ -301,17 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_decode_t1_kernel(const __grid
                                              lane * 4),
                    gated_rms_norm4(o4, z4, w4, silu_gate));
         }
+        __syncthreads();  // y has read the staging slot before it is refilled
 
-        if (__syncthreads_or(failed ? 1 : 0)) {
-            // A wait gave up: record it, let the copies already issued land, stop.
-            if (tid == 0) {
-                atomicOr(&g_t1_error, kErrWaitTimeout);
-                if (has_next)
-                    (void)mbar_wait_bounded(smem_addr(&bars[kBarStage + (slot ^ 1)]), (stage_par >> (slot ^ 1)) & 1u);
-            }
-            if (group_leader) bulk_wait_all();
-            return;
-        }
         // The tile slot takes the next unit's tile once the store has read it.
         if (group_leader && has_next) {
             if (store_pending) bulk_wait_read();

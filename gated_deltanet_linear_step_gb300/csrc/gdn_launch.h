@@ -27,6 +27,7 @@ constexpr uint32_t kNoStateWrite = 0x1u;
 constexpr uint32_t kNoY = 0x2u;
 constexpr uint32_t kSiluGate = 0x4u;
 constexpr uint32_t kGatesReady = 0x8u;  // alpha holds the log decay, beta holds beta (post-activation)
+constexpr uint32_t kTestGiveUp = 0x10u;  // the first wait on a state tile of every CTA gives up (tests the drain)
 
 struct StepArgs {
     const float* qkv;

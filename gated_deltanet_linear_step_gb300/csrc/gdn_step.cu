@@ -334,6 +334,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
     uint32_t tile_par = 0, z_par = 0;
     bool tile_pending = false, z_pending = false;  // copies issued and not yet waited for
     bool failed = false;  // a bounded wait gave up: stop computing, keep taking part in cluster barriers
+    bool give_up = (p.flags & kTestGiveUp) != 0;
     if (tid == 0 && cid < p.n_units) {
         const long long bl = cid / kKHeads;
         const int g = static_cast<int>(cid - bl * kKHeads);
@@ -448,8 +449,11 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
             __syncthreads();
 
             if (c0 == 0 && !failed) {
-                // This unit's tile moves from its slot into registers.
-                const bool late = !mbar_wait_bounded(tile_bar, tile_par);
+                // This unit's tile moves from its slot into registers. (kTestGiveUp: the first
+                // wait gives up at once, to exercise this path; the tile then stays pending and
+                // is waited for before the CTA leaves.)
+                const bool late = give_up || !mbar_wait_bounded(tile_bar, tile_par);
+                give_up = false;
                 if (__syncthreads_or(late ? 1 : 0)) {
                     failed = true;
                 } else {

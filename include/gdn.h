@@ -72,6 +72,11 @@ typedef enum gdn_status {
 #define GDN_FLAG_SILU_GATE 0x4u      /* y = rms_norm(o) * w * SiLU(z): the earlier model variant's gate */
 #define GDN_FLAG_GATES_READY 0x8u    /* alpha holds the log decay and beta holds beta, as gdn_ab_gates writes them;
                                         dt and ssm_a are still passed but do not enter the result */
+#define GDN_FLAG_TEST_GIVE_UP 0x10u  /* for testing the failure path only: in every CTA the first wait for a state
+                                        tile gives up at once, as a wait that ran out of time would. The kernel then
+                                        waits (bounded) for the copies it has in flight, writes nothing more, sets
+                                        bit 0 of the device error word and returns; the call's outputs are not
+                                        valid. Nothing faults or hangs. */
 
 /*
  * gdn_decode_step - one decode call: T tokens applied in order per (sequence, layer).
@@ -232,18 +237,28 @@ gdn_status gdn_step_inputs(const float* x, const uint16_t* w_qkv, const uint16_t
                            int n_embd, void* stream);
 
 /*
- * gdn_in_proj_noalloc - gdn_in_proj without a caller workspace: the split of
- * x goes to a fixed 48 MiB scratch array compiled into the library, one per
- * device, so the call needs no allocation by anyone. The Winery-Strata pages
- * have no counterpart to this call; it is a convenience of this library.
+ * gdn_in_proj_noalloc - gdn_in_proj for callers that cannot allocate device
+ * memory at the point of the call: a plug-in that only receives tensors from a
+ * host framework whose allocator owns all device memory, or code on a
+ * latency-critical path where a cudaMalloc would synchronise the device. The
+ * call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine): the split of x goes to a 48 MiB scratch array compiled into the
+ * library as a file-scope __device__ array, which every GPU that loads the
+ * library holds until the process exits. The Winery-Strata pages have no
+ * counterpart to this call.
  *
  * Arguments, layouts and results are those of gdn_in_proj. Sizes whose
- * workspace (gdn_in_proj_workspace_size) exceeds 48 MiB give GDN_ERR_SHAPE.
- * Every call of this function on a device shares the one scratch array, so
- * calls must not overlap in time: issue them on one stream, or synchronise
- * between the streams that issue them. The other conventions above hold,
- * except that nothing is stated here about capturing this call in a CUDA
- * graph.
+ * workspace (gdn_in_proj_workspace_size) exceeds 48 MiB give GDN_ERR_SHAPE
+ * before anything is launched. The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress, with that device current) and
+ * keeps it for the life of the process: make that first call before any
+ * stream capture, and do not reset the device (cudaDeviceReset) between calls.
+ * Every call on a device shares the one array, which keeps the last call's
+ * contents; each call rewrites every part of it that it reads, so nothing
+ * needs clearing. Calls that overlap in time on the GPU race on the array:
+ * issue them on one stream, or synchronise between the streams that issue
+ * them. The other conventions above hold, except that nothing is stated here
+ * about capturing this call in a CUDA graph.
  */
 gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint16_t* w_gate, float* qkv, float* z,
                                int B, int L, int T, int n_embd, void* stream);

@@ -5,6 +5,10 @@ Tolerance. A result matches the oracle when, for every slice, the normwise
 relative error ``max |gpu - oracle| / max |oracle|`` is at most 1e-4 (y per
 (sequence, layer, token) 6144-vector; state per (sequence, layer, v-head)
 128x128 tile). conv_state must be bit-identical.
+
+The element-wise relative error ``|gpu - oracle| / max(|oracle|, 1e-3 max |oracle|)``
+per slice is reported beside it (``elementwise_error``); it is not a pass
+criterion. A normwise error e bounds it by 1000 e.
 """
 from __future__ import annotations
 
@@ -49,6 +53,27 @@ def y_errors(gy: np.ndarray, ry: np.ndarray) -> float:
         den = np.abs(b).max()
         worst = max(worst, np.abs(a - b).max() / den if den > 0 else np.abs(a).max())
     return worst
+
+
+def elementwise_error(g: np.ndarray, r: np.ndarray, rows: int) -> float:
+    """Worst element-wise relative error over slices of ``rows`` elements, with the
+    denominator floored at 1e-3 of the slice's largest reference magnitude; NaN
+    (invalid) slices of the reference are skipped."""
+    a = np.asarray(g, np.float64).reshape(-1, rows)
+    b = np.asarray(r, np.float64).reshape(-1, rows)
+    keep = ~np.isnan(b[:, 0])
+    a, b = a[keep], b[keep]
+    if a.size == 0:
+        return 0.0
+    floor = 1e-3 * np.abs(b).max(axis=1, keepdims=True)
+    den = np.maximum(np.abs(b), np.where(floor > 0, floor, 1.0))
+    return float(np.max(np.abs(a - b) / den))
+
+
+def report(label: str, gy, ry, gs, rs) -> str:
+    """One line with the normwise and element-wise errors of y and the state."""
+    return (f"{label}: y normwise {y_errors(gy, ry):.2e} element-wise {elementwise_error(gy, ry, ry.shape[-1]):.2e}; "
+            f"state normwise {state_errors(gs, rs):.2e} element-wise {elementwise_error(gs, rs, 128 * 128):.2e}")
 
 
 def state_errors(gs: np.ndarray, rs: np.ndarray) -> float:

@@ -136,7 +136,7 @@ def test_output_aliasing_rejected(lib):
 def test_flags_and_window_rules(lib):
     p = fake_ptrs()
     args = [p[k] for k in ORDER]
-    assert lib.gdn_decode_step_ex(*args, None, B, L, T, 0x10, None) == 6
+    assert lib.gdn_decode_step_ex(*args, None, B, L, T, 0x20, None) == 6  # 0x1 to 0x10 are defined
     # the verify window reads the states: y may not overlap them
     w = dict(p)
     w["y"] = w["state"]

@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py on the CPU: both arms print the same config, the
+reference arm's line has the contract's keys, traffic figures are only used on
+the kernel source they were taken on, and the clock summary keeps the samples
+of the timed region."""
+import json
+import os
+import subprocess
+import sys
+
+import bench
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_the_gpu_arms_config():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "1", "--workload", "decode_b1_l1_t1"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    w = W.WORKLOADS["decode_b1_l1_t1"]
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["config"] == bench.step_config(w, w, 1)
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_step_config_names_the_l2_treatment():
+    big = W.WORKLOADS["decode_b128_l36_t1_beta_hi_decay_hi"]
+    small = W.WORKLOADS["decode_b1_l1_t1"]
+    assert bench.step_config(big, big, 1)["l2"] == bench.L2_NOTE_LARGE
+    assert bench.step_config(small, small, 1)["l2"] == bench.L2_NOTE_FLUSH
+    assert bench.DEFAULT_WORKLOAD == big.name  # the largest single-GPU workload is the headline
+
+
+def test_traffic_is_used_only_on_the_kernel_source_it_was_taken_on(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    import hashlib
+
+    h = hashlib.sha256()
+    for p in bench.kernel_sources(1):
+        h.update(open(p, "rb").read())
+    good = f"workload: decode_b64_l36_t1\ntraffic_bytes_per_launch: 123\nkernel_source_sha256: {h.hexdigest()}\n"
+    (tmp_path / "k_traffic_a.txt").write_text(good)
+    (tmp_path / "k_traffic_b.txt").write_text(good.replace("decode_b64_l36_t1", "decode_b1_l1_t1")
+                                              .replace(h.hexdigest(), "0" * 64))
+    assert bench.committed_traffic("decode_b64_l36_t1", 1) == 123.0
+    assert bench.committed_traffic("decode_b1_l1_t1", 1) is None  # taken on another source
+    assert bench.committed_traffic("decode_b64_l36_t1", 8) is None  # another kernel's source
+
+
+def test_clock_summary_keeps_the_timed_region():
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.source = "test"
+    c.t0, c.t1 = 10.0, 10.1
+    c.samples = [(9.9, 1500.0, 2070.0, 300.0, []), (10.02, 2070.0, 2070.0, 900.0, ["sw_power_cap"]),
+                 (10.05, 2060.0, 2070.0, 950.0, []), (10.3, 1000.0, 2070.0, 200.0, ["hw_slowdown"])]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 2065.0 and s["reasons"] == ["sw_power_cap"]
+    assert "note" not in s
+    c.samples = [(9.9, 1500.0, 2070.0, 300.0, [])]
+    assert "note" in c.summary()

@@ -24,7 +24,10 @@ def _rows_rel_err(g, r):
     return float(np.max(np.abs(g - r).max(axis=1) / np.abs(r).max(axis=1)))
 
 
-@pytest.mark.parametrize("B,L,T,E", [(3, 2, 1, 2560), (2, 3, 5, 2560), (17, 1, 1, 128), (1, 1, 33, 64), (64, 2, 1, 2560)])
+# n_embd 768 and 1280 give each rank of the cluster 3 and 5 64-wide units: a 128-wide slice
+# followed by a 64-wide tail in one double buffer; 33 rows also end in a partial second row block.
+@pytest.mark.parametrize("B,L,T,E", [(3, 2, 1, 2560), (2, 3, 5, 2560), (17, 1, 1, 128), (1, 1, 33, 64), (64, 2, 1, 2560),
+                                     (5, 2, 3, 768), (33, 1, 1, 1280)])
 def test_ab_gates_match_oracle(cuda_device, B, L, T, E):
     import gated_deltanet_linear_step_gb300 as g
 

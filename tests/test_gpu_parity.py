@@ -93,8 +93,10 @@ def test_full_size_workloads_on_sampled_slices(g, name):
         samples = [(b, l) for b in sorted(firsts.values()) for l in (0, 29)]
     for b, l in samples:
         ry, rs, rc = U.oracle_slice(w, b, l)
-        assert U.y_errors(y[b, l].cpu().numpy(), ry) <= U.TOL, (b, l)
-        assert U.state_errors(t["state"][b, l].cpu().numpy(), rs) <= U.TOL, (b, l)
+        gy, gs = y[b, l].cpu().numpy(), t["state"][b, l].cpu().numpy()
+        print(U.report(f"{name} b={b} l={l}", gy, ry, gs, rs))
+        assert U.y_errors(gy, ry) <= U.TOL, (b, l)
+        assert U.state_errors(gs, rs) <= U.TOL, (b, l)
         assert np.array_equal(t["conv_state"][b, l].cpu().numpy(), rc), (b, l)
     # every slice: conv_state is the last three inputs of [old history, valid tokens]
     cs = t["conv_state"].cpu().numpy()

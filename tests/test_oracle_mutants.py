@@ -70,6 +70,11 @@ def _norm_silu_gate(o, z, w, eps=O.EPS, gate="sigmoid"):
     return o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * w * O.silu(z)
 
 
+def _norm_sigmoid_always(o, z, w, eps=O.EPS, gate="sigmoid"):
+    o = np.asarray(o, np.float64)
+    return o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * w * O.sigmoid(z)
+
+
 def _norm_sum(o, z, w, eps=O.EPS, gate="sigmoid"):
     o = np.asarray(o, np.float64)
     return o / np.sqrt(np.sum(o * o, axis=-1, keepdims=True) + eps) * w * O.sigmoid(z)
@@ -136,6 +141,7 @@ MUTANTS = {
     "decay after update": ("delta_rule_step", _step_decay_after),
     "head map h % 16": ("v_head_to_k_head", lambda h: h % 16),
     "SiLU output gate": ("gated_rms_norm", _norm_silu_gate),
+    "sigmoid for SiLU in the gate variant": ("gated_rms_norm", _norm_sigmoid_always),
     "RMS with sum": ("gated_rms_norm", _norm_sum),
     "eps outside sqrt": ("l2_normalize", _l2_eps_outside),
     "conv taps reversed": ("causal_conv", _conv_reversed),

@@ -263,6 +263,24 @@ def test_gated_rms_norm_closed_forms():
     assert ys[5] == pytest.approx(o[5] / math.sqrt(ms + O.EPS) * w[5] * z[5] / (1 + math.exp(-z[5])), rel=1e-14)
 
 
+def test_gated_rms_norm_silu_variant_closed_forms():
+    """The SiLU-gated variant (the earlier model's output gate, named beside the sigmoid in the
+    header comment of include/strata/core/layer.hpp): SiLU(0) = 0 exactly, SiLU(z) -> z for large z
+    and -> 0 from below for very negative z. Sigmoid would give w/2, w and 0+ there instead."""
+    r = _rng(31)
+    w = r.standard_normal(128)
+    o = np.full(128, 3.0)
+    unit = 3.0 / math.sqrt(9.0 + O.EPS)  # o / rms(o) for a constant o = 3
+    assert np.all(O.gated_rms_norm(o, np.zeros(128), w, gate="silu") == 0.0)
+    y = O.gated_rms_norm(o, np.full(128, 40.0), w, gate="silu")
+    # SiLU(40) = 40 / (1 + e^-40) = 40 (1 - 4.2e-18 ...): equal to 40 in fp64 within one ulp
+    assert np.allclose(y, unit * w * 40.0, rtol=2e-16, atol=0)
+    y = O.gated_rms_norm(o, np.full(128, -40.0), w, gate="silu")
+    # SiLU(-40) = -40 e^-40 / (1 + e^-40): a tiny value of the opposite sign to w
+    assert np.allclose(y, -unit * w * 40.0 * math.exp(-40.0), rtol=1e-14, atol=0)
+    assert np.all(np.sign(y) == -np.sign(w))
+
+
 # ------------------------------------------------------- the whole step --
 def _one_layer_inputs(seed, T=1, zero_state=False):
     r = _rng(seed)
