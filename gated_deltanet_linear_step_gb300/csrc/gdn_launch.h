@@ -126,6 +126,13 @@ cudaError_t launch_decode_t1(const StepArgs& a, cudaStream_t stream);
 // Reads and clears the single-token kernel's device error word.
 cudaError_t read_t1_error(uint32_t* out);
 
+// The multi-token kernel with the tiles resident in shared memory, in chunks
+// of up to 8 tokens (gdn_chunk.cu); requires a.T >= 2.
+cudaError_t launch_decode_chunked(const StepArgs& a, cudaStream_t stream);
+
+// Reads and clears the chunked kernel's device error word.
+cudaError_t read_chunk_error(uint32_t* out);
+
 // Synchronises `stream`, then reads and clears the device error words of both kernels.
 cudaError_t read_device_error(cudaStream_t stream, uint32_t* out);
 

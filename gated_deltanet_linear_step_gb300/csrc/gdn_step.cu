@@ -601,8 +601,15 @@ cudaError_t device_setup(int* clusters) {
 
 }  // namespace
 
+// Windows of up to this many tokens run the kernel with the tiles resident in
+// shared memory (gdn_chunk.cu); longer ones run gdn_window_kernel.
+#ifndef GDN_CHUNK_MAX_T
+#define GDN_CHUNK_MAX_T 8
+#endif
+
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     if (a.T == 1) return launch_decode_t1(a, stream);
+    if (a.T <= GDN_CHUNK_MAX_T) return launch_decode_chunked(a, stream);
     int clusters = 0;
     cudaError_t e = device_setup(&clusters);
     if (e != cudaSuccess) return e;
@@ -642,11 +649,13 @@ cudaError_t read_device_error(cudaStream_t stream, uint32_t* out) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
     if (e != cudaSuccess) return e;
-    uint32_t v1 = 0, v2 = 0;
+    uint32_t v1 = 0, v2 = 0, v3 = 0;
     e = read_t1_error(&v1);
     if (e != cudaSuccess) return e;
+    e = read_chunk_error(&v3);
+    if (e != cudaSuccess) return e;
     e = read_proj_error(&v2);
-    *out = v | v1 | v2;
+    *out = v | v1 | v2 | v3;
     return e;
 }
 

@@ -132,10 +132,13 @@ def test_t_tokens_in_one_call_equal_t_single_calls(g):
     assert torch.equal(a["conv_state"], b["conv_state"])
 
 
-def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g):
-    w, h = _small()
+# (window length, prefix length): both calls of a case run the same kernel (windows of up to 8
+# tokens run the shared-memory kernel, longer ones the register kernel), so they agree bit for bit.
+@pytest.mark.parametrize("T,P", [(8, 3), (12, 10)])
+def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
+    w, h = _small(dict(B=3, L=2, T=T))
     dev = torch.device("cuda:0")
-    lens = torch.tensor([0, 3, 9], dtype=torch.int32, device=dev)
+    lens = torch.tensor([0, P, T], dtype=torch.int32, device=dev)
     a = U.to_device(h, dev)
     a["seq_len"] = lens
     sentinel = torch.full(a["z"].shape, 12345.0, device=dev)
@@ -145,25 +148,29 @@ def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g):
     assert torch.equal(ya[0], sentinel[0])
     assert torch.equal(a["state"][0], torch.from_numpy(h["state"][0]).to(dev))
     assert torch.equal(a["conv_state"][0], torch.from_numpy(h["conv_state"][0]).to(dev))
-    # sequence 1: the prefix call with T = 3
+    # sequence 1: the prefix call with T = P
     p = U.to_device(h, dev)
     p = {k: (v[1:2] if v is not None and k not in ("dt", "ssm_a", "conv_w", "ssm_norm") else v) for k, v in p.items()}
     for k in ("qkv", "z", "alpha", "beta"):
-        p[k] = p[k][:, :, :3].contiguous()
+        p[k] = p[k][:, :, :P].contiguous()
     p["seq_len"] = None
     yp = U.run_step(g, p)
     torch.cuda.synchronize()
-    assert torch.equal(ya[1, :, :3], yp[0]) and torch.equal(ya[1, :, 3:], sentinel[1, :, 3:])
+    assert torch.equal(ya[1, :, :P], yp[0]) and torch.equal(ya[1, :, P:], sentinel[1, :, P:])
     assert torch.equal(a["state"][1], p["state"][0]) and torch.equal(a["conv_state"][1], p["conv_state"][0])
     # lengths past T are clamped to T
     c = U.to_device(h, dev)
-    c["seq_len"] = torch.tensor([100, 9, 9], dtype=torch.int32, device=dev)
+    c["seq_len"] = torch.tensor([100, T, T], dtype=torch.int32, device=dev)
     yc = U.run_step(g, c)
     full = U.to_device(h, dev)
     yf = U.run_step(g, full, seq_len=None)
     torch.cuda.synchronize()
     assert torch.equal(yc, yf) and torch.equal(c["state"], full["state"])
     assert torch.equal(yc[2], ya[2]) and torch.equal(c["state"][2], a["state"][2])
+    # and the ragged call matches the oracle
+    ry, rs, _ = U.oracle_full(dict(h, seq_len=lens.cpu().numpy()))
+    assert U.y_errors(np.where(np.isnan(ry), np.nan, ya.cpu().numpy()), ry) <= U.TOL
+    assert U.state_errors(a["state"].cpu().numpy(), rs) <= U.TOL
 
 
 def test_deterministic_and_batch_permutation_equivariant(g):
