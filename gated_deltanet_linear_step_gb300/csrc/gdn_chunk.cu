@@ -24,7 +24,7 @@
 // arithmetic is the definition's, regrouped; the tile crosses shared memory
 // three times per chunk whatever n is, instead of three times per token, so
 // the tiles can stay in shared memory like the single-token kernel's
-// (gdn_decode_t1.cu), with their HBM traffic on bulk copies.
+// (gdn_decode_t1.cu), arriving by bulk copies.
 //
 // Layout and roles. One persistent CTA per SM, 384 threads, owns a contiguous
 // range of units (layer l, k head g, sequence b), b fastest. Group h (threads
@@ -37,15 +37,17 @@
 // 0-255 also convolve one q or k channel each. Conv histories stay in
 // registers from one chunk to the next.
 //
-// Overlap. Shared memory holds the three tiles, the chunk's raw qkv rows and
-// the normalised q and k (separate from the raw rows), so the next chunk's
-// rows (or the next unit's first rows) are requested as soon as the conv has
-// read the current ones, and arrive while the tiles are worked on. Each group
-// stores its tile and requests the next unit's tile as soon as its update is
-// done. The next unit's conv history is loaded into registers, and its conv
-// taps and the next chunk's alpha and beta are prefetched into L1, one step
-// ahead. Waits are bounded; a wait that gives up stops the CTA after every
-// copy it issued has landed (bounded), with the device error word set.
+// Overlap. Shared memory holds the three tiles, the chunk's raw qkv rows (with
+// the heads' alpha, beta, dt and ssm_a) and the normalised q and k (separate
+// from the raw rows), so the next chunk's inputs (or the next unit's first
+// ones) are requested as soon as the conv has read the current ones, and
+// arrive while the tiles are worked on. A unit's last update writes the new
+// tile straight to HBM with streaming stores, so the slot is free once the
+// group has read it: its leader then requests the next unit's tile, which an
+// L2 prefetch issued a unit earlier has already brought into L2. The next
+// unit's conv histories and taps are loaded into registers a unit ahead.
+// Waits are bounded; a wait that gives up stops the CTA after every copy it
+// issued has landed (bounded), with the device error word set.
 
 #include <mutex>
 
@@ -279,9 +281,14 @@ __device__ __forceinline__ void solve_column(const float (&red)[2 * TP], const f
 
 // The rank-tc update of the thread's 32 x 4 block: S = A_{tc-1} S_0 + sum_s k_s e_s^T,
 // e_s = G(s, tc - 1) d_s gathered from the four lanes that solved the block's columns.
+// The new block goes back to the tile in shared memory (dst == kToSmem: more chunks follow),
+// straight to the state in HBM with streaming stores (dst == kToHbm: the unit's last chunk),
+// or nowhere (kDiscard: a window that writes no state).
+constexpr int kToSmem = 0, kToHbm = 1, kDiscard = 2;
+
 template <int TP>
 __device__ __forceinline__ void update_tile(float* tile, const float* X, const float* M, int hh, int col0, int rb,
-                                            int qd, int tc, const float (&d)[kC]) {
+                                            int qd, int tc, const float (&d)[kC], int dst, float* gtile) {
     const float* gam = M + kMGam + hh * kC * kC;  // gam[s * kC + t] = G(s, t)
     float e[TP];
 #pragma unroll
@@ -315,7 +322,10 @@ __device__ __forceinline__ void update_tile(float* tile, const float* X, const f
             s.z = fmaf(kk[q], E[2][q], s.z);
             s.w = fmaf(kk[q], E[3][q], s.w);
         }
-        *sp = s;
+        if (dst == kToSmem)
+            *sp = s;
+        else if (dst == kToHbm)
+            __stcs(reinterpret_cast<float4*>(gtile + i * kS + col0), s);
     }
 }
 
@@ -409,7 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
 
     uint32_t tile_par = 0, stage_par = 0;
     bool failed = false;
-    bool store_pending = false;  // (leaders) a store of this group's tile has not yet been waited for
     bool give_up = (p.flags & kTestGiveUp) != 0;  // the first tile wait gives up (tests this path)
 
     for (long long u = u_begin; u < u_end; ++u) {
@@ -461,18 +470,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                         cs[0] = hq[0];
                         cs[1] = hq[1];
                         cs[2] = hq[2];
-                    }
-                }
-                if (has_next) {  // the next unit's histories and conv taps, one unit ahead
-                    const int nv = unit_channel(vslot, xn.g);
-                    load_hist(p, xn.bl, nv, hv);
-                    wv = __ldg(reinterpret_cast<const float4*>(
-                        p.conv_w + (static_cast<size_t>(xn.l) * kConvChannels + nv) * kDConv));
-                    if (has_qk) {
-                        const int nq = unit_channel(tid, xn.g);
-                        load_hist(p, xn.bl, nq, hq);
-                        wq = __ldg(reinterpret_cast<const float4*>(
-                            p.conv_w + (static_cast<size_t>(xn.l) * kConvChannels + nq) * kDConv));
                     }
                 }
             }
@@ -528,17 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     stage_pending = true;
                 }
             }
-            // ---- (first chunk) the tile slot takes this unit's tile once the previous unit's store
-            //      has read it (the tile is in L2 by now), and the next unit's tile starts for L2
-            if (group_leader && c0 == 0 && u > u_begin && !failed) {
-                if (store_pending) bulk_wait_read();
-                store_pending = false;
-                mbar_arrive_expect_tx(my_bar, kTileBytes);
-                bulk_load_stream(my_tile_s, tile_src(p, x, hh), kTileBytes, my_bar);
-                tile_pending = true;
-                if (has_next) bulk_prefetch_l2(tile_src(p, xn, hh), kTileBytes);
-            }
-
             // ---- q^ and k^ (normalised; q scaled) into X; the k warps keep k^ for the Gram matrices
             const int tp = (tc + 1) & ~1;
             if (has_qk && tc > 0) {
@@ -675,42 +661,54 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                 }
             }
 
-            // ---- the rank-tc update of the tile
-            if (tc > 0 && warp_ok) {
-                if (tc <= 2)
-                    update_tile<2>(my_tile, X, M, hh, col0, rb, qd, tc, d);
-                else if (tc <= 4)
-                    update_tile<4>(my_tile, X, M, hh, col0, rb, qd, tc, d);
-                else if (tc <= 6)
-                    update_tile<6>(my_tile, X, M, hh, col0, rb, qd, tc, d);
-                else
-                    update_tile<8>(my_tile, X, M, hh, col0, rb, qd, tc, d);
-                fence_proxy_async_smem();  // the updated tile is read next by the bulk store
+            // ---- (last chunk) the next unit's conv histories and taps, one unit ahead
+            if (last_chunk && has_next) {
+                const int nv = unit_channel(vslot, xn.g);
+                load_hist(p, xn.bl, nv, hv);
+                wv = __ldg(reinterpret_cast<const float4*>(
+                    p.conv_w + (static_cast<size_t>(xn.l) * kConvChannels + nv) * kDConv));
+                if (has_qk) {
+                    const int nq = unit_channel(tid, xn.g);
+                    load_hist(p, xn.bl, nq, hq);
+                    wq = __ldg(reinterpret_cast<const float4*>(
+                        p.conv_w + (static_cast<size_t>(xn.l) * kConvChannels + nq) * kDConv));
+                }
             }
-            // ---- (last chunk) the tile goes back to HBM; the slot is refilled in the next unit
+
+            // ---- the rank-tc update of the tile; after the unit's last chunk the slot takes the
+            //      next unit's tile (from L2) as soon as the group has read it
+            if (tc > 0 && warp_ok) {
+                const int dst = !last_chunk ? kToSmem : (write_state ? kToHbm : kDiscard);
+                float* gtile = p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile;
+                if (tc <= 2)
+                    update_tile<2>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                else if (tc <= 4)
+                    update_tile<4>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                else if (tc <= 6)
+                    update_tile<6>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                else
+                    update_tile<8>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+            }
+            fence_proxy_async_smem();  // the slot's reads come before the refill's writes
             const bool group_failed = named_barrier_or(1 + hh, kS, failed);
-            if (group_leader && last_chunk && !group_failed && n > 0 && write_state) {
-                bulk_store(p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile, my_tile_s,
-                           kTileBytes);
-                bulk_commit();
-                store_pending = true;
+            if (group_leader && last_chunk && has_next && !group_failed) {
+                mbar_arrive_expect_tx(my_bar, kTileBytes);
+                bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
+                tile_pending = true;
+                if (u + 2 < u_end) bulk_prefetch_l2(tile_src(p, next_unit(p, xn), hh), kTileBytes);
             }
 
             if (__syncthreads_or(failed ? 1 : 0)) {
                 // A wait gave up: record it, let every copy still in flight land (bounded), stop.
                 if (tid == 0) atomicOr(&g_chunk_error, kErrWaitTimeout);
                 if (warp == 0 && lane == 0 && stage_pending) (void)mbar_wait_bounded(stage_bar, stage_par);
-                if (group_leader) {
-                    if (tile_pending) (void)mbar_wait_bounded(my_bar, tile_par);
-                    bulk_wait_all();
-                }
+                if (group_leader && tile_pending) (void)mbar_wait_bounded(my_bar, tile_par);
                 return;
             }
             if (last_chunk) break;
         }
         x = xn;
     }
-    if (group_leader) bulk_wait_all();  // the last stores finish reading shared memory before exit
 }
 
 std::mutex g_mutex;
