@@ -201,11 +201,24 @@ __device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, 
     }
 }
 
+// The history roll of conv_chunk alone, for a channel whose conv output is not needed.
+__device__ __forceinline__ void roll_history(const float* rows, int cc, int tc, float (&h)[3]) {
+#pragma unroll
+    for (int t = 0; t < kC; ++t) {
+        if (t < tc) {
+            h[0] = h[1];
+            h[1] = h[2];
+            h[2] = rows[t * kUnitCh + cc];
+        }
+    }
+}
+
 // Pass A on one tile: red[n] = sum_i S[i][col] X[i][n] for this lane's column
-// col = col0 + rb, n < 2 TP (k^ at n < TP, q^ at TP <= n).
-template <int TP>
-__device__ __forceinline__ void pass_a(const float* tile, const float* X, int col0, int rb, float (&red)[2 * TP]) {
-    constexpr int NT = 2 * TP;
+// col = col0 + rb, n < NT (k^ at n < TP, q^ at TP <= n < 2 TP; NT = TP when
+// only S^T k is needed, a call that produces no y).
+template <int NT>
+__device__ __forceinline__ void pass_a(const float* tile, const float* X, int col0, int rb, float (&red)[NT]) {
+    static_assert(NT % 2 == 0, "X is read in pairs");
     const int lane = threadIdx.x & 31;
     float acc[4][NT];
 #pragma unroll
@@ -224,6 +237,11 @@ __device__ __forceinline__ void pass_a(const float* tile, const float* X, int co
             xv[4 * m + 1] = v.y;
             xv[4 * m + 2] = v.z;
             xv[4 * m + 3] = v.w;
+        }
+        if (NT % 4 != 0) {  // NT = 2 or 6 (only S^T k): the last pair
+            const float2 v = *reinterpret_cast<const float2*>(X + i * kXStride + NT - 2);
+            xv[NT - 2] = v.x;
+            xv[NT - 1] = v.y;
         }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
@@ -253,11 +271,11 @@ __device__ __forceinline__ void pass_a(const float* tile, const float* X, int co
     }
 }
 
-// The recurrence of this lane's column from the chunk's start: d_t and o_t
+// The recurrence of this lane's column from the chunk's start: d_t and (WQ) o_t
 // per token from pass A's u_t = red[t] and w_t = red[TP + t], v_t, the gates
 // and the group's coefficients.
-template <int TP>
-__device__ __forceinline__ void solve_column(const float (&red)[2 * TP], const float* M, int hh, int tc,
+template <int TP, bool WQ>
+__device__ __forceinline__ void solve_column(const float (&red)[WQ ? 2 * TP : TP], const float* M, int hh, int tc,
                                              const float (&v)[kC], float (&d)[kC], float (&o)[kC]) {
     const float* cum = M + kMCum + hh * kC;
     const float* bet = M + kMBeta + hh * kC;
@@ -271,12 +289,26 @@ __device__ __forceinline__ void solve_column(const float (&red)[2 * TP], const f
 #pragma unroll
             for (int s = 0; s < t; ++s) kv = fmaf(coef[8 * s + t], d[s], kv);
             d[t] = bet[t] * (v[t] - kv);
-            float ov = cum[t] * red[TP + t];
+            if (WQ) {
+                float ov = cum[t] * red[(WQ ? TP : 0) + t];
 #pragma unroll
-            for (int s = 0; s <= t; ++s) ov = fmaf(coef[8 * t + s], d[s], ov);
-            o[t] = ov;
+                for (int s = 0; s <= t; ++s) ov = fmaf(coef[8 * t + s], d[s], ov);
+                o[t] = ov;
+            }
         }
     }
+}
+
+// Pass A, a barrier of the tile's group (its coefficients are then in place),
+// and the column recurrence.
+template <int TP, bool WQ>
+__device__ __forceinline__ void pass_and_solve(const float* tile, const float* X, const float* M, int hh, int col0,
+                                               int rb, int tc, const float (&v)[kC], float (&d)[kC],
+                                               float (&o)[kC]) {
+    float red[WQ ? 2 * TP : TP];
+    pass_a<WQ ? 2 * TP : TP>(tile, X, col0, rb, red);
+    named_barrier(1 + hh, kS);
+    solve_column<TP, WQ>(red, M, hh, tc, v, d, o);
 }
 
 // The rank-tc update of the thread's 32 x 4 block: S = A_{tc-1} S_0 + sum_s k_s e_s^T,
@@ -400,11 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             issue_chunk(p, x, 0, min(kC, valid_len(p, x.b)), raw_s, gin_s, stage_bar, lane);
             stage_pending = true;
         }
-        if (group_leader) {
+        if (group_leader && valid_len(p, x.b) > 0) {  // a unit with no valid token reads no tile
             mbar_arrive_expect_tx(my_bar, kTileBytes);
             bulk_load_stream(my_tile_s, tile_src(p, x, hh), kTileBytes, my_bar);
             tile_pending = true;
-            if (u_begin + 1 < u_end) bulk_prefetch_l2(tile_src(p, next_unit(p, x), hh), kTileBytes);
+        }
+        if (group_leader && u_begin + 1 < u_end) {
+            const Unit x1 = next_unit(p, x);
+            if (valid_len(p, x1.b) > 0) bulk_prefetch_l2(tile_src(p, x1, hh), kTileBytes);
         }
         const int vch = unit_channel(vslot, x.g);
         load_hist(p, x.bl, vch, hv);
@@ -458,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             const int tcw = failed ? 0 : tc;
             float ov[kC], oq[kC];
             conv_chunk(wv, raw, vslot, tcw, hv, ov);
-            if (has_qk) conv_chunk(wq, raw, tid, tcw, hq, oq);
+            if (has_qk && (write_y || tid >= kS)) conv_chunk(wq, raw, tid, tcw, hq, oq);
+            else if (has_qk) roll_history(raw, tid, tcw, hq);  // no y: q is not needed, its history still rolls
             if (last_chunk) {
                 if (write_state && n > 0 && !failed) {
                     float* cs = p.conv_state + (static_cast<size_t>(x.bl) * kConvChannels + vch) * 3;
@@ -473,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     }
                 }
             }
-            if (has_qk) {  // q (warps 0-3) and k (warps 4-7): per-warp sums of squares per token
+            if (has_qk && (write_y || tid >= kS)) {  // q (warps 0-3) and k (warps 4-7): per-warp sums of squares
 #pragma unroll
                 for (int t = 0; t < kC; ++t) {
                     if (t < tc) {
@@ -527,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             }
             // ---- q^ and k^ (normalised; q scaled) into X; the k warps keep k^ for the Gram matrices
             const int tp = (tc + 1) & ~1;
-            if (has_qk && tc > 0) {
+            if (has_qk && tc > 0 && (write_y || tid >= kS)) {
                 const bool is_q = tid < kS;
                 const int i = tid & (kS - 1);
                 const int pw = is_q ? 0 : 4;
@@ -586,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                 const float gm = (s < t) ? M[kMGam + (hh * kC + s) * kC + t] : M[kMGam + (hh * kC + t) * kC + s];
                 M[kMCoef + hh * 64 + gtid] = in ? gm * tot : 0.0f;
             }
-            if (c0 == 0 && !failed) {
+            if (c0 == 0 && n > 0 && !failed) {
                 if (!give_up && mbar_wait_bounded(my_bar, tile_par)) {
                     tile_par ^= 1u;
                     tile_pending = false;
@@ -602,26 +638,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
 #pragma unroll
             for (int t = 0; t < kC; ++t) d[t] = o[t] = 0.0f;
             if (tc > 0 && warp_ok) {
-                if (tc <= 2) {
-                    float red[4];
-                    pass_a<2>(my_tile, X, col0, rb, red);
-                    named_barrier(1 + hh, kS);
-                    solve_column<2>(red, M, hh, tc, ov, d, o);
-                } else if (tc <= 4) {
-                    float red[8];
-                    pass_a<4>(my_tile, X, col0, rb, red);
-                    named_barrier(1 + hh, kS);
-                    solve_column<4>(red, M, hh, tc, ov, d, o);
-                } else if (tc <= 6) {
-                    float red[12];
-                    pass_a<6>(my_tile, X, col0, rb, red);
-                    named_barrier(1 + hh, kS);
-                    solve_column<6>(red, M, hh, tc, ov, d, o);
-                } else {
-                    float red[16];
-                    pass_a<8>(my_tile, X, col0, rb, red);
-                    named_barrier(1 + hh, kS);
-                    solve_column<8>(red, M, hh, tc, ov, d, o);
+                if (write_y) {
+                    if (tc <= 2)
+                        pass_and_solve<2, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else if (tc <= 4)
+                        pass_and_solve<4, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else if (tc <= 6)
+                        pass_and_solve<6, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else
+                        pass_and_solve<8, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                } else {  // no y: only S^T k is needed
+                    if (tc <= 2)
+                        pass_and_solve<2, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else if (tc <= 4)
+                        pass_and_solve<4, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else if (tc <= 6)
+                        pass_and_solve<6, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                    else
+                        pass_and_solve<8, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
                 }
             } else {
                 named_barrier(1 + hh, kS);
@@ -677,8 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
 
             // ---- the rank-tc update of the tile; after the unit's last chunk the slot takes the
             //      next unit's tile (from L2) as soon as the group has read it
-            if (tc > 0 && warp_ok) {
-                const int dst = !last_chunk ? kToSmem : (write_state ? kToHbm : kDiscard);
+            const int dst = !last_chunk ? kToSmem : (write_state ? kToHbm : kDiscard);
+            if (tc > 0 && warp_ok && dst != kDiscard) {
                 float* gtile = p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile;
                 if (tc <= 2)
                     update_tile<2>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
@@ -692,10 +726,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             fence_proxy_async_smem();  // the slot's reads come before the refill's writes
             const bool group_failed = named_barrier_or(1 + hh, kS, failed);
             if (group_leader && last_chunk && has_next && !group_failed) {
-                mbar_arrive_expect_tx(my_bar, kTileBytes);
-                bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
-                tile_pending = true;
-                if (u + 2 < u_end) bulk_prefetch_l2(tile_src(p, next_unit(p, xn), hh), kTileBytes);
+                if (n_next > 0) {
+                    mbar_arrive_expect_tx(my_bar, kTileBytes);
+                    bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
+                    tile_pending = true;
+                }
+                if (u + 2 < u_end) {
+                    const Unit xnn = next_unit(p, xn);
+                    if (valid_len(p, xnn.b) > 0) bulk_prefetch_l2(tile_src(p, xnn, hh), kTileBytes);
+                }
             }
 
             if (__syncthreads_or(failed ? 1 : 0)) {

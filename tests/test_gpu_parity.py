@@ -262,3 +262,24 @@ def test_bad_arguments_raise_and_launch_nothing(g):
         g.gdn_decode_step(*args[:10], torch.zeros(1, 1, 3, 6144, device=dev))
     torch.cuda.synchronize()
     assert torch.equal(t["state"], before) and torch.all(y == 0)
+
+
+@pytest.mark.parametrize("T", [1, 4, 12])
+def test_no_y_and_no_state_write_flags_match_the_full_call(g, T):
+    """FLAG_NO_Y gives the full call's state and conv_state bit for bit and writes no y;
+    FLAG_NO_STATE_WRITE gives its y bit for bit and leaves both states untouched."""
+    w, h = _small(dict(B=3, L=2, T=T), name="decode_b64_l36_t1")
+    dev = torch.device("cuda:0")
+    full = U.to_device(h, dev)
+    yf = U.run_step(g, full, seq_len=None)
+    a = U.to_device(h, dev)
+    sentinel = torch.full(a["z"].shape, 777.0, device=dev)
+    ya = U.run_step(g, a, y=sentinel.clone(), seq_len=None, flags=g.FLAG_NO_Y)
+    b = U.to_device(h, dev)
+    yb = U.run_step(g, b, seq_len=None, flags=g.FLAG_NO_STATE_WRITE)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, sentinel)
+    assert torch.equal(a["state"], full["state"]) and torch.equal(a["conv_state"], full["conv_state"])
+    assert torch.equal(yb, yf)
+    assert torch.equal(b["state"], torch.from_numpy(h["state"]).to(dev))
+    assert torch.equal(b["conv_state"], torch.from_numpy(h["conv_state"]).to(dev))
