@@ -113,8 +113,11 @@ size_t proj_static_scratch_bytes();
 // Reads and clears the projection kernel's device error word.
 cudaError_t read_proj_error(uint32_t* out);
 
-// The fused alpha/beta projections with their gate epilogue (gdn_ab.cu).
+// The fused alpha/beta projections with their gate epilogue on the tensor cores (gdn_ab.cu).
 cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream);
+
+// Reads and clears the alpha/beta kernel's device error word.
+cudaError_t read_ab_error(uint32_t* out);
 
 // Launches the fused decode step on `stream`: the single-token kernel when
 // T == 1, the multi-token kernel otherwise. Returns the launch status.

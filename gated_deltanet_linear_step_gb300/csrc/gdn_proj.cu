@@ -65,6 +65,7 @@
 
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -126,84 +127,6 @@ struct SplitParams {
     long long n_items;
 };
 
-// ------------------------------------------------------------ PTX helpers --
-__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
-                                            uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzled
-// layout (8-row groups of 128-byte rows, 1024 bytes apart), tcgen05 format.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
-    d |= static_cast<uint64_t>(1) << 16;                          // leading offset (unused when swizzled)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;                  // stride between 8-row groups
-    d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                          // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor of kind::f16: BF16 A and B, both K-major, fp32 D, M 128.
-__host__ __device__ constexpr uint32_t mma_idesc(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(kBM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives on `bar` once every tcgen05.mma this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// 32 consecutive accumulator columns of this warp's 32 lanes, one lane per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
-          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
-          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // A bounded wait that also gives up as soon as another role of the CTA has.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -217,25 +140,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
             return false;
         }
     }
-}
-
-// Byte offset of 16-byte chunk c of row n in a 128-byte swizzled K-major block.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(int n, int c) {
-    return static_cast<uint32_t>((n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4));
-}
-
-// ------------------------------------------------------------- split of x --
-// Upper halves of two floats (their BF16 truncations), a in the low 16 bits.
-__device__ __forceinline__ uint32_t hi_pair(float a, float b) {
-    return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
-}
-
-// What the truncation left of two floats (exact in fp32), rounded to BF16.
-__device__ __forceinline__ uint32_t lo_pair(float a, float b) {
-    const float ra = a - __uint_as_float(__float_as_uint(a) & 0xFFFF0000u);
-    const float rb = b - __uint_as_float(__float_as_uint(b) & 0xFFFF0000u);
-    const __nv_bfloat162 v = __floats2bfloat162_rn(ra, rb);
-    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // One 16 KB block per iteration: 128 rows x 64 BF16, the 16-byte chunk c of

@@ -649,13 +649,15 @@ cudaError_t read_device_error(cudaStream_t stream, uint32_t* out) {
     const unsigned int zero = 0;
     e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
     if (e != cudaSuccess) return e;
-    uint32_t v1 = 0, v2 = 0, v3 = 0;
+    uint32_t v1 = 0, v2 = 0, v3 = 0, v4 = 0;
     e = read_t1_error(&v1);
     if (e != cudaSuccess) return e;
     e = read_chunk_error(&v3);
     if (e != cudaSuccess) return e;
+    e = read_ab_error(&v4);
+    if (e != cudaSuccess) return e;
     e = read_proj_error(&v2);
-    *out = v | v1 | v2 | v3;
+    *out = v | v1 | v2 | v3 | v4;
     return e;
 }
 

@@ -166,8 +166,12 @@ gdn_status gdn_decode_step_ex(const float* qkv, const float* z, const float* alp
  *   gate, beta [B][L][T][48]   (outputs; feed gdn_decode_step_ex with GDN_FLAG_GATES_READY)
  *   n_embd: a positive multiple of 64, at most 65536.
  *
- * Products are formed in fp32 from the exactly widened BF16 weights and summed
- * in fp32. Same conventions (device memory, 16-byte alignment, asynchronous on
+ * The sums run on the tensor cores: x is split as hi + lo, hi = x truncated to
+ * BF16 and lo = the remainder rounded to BF16, both halves are multiplied by
+ * the BF16 weights, and the products are summed in fp32, so each product
+ * carries x to within 2^-16 relative. A cluster of 4 CTAs shares each layer's
+ * n_embd and reduces through distributed shared memory; no workspace is used.
+ * Same conventions (device memory, 16-byte alignment, asynchronous on
  * `stream`, outputs overlap nothing) as the calls above.
  */
 gdn_status gdn_ab_gates(const float* x, const uint16_t* w_alpha, const uint16_t* w_beta, const float* dt,
