@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
-SOURCES = ["gdn_step.cu", "gdn_decode_t1.cu", "gdn_chunk.cu", "gdn_ab.cu", "gdn_proj.cu", "gdn_proj_noalloc.cu", "gdn_host_pipeline.cpp", "gdn_api.cpp"]
+SOURCES = ["gdn_step.cu", "gdn_decode_t1.cu", "gdn_chunk.cu", "gdn_window_tc.cu", "gdn_ab.cu", "gdn_proj.cu", "gdn_proj_noalloc.cu", "gdn_host_pipeline.cpp", "gdn_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

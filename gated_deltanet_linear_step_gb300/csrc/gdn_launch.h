@@ -136,6 +136,13 @@ cudaError_t launch_decode_chunked(const StepArgs& a, cudaStream_t stream);
 // Reads and clears the chunked kernel's device error word.
 cudaError_t read_chunk_error(uint32_t* out);
 
+// The multi-token kernel in chunks of up to 64 tokens whose contractions run on
+// the tensor cores (gdn_window_tc.cu); requires a.T >= 2.
+cudaError_t launch_decode_window_tc(const StepArgs& a, cudaStream_t stream);
+
+// Reads and clears the tensor-core window kernel's device error word.
+cudaError_t read_window_tc_error(uint32_t* out);
+
 // Synchronises `stream`, then reads and clears the device error words of both kernels.
 cudaError_t read_device_error(cudaStream_t stream, uint32_t* out);
 

@@ -601,15 +601,20 @@ cudaError_t device_setup(int* clusters) {
 
 }  // namespace
 
-// Windows of up to this many tokens run the kernel with the tiles resident in
-// shared memory (gdn_chunk.cu); longer ones run gdn_window_kernel.
+// Windows of up to GDN_CHUNK_MAX_T tokens run the kernel with the tiles resident
+// in shared memory (gdn_chunk.cu); windows of GDN_TC_MIN_T tokens or more run
+// the tensor-core chunk kernel (gdn_window_tc.cu); any others gdn_window_kernel.
 #ifndef GDN_CHUNK_MAX_T
 #define GDN_CHUNK_MAX_T 8
+#endif
+#ifndef GDN_TC_MIN_T
+#define GDN_TC_MIN_T 9
 #endif
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     if (a.T == 1) return launch_decode_t1(a, stream);
     if (a.T <= GDN_CHUNK_MAX_T) return launch_decode_chunked(a, stream);
+    if (a.T >= GDN_TC_MIN_T) return launch_decode_window_tc(a, stream);
     int clusters = 0;
     cudaError_t e = device_setup(&clusters);
     if (e != cudaSuccess) return e;
@@ -657,7 +662,10 @@ cudaError_t read_device_error(cudaStream_t stream, uint32_t* out) {
     e = read_ab_error(&v4);
     if (e != cudaSuccess) return e;
     e = read_proj_error(&v2);
-    *out = v | v1 | v2 | v3 | v4;
+    if (e != cudaSuccess) return e;
+    uint32_t v5 = 0;
+    e = read_window_tc_error(&v5);
+    *out = v | v1 | v2 | v3 | v4 | v5;
     return e;
 }
 

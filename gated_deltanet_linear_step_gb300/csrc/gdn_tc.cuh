@@ -140,3 +140,93 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// Stores 32 consecutive accumulator columns of this warp's 32 lanes, one lane per thread.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// Waits until this thread's tensor-memory stores have completed.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// BF16 hi (truncation) and lo (the rest, rounded) halves of one float, as raw 16-bit patterns.
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+    const uint32_t u = __float_as_uint(x);
+    hi = static_cast<uint16_t>(u >> 16);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __uint_as_float(u & 0xFFFF0000u)));
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+// BF16 hi (rounded to nearest) and lo (the rest, rounded) halves of two floats,
+// a in the low 16 bits of each word. hi + lo leaves a relative residue of at most
+// 2^-16, against 2^-15 when hi is a truncation.
+__device__ __forceinline__ void split_pair_rn(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const uint32_t hu = *reinterpret_cast<const uint32_t*>(&h);
+    const __nv_bfloat162 r =
+        __floats2bfloat162_rn(a - __uint_as_float(hu << 16), b - __uint_as_float(hu & 0xFFFF0000u));
+    hi = hu;
+    lo = *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Eight floats as two 16-byte rows of BF16 pairs (hi and lo), stored at hi_dst and lo_dst.
+__device__ __forceinline__ void store_split8(unsigned char* hi_dst, unsigned char* lo_dst, const float* x) {
+    uint4 h, l;
+    split_pair_rn(x[0], x[1], h.x, l.x);
+    split_pair_rn(x[2], x[3], h.y, l.y);
+    split_pair_rn(x[4], x[5], h.z, l.z);
+    split_pair_rn(x[6], x[7], h.w, l.w);
+    *reinterpret_cast<uint4*>(hi_dst) = h;
+    *reinterpret_cast<uint4*>(lo_dst) = l;
+}
+
+// One float as BF16 hi (rounded to nearest) and lo halves, raw 16-bit patterns.
+__device__ __forceinline__ void split_rn(float x, uint16_t& hi, uint16_t& lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    hi = __bfloat16_as_ushort(h);
+    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+}
+
+}  // namespace gdn
+
+namespace gdn {
+
+// Shared-memory matrix descriptor: MN-major operand in the 128-byte swizzled
+// layout, atoms of 8 K-rows x 64 MN-contiguous BF16 (1024 bytes); `mn_stride`
+// bytes from one atom to the next along MN, 1024 bytes between 8-row groups
+// along K. (A K-major block of 128-byte rows read with its rows as K is this
+// layout: its 64-element row halves are the MN atoms.)
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Bit 16 of the kind::f16 instruction descriptor: B is MN-major.
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
+
+// 8 consecutive accumulator columns of this warp's 32 lanes, one lane per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+}  // namespace gdn

@@ -1,0 +1,829 @@
+// gdn_window_tc.cu - the decode step over windows of more than 8 tokens: chunks
+// of up to 64 tokens whose contractions run on the tensor cores (tcgen05.mma
+// from shared memory into tensor memory), with the conv, the gates, the
+// inversion of the solve matrix and the epilogues on the CUDA cores.
+//
+// Regrouping (exact up to rounding; the method's step is the per-token gated
+// delta rule of the Winery-Strata header include/strata/core/layer.hpp, its
+// operation-order list, composed over the window by Verifier::record_window on
+// src/core/verify.cpp). For one v head, a chunk of n tokens and the state S0
+// before it (rows follow k, columns follow v), with decays a_t, betas b_t,
+// A_t = a_0 ... a_t and G(s,t) = a_{s+1} ... a_t (G(t,t) = 1):
+//
+//   the state the token-t update sees, a_t S_{t-1}, is A_t S0 + sum_{s<t} G(s,t) k_s d_s^T, so
+//   d_t = b_t (v_t - A_t S0^T k_t) - sum_{s<t} b_t G(s,t) (k_t . k_s) d_s   (a unit lower-triangular system)
+//   o_t = A_t S0^T q_t + sum_{s<=t} G(s,t) (q_t . k_s) d_s
+//   S_n = A_{n-1} S0 + sum_s k_s (G(s,n-1) d_s)^T
+//
+// Products on the tensor cores, each as three BF16 MMAs (hi*hi + hi*lo + lo*hi
+// of the operands' round-to-nearest hi + lo halves, fp32 accumulation; the
+// dropped lo*lo term and the halves' residue are at most about 2^-16 of each
+// product, and far less on average):
+//   Gram    [K;Q] [K;Q]^T         128x128x128 (k.k, q.k, and the squared norms on the diagonal)
+//   state   S0^T [K;Q]^T          128x128x128 (S0^T k_t and S0^T q_t, one TMEM lane per v column)
+//   solve   R^T X^T               128x64x64   (d = X r, X the inverse of the solve matrix)
+//   output  D^T P^T               128x64x64   (P[t][s] = G(s,t) (q_t . k_s), s <= t)
+//   update  E^T K, onto A_{n-1} S0^T held in tensor memory   128x128x64 (K read MN-major)
+// q and k enter the MMAs un-normalised; their L2 norms come from the Gram
+// diagonal and scale the products' results instead. The solve matrix is
+// inverted by 16x16 blocks: diagonal blocks by forward substitution, the blocks
+// below by block products, distance by distance.
+//
+// Work: one CTA (256 threads, 8 warps) per k head of a (sequence, layer), its
+// three v heads one after another; one CTA per SM (about 202 KB of shared memory
+// and all 512 tensor-memory columns), persistent over the units. For a single
+// chunk, the q/k preparation and the Gram matrix serve all three v heads.
+// Longer windows run the chunks of one v head in turn with its state in tensor
+// memory (fp32) between chunks, redoing the q/k preparation per v head, so
+// nothing intermediate is written to global memory (the window may be a verify
+// pass that must not write the state).
+//
+// Rows reach shared memory by bulk copies (the q|k rows of a chunk, a v head's
+// v rows, the state tile, the z rows), each signalled on its own mbarrier, so a
+// phase waits for one round trip instead of one per token. The next unit's
+// inputs are prefetched into L2 during the last v head.
+//
+// Waits are bounded; a wait that gives up marks the CTA failed, after which it
+// writes nothing more, waits (bounded) for the MMAs and copies it issued, frees
+// its tensor memory, sets the device error word and returns.
+
+#include <mutex>
+
+#include "gdn_launch.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kS = kHeadDim;                // 128
+constexpr int kTile = kS * kS;
+constexpr int kC = 64;                      // tokens per chunk
+constexpr int kTcThreads = 256;
+constexpr int kLStride = kC + 4;            // fp32 row stride of the solve matrix (bank spread)
+
+// Shared memory (bytes from a 1024-aligned base). Operand blocks are K-major,
+// 128-byte swizzled: rows of 64 BF16, 8-row groups 1024 bytes apart.
+constexpr uint32_t kBlk128 = 128 * 128;     // one 64-wide K block of 128 rows
+constexpr uint32_t kOffKQ = 0;              // [K;Q] rows (k tokens 0-63, q tokens 64-127) x 128 dims: hi, lo
+constexpr uint32_t kOffS = kOffKQ + 4 * kBlk128;    // S0^T: 128 columns x 128 dims: hi, lo
+// Before S0^T the region stages by bulk copy the chunk's raw q|k rows (1 KB per
+// token), then the state tile (fp32, 64 KB), which the threads read into
+// registers before writing its split over it. After the state MMA:
+constexpr uint32_t kOffR = kOffS;                   //   R^T, 128 x 64: hi, lo
+constexpr uint32_t kOffX = kOffS + 2 * kBlk128;     //   the inverse X, fp32 [64][64]
+constexpr uint32_t kOffXop = kOffX + 64 * 64 * 4;   //   X as the BF16 operand, 64 x 64: hi, lo
+constexpr uint32_t kOffDT = kOffS;                  // then D^T (128 x 64: hi, lo)
+constexpr uint32_t kOffET = kOffS + 2 * kBlk128;    //   and E^T (128 x 64: hi, lo)
+constexpr uint32_t kOffO = kOffS;                   // then o, fp32 [64][128], for the y epilogue,
+constexpr uint32_t kOffZ = kOffS + 2 * kBlk128;     //   beside the chunk's z rows (fp32 [64][128])
+constexpr uint32_t kOffP = kOffS + 4 * kBlk128;     // P: 64 tokens x 64 tokens: hi, lo
+constexpr uint32_t kOffL = kOffP + 2 * 64 * 128;    // the solve matrix, negated, fp32 [64][kLStride]
+constexpr uint32_t kOffV = kOffL + kC * kLStride * 4;  // v rows of a v head: 3 history + 64 tokens, 512 B each
+constexpr uint32_t kOffVHist = kOffV + (kC + 3) * kS * 4;  // its conv history at the window start, [128][3]
+constexpr uint32_t kOffHist = kOffVHist + kS * 12;     // q/k conv history before the chunk, 3 KB
+constexpr uint32_t kOffTab = kOffHist + 3072;
+constexpr int kTabBeta = 0, kTabDec = 64, kTabA = 128, kTabGl = 192, kTabRk = 256, kTabRq = 320, kTabNorm = 384;
+constexpr uint32_t kOffBar = kOffTab + 512 * 4;
+constexpr uint32_t kSmemUsed = kOffBar + 80;
+constexpr uint32_t kTcSmem = kSmemUsed + 1024;     // room to align the base
+
+static_assert(kOffS % 1024 == 0 && kOffP % 1024 == 0, "operand blocks are 1024-aligned");
+static_assert(kC * kS * 4 <= 2 * kBlk128, "o and z fit where S0^T was");
+static_assert(kOffXop + 2 * 64 * 128 <= kOffS + 4 * kBlk128, "R^T and X fit where S0^T was");
+static_assert(kC * 1024 <= 4 * kBlk128 && kTile * 4 <= 4 * kBlk128, "the staged rows and tile fit there too");
+static_assert(kOffV % 16 == 0 && kOffVHist % 16 == 0 && kOffHist % 16 == 0, "bulk copy destinations");
+static_assert(kTcSmem <= 232448, "one CTA per SM");
+
+// Tensor memory columns (512 allocated).
+constexpr uint32_t kTmGram = 0, kTmAb = 128, kTmS = 256, kTmPd = 384, kTmD = 448, kTmCols = 512;
+
+__device__ unsigned int g_wtc_error = 0;
+
+struct TcParams {
+    const float* qkv;
+    const float* z;
+    const float* alpha;
+    const float* beta;
+    const float* dt;
+    const float* ssm_a;
+    const float* conv_w;
+    const float* ssm_norm;
+    float* conv_state;
+    float* state;
+    float* y;
+    const int32_t* seq_len;
+    int B, L, T;
+    uint32_t flags;
+    long long n_units;
+};
+
+__device__ __forceinline__ float u2f(uint32_t v) { return __uint_as_float(v); }
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ float4 conv_taps(const TcParams& p, int l, int ch) {
+    return __ldg(reinterpret_cast<const float4*>(p.conv_w + (static_cast<size_t>(l) * kConvChannels + ch) * kDConv));
+}
+
+// One token of the causal conv + SiLU of a channel: xc from the history (h0
+// oldest) and x; the history shifts only for a valid token. Returns SiLU(xc),
+// or 0 for an invalid one.
+__device__ __forceinline__ float conv_step(float4 w, float& h0, float& h1, float& h2, float x, bool valid) {
+    const float xc = conv4(w, h0, h1, h2, x);
+    if (valid) {
+        h0 = h1;
+        h1 = h2;
+        h2 = x;
+    }
+    return valid ? siluf_(xc) : 0.0f;
+}
+
+// Three BF16 products of two hi/lo operand pairs into d (accumulate = 0 only for the first).
+__device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl, uint32_t idesc,
+                                     bool first) {
+    mma_bf16(d, ah, bh, idesc, first ? 0u : 1u);
+    mma_bf16(d, ah, bl, idesc, 1u);
+    mma_bf16(d, al, bh, idesc, 1u);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    unsigned char* sm = smem_raw + (base - raw_addr);
+    float* tab = reinterpret_cast<float*>(sm + kOffTab);
+    float* beta_s = tab + kTabBeta;
+    float* dec_s = tab + kTabDec;
+    float* A_s = tab + kTabA;
+    float* gl_s = tab + kTabGl;
+    float* rk_s = tab + kTabRk;
+    float* rq_s = tab + kTabRq;
+    float* nw_s = tab + kTabNorm;
+    float* L_s = reinterpret_cast<float*>(sm + kOffL);
+    float* O_s = reinterpret_cast<float*>(sm + kOffO);
+    float* Xs = reinterpret_cast<float*>(sm + kOffX);  // fp32 [64][64]; blocks above the diagonal hold temporaries
+    const float* Rs = reinterpret_cast<const float*>(sm + kOffS);       // staged q|k rows, then the fp32 state tile
+    const float* Hs = reinterpret_cast<const float*>(sm + kOffHist);    // staged q/k history
+    const float* Vs = reinterpret_cast<const float*>(sm + kOffV);       // staged v rows (token t at row t + 3)
+    const float* VHs = reinterpret_cast<const float*>(sm + kOffVHist);  // staged v history (window start)
+    const float* Zs = reinterpret_cast<const float*>(sm + kOffZ);       // staged z rows
+    const uint32_t bar_gram = base + kOffBar, bar_ab = bar_gram + 8, bar_out = bar_gram + 16, bar_d = bar_gram + 24;
+    const uint32_t bar_qk = bar_gram + 32, bar_s = bar_gram + 40, bar_z = bar_gram + 48, bar_v = bar_gram + 56;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;                    // the tensor-memory lanes this warp may access
+    const int col = 32 * quarter + lane;             // v column (tensor-memory lane) of this thread
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+    const bool write_state = (p.flags & kNoStateWrite) == 0;
+    const bool write_y = (p.flags & kNoY) == 0;
+    const bool silu_gate = (p.flags & kSiluGate) != 0;
+    const bool gates_ready = (p.flags & kGatesReady) != 0;
+
+    if (tid == 0) {
+        mbar_init(bar_gram, 1);
+        mbar_init(bar_ab, 1);
+        mbar_init(bar_out, 1);
+        mbar_init(bar_d, 1);
+        mbar_init(bar_qk, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_z, 1);
+        mbar_init(bar_v, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(smem_addr(tmem_slot), kTmCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    uint32_t ph_gram = 0, ph_ab = 0, ph_out = 0, ph_d = 0, ph_qk = 0, ph_s = 0, ph_z = 0, ph_v = 0;
+    uint32_t pend_bar = 0, pend_par = 0;  // (thread 0) the last MMA commit, drained if a wait gives up
+    bool pend_qk = false, pend_s = false, pend_z = false, pend_v = false;  // copies issued, not yet waited for
+    bool failed = false;
+    bool give_up = (p.flags & kTestGiveUp) != 0;
+
+    // Every thread waits for an MMA group or a copy; false (uniform over the CTA) if any wait gave up.
+    auto wait_all = [&](uint32_t bar, uint32_t& ph) -> bool {
+        const bool late = give_up || !mbar_wait_bounded(bar, ph);
+        give_up = false;
+        if (__syncthreads_or(late ? 1 : 0)) return false;
+        ph ^= 1u;
+        tc_fence_after();
+        return true;
+    };
+
+    const uint32_t idesc128 = mma_idesc(128), idesc64 = mma_idesc(64);
+    const uint32_t kq_hi = base + kOffKQ, kq_lo = kq_hi + 2 * kBlk128;
+    const uint32_t s_hi = base + kOffS, s_lo = s_hi + 2 * kBlk128;
+    const uint32_t dt_hi = base + kOffDT, dt_lo = dt_hi + kBlk128;
+    const uint32_t et_hi = base + kOffET, et_lo = et_hi + kBlk128;
+    const uint32_t p_hi = base + kOffP, p_lo = p_hi + 64 * 128;
+    const uint32_t r_hi = base + kOffR, r_lo = r_hi + kBlk128;
+    const uint32_t x_hi = base + kOffXop, x_lo = x_hi + 64 * 128;
+
+    for (long long u = blockIdx.x; u < p.n_units && !failed; u += gridDim.x) {
+        const long long bl = u / kKHeads;
+        const int g = static_cast<int>(u - bl * kKHeads);
+        const int l = static_cast<int>(bl % p.L);
+        const int b = static_cast<int>(bl / p.L);
+        int n = p.T;
+        if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + b), 0), p.T);
+        if (n == 0) continue;
+        const bool multi = n > kC;
+        if (write_y && tid < kS) nw_s[tid] = __ldg(p.ssm_norm + static_cast<size_t>(l) * kS + tid);
+
+        // q (threads 0-127) or k (128-255) channel of this thread in the q/k preparation
+        const bool prep_k = tid >= kS;
+        const int prep_col = tid & (kS - 1);
+        const int prep_ch = (prep_k ? kKOffset : 0) + g * kS + prep_col;
+        float qk_hist[3] = {0.f, 0.f, 0.f};
+
+        for (int h = 0; h < kGroup && !failed; ++h) {
+            const int vh = g * kGroup + h;
+            const int v_ch = kVOffset + vh * kS + col;  // (warps 4-7) the v channel of this thread's column
+            float v_hist[3] = {0.f, 0.f, 0.f};
+
+            for (int c0 = 0; c0 < n && !failed; c0 += kC) {
+                const int tc = min(kC, n - c0);
+                const bool last = c0 + tc == n;
+                const int nh = c0 > 0 ? 3 : 0;  // history rows staged with the chunk's rows
+
+                // ---- v rows of this v head (and, at the window start, its conv history) by bulk copy
+                if (warp == 2) {
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>(tc + nh) * kS * 4 + (c0 == 0 ? kS * 12 : 0));
+                    __syncwarp();
+                    for (int i = lane; i < tc + nh; i += 32) {
+                        const int t = i - nh;
+                        bulk_load(base + kOffV + (t + 3) * kS * 4,
+                                  p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels + kVOffset + vh * kS,
+                                  kS * 4, bar_v);
+                    }
+                    if (lane == 0 && c0 == 0)
+                        bulk_load(base + kOffVHist,
+                                  p.conv_state + (static_cast<size_t>(bl) * kConvChannels + kVOffset + vh * kS) * 3,
+                                  kS * 12, bar_v);
+                }
+                pend_v = true;
+
+                if (h == 0 || multi) {
+                    // ---- q/k: the chunk's rows and the history before it by bulk copy (warp 1), then
+                    //      conv, SiLU and split into the [K;Q] rows, 8 tokens at a time
+                    if (warp == 1) {
+                        if (lane == 0) mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>(tc) * 1024u + 3072u);
+                        __syncwarp();
+                        for (int t = lane; t < tc; t += 32) {
+                            const float* row = p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels;
+                            bulk_load(base + kOffS + t * 1024, row + g * kS, kS * 4, bar_qk);
+                            bulk_load(base + kOffS + t * 1024 + 512, row + kKOffset + g * kS, kS * 4, bar_qk);
+                        }
+                        if (lane == 0) {
+                            if (c0 == 0) {
+                                const float* cs = p.conv_state + static_cast<size_t>(bl) * kConvChannels * (kDConv - 1);
+                                bulk_load(base + kOffHist, cs + g * kS * 3, kS * 12, bar_qk);
+                                bulk_load(base + kOffHist + 1536, cs + (kKOffset + g * kS) * 3, kS * 12, bar_qk);
+                            } else {
+                                for (int r = 0; r < 3; ++r) {
+                                    const float* row =
+                                        p.qkv + (static_cast<size_t>(bl) * p.T + c0 - 3 + r) * kConvChannels;
+                                    bulk_load(base + kOffHist + r * 1024, row + g * kS, kS * 4, bar_qk);
+                                    bulk_load(base + kOffHist + r * 1024 + 512, row + kKOffset + g * kS, kS * 4, bar_qk);
+                                }
+                            }
+                        }
+                    }
+                    pend_qk = true;
+                    if (!wait_all(bar_qk, ph_qk)) {
+                        failed = true;
+                        break;
+                    }
+                    pend_qk = false;
+                    {
+                        const int seg = prep_k ? kS : 0;
+                        float h0, h1, h2;
+                        if (c0 == 0) {
+                            h0 = Hs[3 * (seg + prep_col)];
+                            h1 = Hs[3 * (seg + prep_col) + 1];
+                            h2 = Hs[3 * (seg + prep_col) + 2];
+                        } else {
+                            h0 = Hs[seg + prep_col];
+                            h1 = Hs[2 * kS + seg + prep_col];
+                            h2 = Hs[4 * kS + seg + prep_col];
+                        }
+                        const float4 w = conv_taps(p, l, prep_ch);
+                        const float* xr = Rs + seg + prep_col;
+                        const int kb = prep_col >> 6, cc = (prep_col & 63) >> 3, e = prep_col & 7;
+#pragma unroll 1
+                        for (int j = 0; j < kC / 8; ++j) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int t = 8 * j + i;
+                                const float x = conv_step(w, h0, h1, h2, xr[min(t, tc - 1) * 2 * kS], t < tc);
+                                const uint32_t off =
+                                    kOffKQ + kb * kBlk128 + sw128_offset(prep_k ? t : kC + t, cc) + 2 * e;
+                                uint16_t hi, lo;
+                                split_rn(x, hi, lo);
+                                *reinterpret_cast<uint16_t*>(sm + off) = hi;
+                                *reinterpret_cast<uint16_t*>(sm + off + 2 * kBlk128) = lo;
+                            }
+                        }
+                        qk_hist[0] = h0;
+                        qk_hist[1] = h1;
+                        qk_hist[2] = h2;
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncthreads();
+                    if (tid == 0) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ah = sw128_desc(kq_hi + kb2 * kBlk128) + 2 * kk;
+                                const uint64_t al = sw128_desc(kq_lo + kb2 * kBlk128) + 2 * kk;
+                                mma3(tmem + kTmGram, ah, al, ah, al, idesc128, (kb2 | kk) == 0);
+                            }
+                        mma_commit(bar_gram);
+                        pend_bar = bar_gram;
+                        pend_par = ph_gram;
+                    }
+                    if (!wait_all(bar_gram, ph_gram)) {
+                        failed = true;
+                        break;
+                    }
+                    // ---- L2 norms from the Gram diagonal (row r: k token r, or q token r - 64)
+                    if (warp < 4) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + kTmGram + lane_off + 32 * warp, v);
+                        float dg = 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (lane == j) dg = u2f(v[j]);
+                        const float r = rsqrtf(dg + kEps);
+                        if (warp < 2)
+                            rk_s[32 * warp + lane] = r;
+                        else
+                            rq_s[32 * (warp - 2) + lane] = r * kQScale;
+                    }
+                }
+
+                // ---- the next unit's inputs into L2, during this unit's last v head
+                if (h == kGroup - 1 && c0 == 0) {
+                    const long long nu = u + gridDim.x;
+                    if (nu < p.n_units) {
+                        const long long nbl = nu / kKHeads;
+                        const int ng = static_cast<int>(nu - nbl * kKHeads);
+                        int nn = p.T;
+                        if (p.seq_len != nullptr) nn = min(max(__ldg(p.seq_len + nbl / p.L), 0), p.T);
+                        nn = min(nn, kC);
+                        if (tid < kGroup && nn > 0)
+                            prefetch_l2(p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + tid) * kTile,
+                                        kTile * 4);
+                        if (tid >= 32 && tid < 32 + nn) {
+                            const float* row = p.qkv + (static_cast<size_t>(nbl) * p.T + (tid - 32)) * kConvChannels;
+                            prefetch_l2(row + ng * kS, kS * 4);
+                            prefetch_l2(row + kKOffset + ng * kS, kS * 4);
+                            prefetch_l2(row + kVOffset + ng * kGroup * kS, kGroup * kS * 4);
+                            if (write_y)
+                                prefetch_l2(p.z + (static_cast<size_t>(nbl) * p.T + (tid - 32)) * kValueDim +
+                                                ng * kGroup * kS,
+                                            kGroup * kS * 4);
+                        }
+                    }
+                }
+
+                // ---- the state tile by bulk copy (the region is free: the q/k rows are consumed, the
+                //      previous y is written); the gates are computed meanwhile
+                if (c0 == 0) {
+                    if (tid == 32) {
+                        mbar_arrive_expect_tx(bar_s, kTile * 4);
+                        bulk_load(base + kOffS, p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile, kTile * 4,
+                                  bar_s);
+                    }
+                    pend_s = true;
+                }
+                if (tid < kC) {
+                    float bt = 0.0f, dc = 1.0f;
+                    if (tid < tc) {
+                        const size_t row = (static_cast<size_t>(bl) * p.T + c0 + tid) * kVHeads + vh;
+                        head_gates_in(gates_ready, __ldg(p.alpha + row), __ldg(p.beta + row),
+                                      __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh),
+                                      __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
+                    }
+                    beta_s[tid] = bt;
+                    dec_s[tid] = dc;
+                }
+                __syncthreads();
+                if (tid < kC) {
+                    float a = 1.0f;
+                    for (int r = 0; r <= tid; ++r) a *= dec_s[r];
+                    float gl = 0.0f;
+                    if (tid < tc) {
+                        gl = 1.0f;
+                        for (int r = tid + 1; r < tc; ++r) gl *= dec_s[r];
+                    }
+                    A_s[tid] = a;
+                    gl_s[tid] = gl;
+                }
+
+                // ---- the state: S^T (hi, lo) for the MMA, A_{n-1} S into the update accumulator
+                {
+                    const int kh = warp >> 2;  // dims [64 kh, 64 kh + 64)
+                    float sv[64];
+                    if (c0 == 0) {
+                        if (!wait_all(bar_s, ph_s)) {
+                            failed = true;
+                            break;
+                        }
+                        pend_s = false;
+#pragma unroll
+                        for (int k = 0; k < 64; ++k) sv[k] = Rs[(64 * kh + k) * kS + col];
+                        __syncthreads();  // the whole tile is read before its split overwrites it
+                    } else {
+                        __syncthreads();  // A_s is written
+                        uint32_t v[32];
+                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) sv[k] = u2f(v[k]);
+                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh + 32, v);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) sv[32 + k] = u2f(v[k]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t off = kOffS + kh * kBlk128 + sw128_offset(col, j);
+                        store_split8(sm + off, sm + off + 2 * kBlk128, sv + 8 * j);
+                    }
+                    const float al = A_s[tc - 1];
+                    uint32_t v[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(al * sv[k]);
+                    tmem_st32(tmem + kTmS + lane_off + 64 * kh, v);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(al * sv[32 + k]);
+                    tmem_st32(tmem + kTmS + lane_off + 64 * kh + 32, v);
+                    tmem_st_wait();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kb2 = 0; kb2 < 2; ++kb2)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma3(tmem + kTmAb, sw128_desc(s_hi + kb2 * kBlk128) + 2 * kk,
+                                 sw128_desc(s_lo + kb2 * kBlk128) + 2 * kk, sw128_desc(kq_hi + kb2 * kBlk128) + 2 * kk,
+                                 sw128_desc(kq_lo + kb2 * kBlk128) + 2 * kk, idesc128, (kb2 | kk) == 0);
+                    mma_commit(bar_ab);
+                    pend_bar = bar_ab;
+                    pend_par = ph_ab;
+                }
+
+                if (warp < 4) {
+                    // ---- solve matrix (k rows, warps 0-1) and P (q rows, warps 2-3) from the Gram rows,
+                    //      s from 63 down so that G(s, t) = a_{s+1} ... a_t builds up as one running product
+                    const int t = (32 * warp + lane) & (kC - 1);
+                    const bool is_q = warp >= 2;
+                    const bool valid_t = t < tc;
+                    const float rt = valid_t ? (is_q ? rq_s[t] : -beta_s[t] * rk_s[t]) : 0.0f;
+                    float pr = 1.0f;
+#pragma unroll
+                    for (int half = 1; half >= 0; --half) {
+                        uint32_t raw[32];
+                        tmem_ld32(tmem + kTmGram + lane_off + 32 * half, raw);
+                        float val[32];
+#pragma unroll
+                        for (int i = 31; i >= 0; --i) {
+                            const int s = 32 * half + i;
+                            if (s < t) pr *= dec_s[s + 1];
+                            // L: s < t (negated, with beta_t); P: s <= t
+                            const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
+                            val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
+                        }
+                        if (!is_q) {
+                            float* Lr = L_s + t * kLStride + 32 * half;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<float4*>(Lr + 4 * j) =
+                                    make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t off = kOffP + sw128_offset(t, 4 * half + j);
+                                store_split8(sm + off, sm + off + 64 * 128, val + 8 * j);
+                            }
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncthreads();  // the solve matrix and P are written
+                if (!wait_all(bar_ab, ph_ab)) {
+                    failed = true;
+                    break;
+                }
+                if (!wait_all(bar_v, ph_v)) {
+                    failed = true;
+                    break;
+                }
+                pend_v = false;
+
+                // ---- r_t = b_t (v_t - A_t S0^T k_t) into R^T (warps 4-7, with the v conv, 8 tokens at a
+                //      time), and the inverse X of the solve matrix I - Lneg by 16x16 blocks; both go where
+                //      S0^T was, and d = X r follows as one more MMA
+                if (warp >= 4) {
+                    float h0, h1, h2;
+                    if (c0 == 0) {
+                        h0 = VHs[3 * col];
+                        h1 = VHs[3 * col + 1];
+                        h2 = VHs[3 * col + 2];
+                    } else {
+                        h0 = Vs[col];
+                        h1 = Vs[kS + col];
+                        h2 = Vs[2 * kS + col];
+                    }
+                    const float4 w = conv_taps(p, l, v_ch);
+#pragma unroll 1
+                    for (int j = 0; j < kC / 8; ++j) {
+                        uint32_t a8[8];
+                        tmem_ld8(tmem + kTmAb + lane_off + 8 * j, a8);
+                        float r8[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int t = 8 * j + i;
+                            const float v = conv_step(w, h0, h1, h2, Vs[(min(t, tc - 1) + 3) * kS + col], t < tc);
+                            r8[i] = beta_s[t] * (v - A_s[t] * rk_s[t] * u2f(a8[i]));
+                        }
+                        const uint32_t off = kOffR + sw128_offset(col, j);
+                        store_split8(sm + off, sm + off + kBlk128, r8);
+                    }
+                    v_hist[0] = h0;
+                    v_hist[1] = h1;
+                    v_hist[2] = h2;
+                } else if (tid < kC) {
+                    // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
+                    const int i = tid >> 4, j = tid & 15;
+                    float x[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        const float* Lr = L_s + (16 * i + r) * kLStride + 16 * i;
+                        float acc = 0.0f;
+#pragma unroll
+                        for (int m = 0; m < r; ++m) acc = fmaf(Lr[m], x[m], acc);
+                        x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
+                }
+                __syncthreads();
+                {
+                    // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj
+                    const int r = tid >> 4, c = tid & 15;
+#pragma unroll
+                    for (int dist = 1; dist < 4; ++dist) {
+                        for (int j = 0; j + dist < 4; ++j) {
+                            const int i = j + dist;
+                            float y = 0.0f;
+                            for (int k = j; k < i; ++k) {
+                                const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
+#pragma unroll
+                                for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
+                            }
+                            Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
+                        }
+                        __syncthreads();
+                        for (int j = 0; j + dist < 4; ++j) {
+                            const int i = j + dist;
+                            float x = 0.0f;
+#pragma unroll
+                            for (int m = 0; m < 16; ++m)
+                                x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
+                            Xs[(16 * i + r) * kC + 16 * j + c] = x;
+                        }
+                        __syncthreads();
+                    }
+                }
+                {
+                    // X as the BF16 operand [t][s]; blocks above the diagonal are zero
+                    const int t = tid >> 2;
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int j = 2 * (tid & 3) + h2;  // columns [8 j, 8 j + 8)
+                        float xv[8];
+                        const bool upper = (j >> 1) > (t >> 4);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
+                        const uint32_t off = kOffXop + sw128_offset(t, j);
+                        store_split8(sm + off, sm + off + 64 * 128, xv);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma3(tmem + kTmD, sw128_desc(r_hi) + 2 * kk, sw128_desc(r_lo) + 2 * kk, sw128_desc(x_hi) + 2 * kk,
+                             sw128_desc(x_lo) + 2 * kk, idesc64, kk == 0);
+                    mma_commit(bar_d);
+                    pend_bar = bar_d;
+                    pend_par = ph_d;
+                }
+                if (!wait_all(bar_d, ph_d)) {
+                    failed = true;
+                    break;
+                }
+                if (warp >= 4) {
+                    // ---- d, then the D^T and E^T rows (E: d scaled by G(s, n-1) and the k norm)
+#pragma unroll 1
+                    for (int j = 0; j < kC / 8; ++j) {
+                        uint32_t d8[8];
+                        tmem_ld8(tmem + kTmD + lane_off + 8 * j, d8);
+                        float d[8], ev[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            d[e] = u2f(d8[e]);
+                            ev[e] = gl_s[8 * j + e] * rk_s[8 * j + e] * d[e];
+                        }
+                        const uint32_t off = sw128_offset(col, j);
+                        store_split8(sm + kOffDT + off, sm + kOffDT + kBlk128 + off, d);
+                        store_split8(sm + kOffET + off, sm + kOffET + kBlk128 + off, ev);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                if (tid == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma3(tmem + kTmPd, sw128_desc(dt_hi) + 2 * kk, sw128_desc(dt_lo) + 2 * kk,
+                             sw128_desc(p_hi) + 2 * kk, sw128_desc(p_lo) + 2 * kk, idesc64, kk == 0);
+                    // K as B, MN-major: tokens 16 kk .. 16 kk + 15 are two 8-row groups of the [K;Q] blocks
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma3(tmem + kTmS, sw128_desc(et_hi) + 2 * kk, sw128_desc(et_lo) + 2 * kk,
+                             sw128_mn_desc(kq_hi + kk * 2048, kBlk128), sw128_mn_desc(kq_lo + kk * 2048, kBlk128),
+                             idesc128 | kIdescBMnMajor, false);
+                    mma_commit(bar_out);
+                    pend_bar = bar_out;
+                    pend_par = ph_out;
+                }
+                if (!wait_all(bar_out, ph_out)) {
+                    failed = true;
+                    break;
+                }
+                if (write_y) {
+                    // z rows of the chunk into the half of the region that E^T held
+                    if (warp == 1) {
+                        if (lane == 0) mbar_arrive_expect_tx(bar_z, static_cast<uint32_t>(tc) * kS * 4);
+                        __syncwarp();
+                        for (int t = lane; t < tc; t += 32)
+                            bulk_load(base + kOffZ + t * kS * 4,
+                                      p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, bar_z);
+                    }
+                    pend_z = true;
+                }
+
+                if (warp >= 4) {
+                    // ---- o_t = A_t S0^T q_t + (D^T P^T)_t, into o[t][col] for the y epilogue
+                    if (write_y) {
+#pragma unroll 1
+                        for (int j = 0; j < kC / 8; ++j) {
+                            uint32_t bq[8], pd[8];
+                            tmem_ld8(tmem + kTmAb + lane_off + kC + 8 * j, bq);
+                            tmem_ld8(tmem + kTmPd + lane_off + 8 * j, pd);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int t = 8 * j + i;
+                                O_s[t * kS + col] = A_s[t] * rq_s[t] * u2f(bq[i]) + u2f(pd[i]);
+                            }
+                        }
+                    }
+                } else if (last && write_state) {
+                    // ---- the new state tile: column col, all 128 dims
+                    float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile + col;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t v[32];
+                        tmem_ld32(tmem + kTmS + lane_off + 32 * q, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) __stcs(dst + (32 * q + i) * kS, u2f(v[i]));
+                    }
+                }
+                tc_fence_before();
+                __syncthreads();
+                if (write_y) {
+                    if (!wait_all(bar_z, ph_z)) {
+                        failed = true;
+                        break;
+                    }
+                    pend_z = false;
+                    const float4 w4 = *reinterpret_cast<const float4*>(nw_s + lane * 4);
+                    for (int t = warp; t < tc; t += kTcThreads / 32) {
+                        const float4 o4 = *reinterpret_cast<const float4*>(O_s + t * kS + lane * 4);
+                        const float4 z4 = *reinterpret_cast<const float4*>(Zs + t * kS + lane * 4);
+                        __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim +
+                                                         vh * kS + lane * 4),
+                               gated_rms_norm4(o4, z4, w4, silu_gate));
+                    }
+                }
+                __syncthreads();  // o, z and the operand blocks are rewritten next
+            }
+            if (!failed && write_state && warp >= 4) {
+                float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + v_ch) * (kDConv - 1);
+                cs[0] = v_hist[0];
+                cs[1] = v_hist[1];
+                cs[2] = v_hist[2];
+            }
+        }
+        // The q/k history last: every v head's pass has read the old one.
+        if (!failed && write_state) {
+            float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + prep_ch) * (kDConv - 1);
+            cs[0] = qk_hist[0];
+            cs[1] = qk_hist[1];
+            cs[2] = qk_hist[2];
+        }
+    }
+
+    // MMAs and copies still in flight finish before the tensor memory is freed (bounded).
+    if (tid == 0 && failed) (void)mbar_wait_bounded(pend_bar, pend_par);
+    if (tid == 32 && failed) {
+        if (pend_qk) (void)mbar_wait_bounded(bar_qk, ph_qk);
+        if (pend_s) (void)mbar_wait_bounded(bar_s, ph_s);
+        if (pend_z) (void)mbar_wait_bounded(bar_z, ph_z);
+        if (pend_v) (void)mbar_wait_bounded(bar_v, ph_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmCols);
+    }
+    if (tid == 0 && failed) atomicOr(&g_wtc_error, kErrWaitTimeout);
+}
+
+std::mutex g_mutex;
+int g_sms[64] = {};
+
+}  // namespace
+
+cudaError_t launch_decode_window_tc(const StepArgs& a, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int sms;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_sms[dev] == 0) {
+            int n = 0;
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(gdn_window_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kTcSmem));
+            if (e != cudaSuccess) return e;
+            g_sms[dev] = n;
+        }
+        sms = g_sms[dev];
+    }
+    TcParams p;
+    p.qkv = a.qkv;
+    p.z = a.z;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
+    p.dt = a.dt;
+    p.ssm_a = a.ssm_a;
+    p.conv_w = a.conv_w;
+    p.ssm_norm = a.ssm_norm;
+    p.conv_state = a.conv_state;
+    p.state = a.state;
+    p.y = a.y;
+    p.seq_len = a.seq_len;
+    p.B = a.B;
+    p.L = a.L;
+    p.T = a.T;
+    p.flags = a.flags;
+    p.n_units = static_cast<long long>(a.B) * a.L * kKHeads;
+    const long long grid = p.n_units < sms ? p.n_units : sms;
+    gdn_window_tc_kernel<<<static_cast<unsigned>(grid), kTcThreads, kTcSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t read_window_tc_error(uint32_t* out) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_wtc_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_wtc_error, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+}  // namespace gdn

@@ -113,8 +113,11 @@ def _small(scale=dict(B=3, L=2, T=9), name="verify_b16_l36_t8_ragged"):
 
 
 def test_t_tokens_in_one_call_equal_t_single_calls(g):
-    """One T-token call and T one-token calls agree to rounding: the two kernels
-    sum the same terms in different groupings (32- vs 16-row partial sums)."""
+    """One T-token call and T one-token calls agree to within the parity tolerance:
+    both follow the same definition, but the window kernel regroups it by chunks and
+    runs its products on the tensor cores with BF16 hi + lo operands (errors near
+    2e-5 of the largest value), while the single-token kernel sums in fp32 on the
+    CUDA cores."""
     w, h = _small(name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     a = U.to_device(h, dev)
@@ -127,13 +130,13 @@ def test_t_tokens_in_one_call_equal_t_single_calls(g):
             one[k] = b[k][:, :, tt:tt + 1].contiguous()
         ys.append(U.run_step(g, one))
     torch.cuda.synchronize()
-    assert U.y_errors(ya.cpu().numpy(), torch.cat(ys, dim=2).cpu().numpy().astype("float64")) <= 1e-5
-    assert U.state_errors(a["state"].cpu().numpy(), b["state"].cpu().numpy().astype("float64")) <= 1e-5
+    assert U.y_errors(ya.cpu().numpy(), torch.cat(ys, dim=2).cpu().numpy().astype("float64")) <= U.TOL
+    assert U.state_errors(a["state"].cpu().numpy(), b["state"].cpu().numpy().astype("float64")) <= U.TOL
     assert torch.equal(a["conv_state"], b["conv_state"])
 
 
 # (window length, prefix length): both calls of a case run the same kernel (windows of up to 8
-# tokens run the shared-memory kernel, longer ones the register kernel), so they agree bit for bit.
+# tokens run the shared-memory kernel, longer ones the tensor-core kernel), so they agree bit for bit.
 @pytest.mark.parametrize("T,P", [(8, 3), (12, 10)])
 def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
     w, h = _small(dict(B=3, L=2, T=T))
