@@ -82,8 +82,10 @@ constexpr uint32_t kOffV = kOffL + kC * kLStride * 4;  // v rows of a v head: 3 
 constexpr uint32_t kOffVHist = kOffV + (kC + 3) * kS * 4;  // its conv history at the window start, [128][3]
 constexpr uint32_t kOffHist = kOffVHist + kS * 12;     // q/k conv history before the chunk, 3 KB
 constexpr uint32_t kOffTab = kOffHist + 3072;
-constexpr int kTabBeta = 0, kTabDec = 64, kTabA = 128, kTabGl = 192, kTabRk = 256, kTabRq = 320, kTabNorm = 384;
-constexpr uint32_t kOffBar = kOffTab + 512 * 4;
+// gates of the unit's three v heads ([head][64] each), then the q/k norms, ssm_norm, scan totals
+constexpr int kTabBeta = 0, kTabDec = 192, kTabA = 384, kTabGl = 576, kTabRk = 768, kTabRq = 832, kTabNorm = 896,
+              kTabTot = 1024;
+constexpr uint32_t kOffBar = kOffTab + 1032 * 4;
 constexpr uint32_t kSmemUsed = kOffBar + 80;
 constexpr uint32_t kTcSmem = kSmemUsed + 1024;     // room to align the base
 
@@ -140,6 +142,19 @@ __device__ __forceinline__ float conv_step(float4 w, float& h0, float& h1, float
     return valid ? siluf_(xc) : 0.0f;
 }
 
+// Raw q/k input of staged channel c (q at [0, 128), k at [128, 256)) at token c0 + t (t in
+// [-3, tc)): token t >= 0 is staged row t; before it, the staged history, which at the window
+// start is conv_state ([channel][3]) and otherwise the three qkv rows before c0.
+__device__ __forceinline__ float qk_raw(const float* Rs, const float* Hs, int c0, int c, int t) {
+    return t >= 0 ? Rs[t * 2 * kS + c] : (c0 == 0 ? Hs[3 * c + 3 + t] : Hs[(t + 3) * 2 * kS + c]);
+}
+
+// Raw v input of column col at token c0 + t (t in [-3, tc)) from the staged rows: token t is
+// row t + 3; before the window start (c0 == 0, t < 0) it is the staged conv history.
+__device__ __forceinline__ float v_raw(const float* Vs, const float* VHs, int c0, int col, int t) {
+    return (c0 == 0 && t < 0) ? VHs[3 * col + 3 + t] : Vs[(t + 3) * kS + col];
+}
+
 // Three BF16 products of two hi/lo operand pairs into d (accumulate = 0 only for the first).
 __device__ __forceinline__ void mma3(uint32_t d, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl, uint32_t idesc,
                                      bool first) {
@@ -161,6 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     float* rk_s = tab + kTabRk;
     float* rq_s = tab + kTabRq;
     float* nw_s = tab + kTabNorm;
+    float* tot_s = tab + kTabTot;
     float* L_s = reinterpret_cast<float*>(sm + kOffL);
     float* O_s = reinterpret_cast<float*>(sm + kOffO);
     float* Xs = reinterpret_cast<float*>(sm + kOffX);  // fp32 [64][64]; blocks above the diagonal hold temporaries
@@ -202,6 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 
     uint32_t ph_gram = 0, ph_ab = 0, ph_out = 0, ph_d = 0, ph_qk = 0, ph_s = 0, ph_z = 0, ph_v = 0;
     uint32_t pend_bar = 0, pend_par = 0;  // (thread 0) the last MMA commit, drained if a wait gives up
+    bool pend_mma = false;                // (thread 0) an MMA commit not yet waited for
     bool pend_qk = false, pend_s = false, pend_z = false, pend_v = false;  // copies issued, not yet waited for
     bool failed = false;
     bool give_up = (p.flags & kTestGiveUp) != 0;
@@ -211,6 +228,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         const bool late = give_up || !mbar_wait_bounded(bar, ph);
         give_up = false;
         if (__syncthreads_or(late ? 1 : 0)) return false;
+        if (bar == pend_bar) pend_mma = false;
         ph ^= 1u;
         tc_fence_after();
         return true;
@@ -241,11 +259,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         const int prep_col = tid & (kS - 1);
         const int prep_ch = (prep_k ? kKOffset : 0) + g * kS + prep_col;
         float qk_hist[3] = {0.f, 0.f, 0.f};
+        float gpre = 1.0f, gsuf = 1.0f;  // (warps 0-5) decay scans of the q/k preparation
 
         for (int h = 0; h < kGroup && !failed; ++h) {
             const int vh = g * kGroup + h;
+            const float* beta_h = beta_s + 64 * h;  // this v head's gates
+            const float* dec_h = dec_s + 64 * h;
+            const float* A_h = A_s + 64 * h;
+            const float* gl_h = gl_s + 64 * h;
+            float v_hist[3] = {0.f, 0.f, 0.f};  // (warps 4-7) the v history after the window
             const int v_ch = kVOffset + vh * kS + col;  // (warps 4-7) the v channel of this thread's column
-            float v_hist[3] = {0.f, 0.f, 0.f};
 
             for (int c0 = 0; c0 < n && !failed; c0 += kC) {
                 const int tc = min(kC, n - c0);
@@ -296,6 +319,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                             }
                         }
                     }
+                    // gates of the three v heads for the chunk's tokens (warps 0-5: head warp / 2, tokens
+                    // [32 (warp & 1), +32)), with in-warp prefix and suffix products of the decays
+                    if (warp < 2 * kGroup) {
+                        const int hh = warp >> 1, t = 32 * (warp & 1) + lane;
+                        float bt = 0.0f, dc = 1.0f;
+                        if (t < tc) {
+                            const size_t row = (static_cast<size_t>(bl) * p.T + c0 + t) * kVHeads + g * kGroup + hh;
+                            const size_t lh = static_cast<size_t>(l) * kVHeads + g * kGroup + hh;
+                            head_gates_in(gates_ready, __ldg(p.alpha + row), __ldg(p.beta + row), __ldg(p.dt + lh),
+                                          __ldg(p.ssm_a + lh), bt, dc);
+                        }
+                        gpre = dc;
+                        gsuf = dc;
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const float up = __shfl_up_sync(0xffffffffu, gpre, d);
+                            const float dn = __shfl_down_sync(0xffffffffu, gsuf, d);
+                            if (lane >= d) gpre *= up;
+                            if (lane + d < 32) gsuf *= dn;
+                        }
+                        if (lane == 31) tot_s[warp] = gpre;
+                        beta_s[64 * hh + t] = bt;
+                        dec_s[64 * hh + t] = dc;
+                    }
                     pend_qk = true;
                     if (!wait_all(bar_qk, ph_qk)) {
                         failed = true;
@@ -303,37 +350,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                     pend_qk = false;
                     {
-                        const int seg = prep_k ? kS : 0;
-                        float h0, h1, h2;
-                        if (c0 == 0) {
-                            h0 = Hs[3 * (seg + prep_col)];
-                            h1 = Hs[3 * (seg + prep_col) + 1];
-                            h2 = Hs[3 * (seg + prep_col) + 2];
-                        } else {
-                            h0 = Hs[seg + prep_col];
-                            h1 = Hs[2 * kS + seg + prep_col];
-                            h2 = Hs[4 * kS + seg + prep_col];
-                        }
-                        const float4 w = conv_taps(p, l, prep_ch);
-                        const float* xr = Rs + seg + prep_col;
-                        const int kb = prep_col >> 6, cc = (prep_col & 63) >> 3, e = prep_col & 7;
+                        // two adjacent channels per thread (q: tid & 64 == 0, k otherwise), tokens
+                        // [32 (tid >> 7), +32); groups past tc are zero rows
+                        const int pc = (tid & 64 ? kS : 0) + 2 * (tid & 63);  // staged channel of the pair
+                        const int t0 = 32 * (tid >> 7);
+                        const int ch = (pc < kS ? 0 : kKOffset - kS) + g * kS + pc;
+                        const float4 w0 = conv_taps(p, l, ch), w1 = conv_taps(p, l, ch + 1);
+                        float a0 = qk_raw(Rs, Hs, c0, pc, t0 - 3), a1 = qk_raw(Rs, Hs, c0, pc, t0 - 2),
+                              a2 = qk_raw(Rs, Hs, c0, pc, t0 - 1);
+                        float b0 = qk_raw(Rs, Hs, c0, pc + 1, t0 - 3), b1 = qk_raw(Rs, Hs, c0, pc + 1, t0 - 2),
+                              b2 = qk_raw(Rs, Hs, c0, pc + 1, t0 - 1);
+                        const int cpos = pc & (kS - 1);
+                        const int kb = cpos >> 6, cc = (cpos & 63) >> 3, e = cpos & 7;
 #pragma unroll 1
-                        for (int j = 0; j < kC / 8; ++j) {
+                        for (int j = 0; j < 4; ++j) {
+                            const bool any = t0 + 8 * j < tc;
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
-                                const int t = 8 * j + i;
-                                const float x = conv_step(w, h0, h1, h2, xr[min(t, tc - 1) * 2 * kS], t < tc);
+                                const int t = t0 + 8 * j + i;
+                                float x0 = 0.0f, x1 = 0.0f;
+                                if (any) {
+                                    const float2 xv = *reinterpret_cast<const float2*>(Rs + min(t, tc - 1) * 2 * kS + pc);
+                                    x0 = conv_step(w0, a0, a1, a2, xv.x, t < tc);
+                                    x1 = conv_step(w1, b0, b1, b2, xv.y, t < tc);
+                                }
+                                uint32_t hi, lo;
+                                split_pair_rn(x0, x1, hi, lo);
                                 const uint32_t off =
-                                    kOffKQ + kb * kBlk128 + sw128_offset(prep_k ? t : kC + t, cc) + 2 * e;
-                                uint16_t hi, lo;
-                                split_rn(x, hi, lo);
-                                *reinterpret_cast<uint16_t*>(sm + off) = hi;
-                                *reinterpret_cast<uint16_t*>(sm + off + 2 * kBlk128) = lo;
+                                    kOffKQ + kb * kBlk128 + sw128_offset(pc < kS ? kC + t : t, cc) + 2 * e;
+                                *reinterpret_cast<uint32_t*>(sm + off) = hi;
+                                *reinterpret_cast<uint32_t*>(sm + off + 2 * kBlk128) = lo;
                             }
                         }
-                        qk_hist[0] = h0;
-                        qk_hist[1] = h1;
-                        qk_hist[2] = h2;
+                        if (last) {
+                            // the history after the window: the last three raw inputs of channel tid
+                            const int sc = prep_k ? kS + prep_col : prep_col;
+                            qk_hist[0] = qk_raw(Rs, Hs, c0, sc, tc - 3);
+                            qk_hist[1] = qk_raw(Rs, Hs, c0, sc, tc - 2);
+                            qk_hist[2] = qk_raw(Rs, Hs, c0, sc, tc - 1);
+                        }
                     }
                     fence_proxy_async_smem();
                     tc_fence_before();
@@ -350,11 +405,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                             }
                         mma_commit(bar_gram);
                         pend_bar = bar_gram;
+                        pend_mma = true;
                         pend_par = ph_gram;
                     }
                     if (!wait_all(bar_gram, ph_gram)) {
                         failed = true;
                         break;
+                    }
+                    // ---- A_t (prefix) and G(t, n-1) (exclusive suffix) across the two token halves
+                    if (warp < 2 * kGroup) {
+                        const int hh = warp >> 1, half = warp & 1, t = 32 * half + lane;
+                        float sx = __shfl_down_sync(0xffffffffu, gsuf, 1);
+                        if (lane == 31) sx = 1.0f;
+                        A_s[64 * hh + t] = half ? tot_s[2 * hh] * gpre : gpre;
+                        gl_s[64 * hh + t] = t < tc ? (half ? sx : sx * tot_s[2 * hh + 1]) : 0.0f;
                     }
                     // ---- L2 norms from the Gram diagonal (row r: k token r, or q token r - 64)
                     if (warp < 4) {
@@ -372,31 +436,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                 }
 
-                // ---- the next unit's inputs into L2, during this unit's last v head
-                if (h == kGroup - 1 && c0 == 0) {
-                    const long long nu = u + gridDim.x;
-                    if (nu < p.n_units) {
-                        const long long nbl = nu / kKHeads;
-                        const int ng = static_cast<int>(nu - nbl * kKHeads);
-                        int nn = p.T;
-                        if (p.seq_len != nullptr) nn = min(max(__ldg(p.seq_len + nbl / p.L), 0), p.T);
-                        nn = min(nn, kC);
-                        if (tid < kGroup && nn > 0)
-                            prefetch_l2(p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + tid) * kTile,
-                                        kTile * 4);
-                        if (tid >= 32 && tid < 32 + nn) {
-                            const float* row = p.qkv + (static_cast<size_t>(nbl) * p.T + (tid - 32)) * kConvChannels;
-                            prefetch_l2(row + ng * kS, kS * 4);
-                            prefetch_l2(row + kKOffset + ng * kS, kS * 4);
-                            prefetch_l2(row + kVOffset + ng * kGroup * kS, kGroup * kS * 4);
-                            if (write_y)
-                                prefetch_l2(p.z + (static_cast<size_t>(nbl) * p.T + (tid - 32)) * kValueDim +
-                                                ng * kGroup * kS,
-                                            kGroup * kS * 4);
-                        }
-                    }
-                }
-
                 // ---- the state tile by bulk copy (the region is free: the q/k rows are consumed, the
                 //      previous y is written); the gates are computed meanwhile
                 if (c0 == 0) {
@@ -407,30 +446,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                     pend_s = true;
                 }
-                if (tid < kC) {
-                    float bt = 0.0f, dc = 1.0f;
-                    if (tid < tc) {
-                        const size_t row = (static_cast<size_t>(bl) * p.T + c0 + tid) * kVHeads + vh;
-                        head_gates_in(gates_ready, __ldg(p.alpha + row), __ldg(p.beta + row),
-                                      __ldg(p.dt + static_cast<size_t>(l) * kVHeads + vh),
-                                      __ldg(p.ssm_a + static_cast<size_t>(l) * kVHeads + vh), bt, dc);
-                    }
-                    beta_s[tid] = bt;
-                    dec_s[tid] = dc;
-                }
-                __syncthreads();
-                if (tid < kC) {
-                    float a = 1.0f;
-                    for (int r = 0; r <= tid; ++r) a *= dec_s[r];
-                    float gl = 0.0f;
-                    if (tid < tc) {
-                        gl = 1.0f;
-                        for (int r = tid + 1; r < tc; ++r) gl *= dec_s[r];
-                    }
-                    A_s[tid] = a;
-                    gl_s[tid] = gl;
-                }
-
                 // ---- the state: S^T (hi, lo) for the MMA, A_{n-1} S into the update accumulator
                 {
                     const int kh = warp >> 2;  // dims [64 kh, 64 kh + 64)
@@ -445,7 +460,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         for (int k = 0; k < 64; ++k) sv[k] = Rs[(64 * kh + k) * kS + col];
                         __syncthreads();  // the whole tile is read before its split overwrites it
                     } else {
-                        __syncthreads();  // A_s is written
                         uint32_t v[32];
                         tmem_ld32(tmem + kTmS + lane_off + 64 * kh, v);
 #pragma unroll
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         const uint32_t off = kOffS + kh * kBlk128 + sw128_offset(col, j);
                         store_split8(sm + off, sm + off + 2 * kBlk128, sv + 8 * j);
                     }
-                    const float al = A_s[tc - 1];
+                    const float al = A_h[tc - 1];
                     uint32_t v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(al * sv[k]);
@@ -483,7 +497,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                  sw128_desc(kq_lo + kb2 * kBlk128) + 2 * kk, idesc128, (kb2 | kk) == 0);
                     mma_commit(bar_ab);
                     pend_bar = bar_ab;
+                    pend_mma = true;
                     pend_par = ph_ab;
+                }
+                // ---- the next unit's inputs into L2, a third per v head: its state tile h and a third
+                //      of its first chunk's rows
+                if (c0 == 0) {
+                    const long long nu = u + gridDim.x;
+                    if (nu < p.n_units) {
+                        const long long nbl = nu / kKHeads;
+                        const int ng = static_cast<int>(nu - nbl * kKHeads);
+                        int nn = p.T;
+                        if (p.seq_len != nullptr) nn = min(max(__ldg(p.seq_len + nbl / p.L), 0), p.T);
+                        nn = min(nn, kC);
+                        if (tid == 128 && nn > 0)
+                            prefetch_l2(p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + h) * kTile,
+                                        kTile * 4);
+                        const int t = tid - 160 + h * 22;  // tokens [22 h, 22 h + 22)
+                        if (tid >= 160 && tid < 160 + 22 && t < nn) {
+                            const float* row = p.qkv + (static_cast<size_t>(nbl) * p.T + t) * kConvChannels;
+                            prefetch_l2(row + ng * kS, kS * 4);
+                            prefetch_l2(row + kKOffset + ng * kS, kS * 4);
+                            prefetch_l2(row + kVOffset + ng * kGroup * kS, kGroup * kS * 4);
+                            if (write_y)
+                                prefetch_l2(p.z + (static_cast<size_t>(nbl) * p.T + t) * kValueDim + ng * kGroup * kS,
+                                            kGroup * kS * 4);
+                        }
+                    }
                 }
 
                 if (warp < 4) {
@@ -492,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     const int t = (32 * warp + lane) & (kC - 1);
                     const bool is_q = warp >= 2;
                     const bool valid_t = t < tc;
-                    const float rt = valid_t ? (is_q ? rq_s[t] : -beta_s[t] * rk_s[t]) : 0.0f;
+                    const float rt = valid_t ? (is_q ? rq_s[t] : -beta_h[t] * rk_s[t]) : 0.0f;
                     float pr = 1.0f;
 #pragma unroll
                     for (int half = 1; half >= 0; --half) {
@@ -502,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 #pragma unroll
                         for (int i = 31; i >= 0; --i) {
                             const int s = 32 * half + i;
-                            if (s < t) pr *= dec_s[s + 1];
+                            if (s < t) pr *= dec_h[s + 1];
                             // L: s < t (negated, with beta_t); P: s <= t
                             const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
                             val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
@@ -533,40 +573,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     break;
                 }
                 pend_v = false;
+                if (last && warp >= 4) {
+                    // the v history after the window: the last three raw inputs (the staging is reused later)
+                    v_hist[0] = v_raw(Vs, VHs, c0, col, tc - 3);
+                    v_hist[1] = v_raw(Vs, VHs, c0, col, tc - 2);
+                    v_hist[2] = v_raw(Vs, VHs, c0, col, tc - 1);
+                }
 
                 // ---- r_t = b_t (v_t - A_t S0^T k_t) into R^T (warps 4-7, with the v conv, 8 tokens at a
                 //      time), and the inverse X of the solve matrix I - Lneg by 16x16 blocks; both go where
                 //      S0^T was, and d = X r follows as one more MMA
-                if (warp >= 4) {
-                    float h0, h1, h2;
-                    if (c0 == 0) {
-                        h0 = VHs[3 * col];
-                        h1 = VHs[3 * col + 1];
-                        h2 = VHs[3 * col + 2];
-                    } else {
-                        h0 = Vs[col];
-                        h1 = Vs[kS + col];
-                        h2 = Vs[2 * kS + col];
-                    }
+                {
+                    // warps 4-7 take tokens [0, 32), warps 0-3 tokens [32, 64); groups past tc are zero
+                    const int j0 = warp >= 4 ? 0 : kC / 16;
+                    float h0 = v_raw(Vs, VHs, c0, col, 8 * j0 - 3), h1 = v_raw(Vs, VHs, c0, col, 8 * j0 - 2),
+                          h2 = v_raw(Vs, VHs, c0, col, 8 * j0 - 1);
                     const float4 w = conv_taps(p, l, v_ch);
 #pragma unroll 1
-                    for (int j = 0; j < kC / 8; ++j) {
-                        uint32_t a8[8];
-                        tmem_ld8(tmem + kTmAb + lane_off + 8 * j, a8);
+                    for (int j = j0; j < j0 + kC / 16; ++j) {
                         float r8[8];
+                        if (8 * j < tc) {
+                            uint32_t a8[8];
+                            tmem_ld8(tmem + kTmAb + lane_off + 8 * j, a8);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int t = 8 * j + i;
-                            const float v = conv_step(w, h0, h1, h2, Vs[(min(t, tc - 1) + 3) * kS + col], t < tc);
-                            r8[i] = beta_s[t] * (v - A_s[t] * rk_s[t] * u2f(a8[i]));
+                            for (int i = 0; i < 8; ++i) {
+                                const int t = 8 * j + i;
+                                const float v = conv_step(w, h0, h1, h2, Vs[(min(t, tc - 1) + 3) * kS + col], t < tc);
+                                r8[i] = beta_h[t] * (v - A_h[t] * rk_s[t] * u2f(a8[i]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) r8[i] = 0.0f;
                         }
                         const uint32_t off = kOffR + sw128_offset(col, j);
                         store_split8(sm + off, sm + off + kBlk128, r8);
                     }
-                    v_hist[0] = h0;
-                    v_hist[1] = h1;
-                    v_hist[2] = h2;
-                } else if (tid < kC) {
+                }
+                if (tid < kC) {
                     // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
                     const int i = tid >> 4, j = tid & 15;
                     float x[16];
@@ -633,6 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                              sw128_desc(x_lo) + 2 * kk, idesc64, kk == 0);
                     mma_commit(bar_d);
                     pend_bar = bar_d;
+                    pend_mma = true;
                     pend_par = ph_d;
                 }
                 if (!wait_all(bar_d, ph_d)) {
@@ -649,7 +693,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             d[e] = u2f(d8[e]);
-                            ev[e] = gl_s[8 * j + e] * rk_s[8 * j + e] * d[e];
+                            ev[e] = gl_h[8 * j + e] * rk_s[8 * j + e] * d[e];
                         }
                         const uint32_t off = sw128_offset(col, j);
                         store_split8(sm + kOffDT + off, sm + kOffDT + kBlk128 + off, d);
@@ -673,6 +717,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                              idesc128 | kIdescBMnMajor, false);
                     mma_commit(bar_out);
                     pend_bar = bar_out;
+                    pend_mma = true;
                     pend_par = ph_out;
                 }
                 if (!wait_all(bar_out, ph_out)) {
@@ -691,34 +736,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     pend_z = true;
                 }
 
-                if (warp >= 4) {
-                    // ---- o_t = A_t S0^T q_t + (D^T P^T)_t, into o[t][col] for the y epilogue
-                    if (write_y) {
+                if (write_y) {
+                    // ---- o_t = A_t S0^T q_t + (D^T P^T)_t into o[t][col] for the y epilogue (warps 4-7:
+                    //      tokens [0, 32), warps 0-3: [32, 64))
+                    const int j0 = warp >= 4 ? 0 : kC / 16;
 #pragma unroll 1
-                        for (int j = 0; j < kC / 8; ++j) {
-                            uint32_t bq[8], pd[8];
-                            tmem_ld8(tmem + kTmAb + lane_off + kC + 8 * j, bq);
-                            tmem_ld8(tmem + kTmPd + lane_off + 8 * j, pd);
+                    for (int j = j0; j < j0 + kC / 16 && 8 * j < tc; ++j) {
+                        uint32_t bq[8], pd[8];
+                        tmem_ld8(tmem + kTmAb + lane_off + kC + 8 * j, bq);
+                        tmem_ld8(tmem + kTmPd + lane_off + 8 * j, pd);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int t = 8 * j + i;
-                                O_s[t * kS + col] = A_s[t] * rq_s[t] * u2f(bq[i]) + u2f(pd[i]);
-                            }
+                        for (int i = 0; i < 8; ++i) {
+                            const int t = 8 * j + i;
+                            O_s[t * kS + col] = A_h[t] * rq_s[t] * u2f(bq[i]) + u2f(pd[i]);
                         }
                     }
-                } else if (last && write_state) {
-                    // ---- the new state tile: column col, all 128 dims
-                    float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile + col;
+                }
+                if (last && write_state) {
+                    // ---- the new state tile, dims [0, 64) into the P and solve-matrix regions, [64, 128)
+                    //      into the v staging (both free now), for two 32 KB bulk stores
+                    const int kh = warp >> 2;
+                    float* half_s = reinterpret_cast<float*>(sm + (kh ? kOffV : kOffP));
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         uint32_t v[32];
-                        tmem_ld32(tmem + kTmS + lane_off + 32 * q, v);
+                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh + 32 * q, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) __stcs(dst + (32 * q + i) * kS, u2f(v[i]));
+                        for (int i = 0; i < 32; ++i) half_s[(32 * q + i) * kS + col] = u2f(v[i]);
                     }
+                    fence_proxy_async_smem();
                 }
                 tc_fence_before();
                 __syncthreads();
+                if (last && write_state && tid == 32) {
+                    float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile;
+                    bulk_store(dst, base + kOffP, kTile * 2);
+                    bulk_store(dst + kTile / 2, base + kOffV, kTile * 2);
+                    bulk_commit();
+                }
                 if (write_y) {
                     if (!wait_all(bar_z, ph_z)) {
                         failed = true;
@@ -727,13 +782,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     pend_z = false;
                     const float4 w4 = *reinterpret_cast<const float4*>(nw_s + lane * 4);
                     for (int t = warp; t < tc; t += kTcThreads / 32) {
-                        const float4 o4 = *reinterpret_cast<const float4*>(O_s + t * kS + lane * 4);
+                        float4* o4 = reinterpret_cast<float4*>(O_s + t * kS + lane * 4);
                         const float4 z4 = *reinterpret_cast<const float4*>(Zs + t * kS + lane * 4);
-                        __stcs(reinterpret_cast<float4*>(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim +
-                                                         vh * kS + lane * 4),
-                               gated_rms_norm4(o4, z4, w4, silu_gate));
+                        *o4 = gated_rms_norm4(*o4, z4, w4, silu_gate);
+                    }
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                    if (warp == 1) {
+                        for (int t = lane; t < tc; t += 32)
+                            bulk_store(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS,
+                                       base + kOffO + t * kS * 4, kS * 4);
+                        bulk_commit();
                     }
                 }
+                // the bulk stores have read shared memory before it is rewritten
+                if (warp == 1) bulk_wait_read();
                 __syncthreads();  // o, z and the operand blocks are rewritten next
             }
             if (!failed && write_state && warp >= 4) {
@@ -753,13 +816,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     }
 
     // MMAs and copies still in flight finish before the tensor memory is freed (bounded).
-    if (tid == 0 && failed) (void)mbar_wait_bounded(pend_bar, pend_par);
+    if (tid == 0 && failed && pend_mma) (void)mbar_wait_bounded(pend_bar, pend_par);
     if (tid == 32 && failed) {
         if (pend_qk) (void)mbar_wait_bounded(bar_qk, ph_qk);
         if (pend_s) (void)mbar_wait_bounded(bar_s, ph_s);
         if (pend_z) (void)mbar_wait_bounded(bar_z, ph_z);
         if (pend_v) (void)mbar_wait_bounded(bar_v, ph_v);
     }
+    if (warp == 1) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {

@@ -47,7 +47,7 @@ def test_ab_gates_match_oracle(cuda_device, B, L, T, E):
     assert _rows_rel_err(beta.cpu().numpy(), rb) <= U.TOL
 
 
-@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("T", [1, 4, 36])
 def test_step_fed_by_ab_gates_matches_oracle(cuda_device, T):
     import gated_deltanet_linear_step_gb300 as g
 

@@ -17,7 +17,7 @@ def _case(B, L, T, name="verify_b16_l36_t8_ragged"):
 
 
 def test_longest_window_matches_oracle(cuda_device):
-    """T at its maximum (1024 tokens, 64 chunks of the multi-token kernel) against the oracle."""
+    """T at its maximum (1024 tokens, 16 chunks of the tensor-core kernel) against the oracle."""
     import gated_deltanet_linear_step_gb300 as g
 
     T = g.gdn_get_geometry()["max_t"]
@@ -31,7 +31,7 @@ def test_longest_window_matches_oracle(cuda_device):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("T", [1, 5, 40])
 def test_negative_and_all_zero_lengths_change_nothing(cuda_device, T):
     import gated_deltanet_linear_step_gb300 as g
 
@@ -71,13 +71,13 @@ def test_single_token_call_with_lengths(cuda_device):
 
 
 @pytest.mark.parametrize("T,name", [(1, "decode_b64_l36_t1"), (5, "verify_b16_l36_t8_ragged"),
-                                    (20, "verify_b16_l36_t8_ragged")])
+                                    (20, "verify_b16_l36_t8_ragged"), (40, "verify_b16_l36_t8_ragged")])
 @pytest.mark.parametrize("gate", ["sigmoid", "silu"])
 def test_saturated_activations_match_oracle(cuda_device, T, name, gate):
     """Inputs scaled so that SiLU, sigmoid and softplus see arguments far beyond +-88, where e^-x
     overflows or underflows in fp32: SiLU must go to x or 0, sigmoid to 1 or 0, beta to 0 or 1 and
-    decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel and both instances of
-    the multi-token kernel."""
+    decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel and the three
+    multi-token kernels."""
     import gated_deltanet_linear_step_gb300 as g
 
     w, h = _case(3, 2, T, name=name)

@@ -38,6 +38,9 @@ SMALL = [
     ("decode_b64_l36_t1", dict(B=1, L=2, T=9)),
     ("decode_b64_l36_t1", dict(B=2, L=1, T=17)),
     ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=20)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=40)),
+    ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=1, L=1, T=64)),
+    ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=70)),
 ]
 
 
@@ -136,8 +139,9 @@ def test_t_tokens_in_one_call_equal_t_single_calls(g):
 
 
 # (window length, prefix length): both calls of a case run the same kernel (windows of up to 8
-# tokens run the shared-memory kernel, longer ones the tensor-core kernel), so they agree bit for bit.
-@pytest.mark.parametrize("T,P", [(8, 3), (12, 10)])
+# tokens run the shared-memory kernel, 9 to 31 the register kernel, 32 or more the tensor-core
+# kernel, in chunks of 64), so they agree bit for bit.
+@pytest.mark.parametrize("T,P", [(8, 3), (12, 10), (40, 33), (70, 66)])
 def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
     w, h = _small(dict(B=3, L=2, T=T))
     dev = torch.device("cuda:0")
@@ -194,8 +198,9 @@ def test_deterministic_and_batch_permutation_equivariant(g):
     assert torch.equal(c["conv_state"], a["conv_state"][perm])
 
 
-def test_verify_window_then_commit(g):
-    w, h = _small(dict(B=3, L=2, T=6))
+@pytest.mark.parametrize("T", [6, 40])
+def test_verify_window_then_commit(g, T):
+    w, h = _small(dict(B=3, L=2, T=T))
     dev = torch.device("cuda:0")
     win = U.to_device(h, dev)
     y = torch.full(win["z"].shape, float("nan"), device=dev)
@@ -208,8 +213,8 @@ def test_verify_window_then_commit(g):
     assert torch.equal(y, yref)
     assert torch.equal(win["state"], torch.from_numpy(h["state"]).to(dev))
     assert torch.equal(win["conv_state"], torch.from_numpy(h["conv_state"]).to(dev))
-    # phase 2: keep 2, 6 and 0 tokens
-    n_keep = torch.tensor([2, 6, 0], dtype=torch.int32, device=dev)
+    # phase 2: keep 2, T and 0 tokens
+    n_keep = torch.tensor([2, T, 0], dtype=torch.int32, device=dev)
     g.gdn_verify_commit(win["qkv"], win["alpha"], win["beta"], win["dt"], win["ssm_a"], win["conv_w"],
                         win["conv_state"], win["state"], n_keep)
     exp = U.to_device(h, dev)
@@ -267,7 +272,7 @@ def test_bad_arguments_raise_and_launch_nothing(g):
     assert torch.equal(t["state"], before) and torch.all(y == 0)
 
 
-@pytest.mark.parametrize("T", [1, 4, 12])
+@pytest.mark.parametrize("T", [1, 4, 12, 40, 70])
 def test_no_y_and_no_state_write_flags_match_the_full_call(g, T):
     """FLAG_NO_Y gives the full call's state and conv_state bit for bit and writes no y;
     FLAG_NO_STATE_WRITE gives its y bit for bit and leaves both states untouched."""

@@ -12,7 +12,7 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [1, 3, 20])
+@pytest.mark.parametrize("T", [1, 3, 20, 40, 70])
 def test_every_v_head_of_a_k_head_sees_the_old_conv_history(cuda_device, T):
     """The q/k conv history of head g is read by the work of all three v heads 3g..3g+2 and
     rolled once. Old history entries 1000x larger than any new input make a read of the
