@@ -169,10 +169,39 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# Windows of 2-8 tokens run the kernel with the tiles in shared memory, 9-31 the register
+# window kernel, 32 or more the tensor-core chunk kernel (the library's dispatch).
+CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 8, 32, 64
+
+
 def kernel_sources(T: int) -> list:
-    """The sources of the kernel a call with T tokens runs (the single-token kernel or the window kernel)."""
-    names = ("gdn_decode_t1.cu", "gdn_device.cuh") if T == 1 else ("gdn_step.cu", "gdn_device.cuh")
+    """The sources of the kernel a call with T tokens runs."""
+    if T == 1:
+        names = ("gdn_decode_t1.cu", "gdn_device.cuh")
+    elif T <= CHUNK_MAX_T:
+        names = ("gdn_chunk.cu", "gdn_device.cuh")
+    elif T < TC_MIN_T:
+        names = ("gdn_step.cu", "gdn_device.cuh")
+    else:
+        names = ("gdn_window_tc.cu", "gdn_tc.cuh", "gdn_device.cuh")
     return [os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", f) for f in names]
+
+
+def tc_mma_flops(w: W.Workload, lens) -> float:
+    """Tensor-core flops of one call on the chunk kernel: per 64-token chunk and k head the Gram
+    matrix (128x128x128), per chunk and v head the state, solve, output and update products
+    (128x128x128, 128x64x64 twice, 128x128x64), each as three BF16 MMAs. A window longer than
+    one chunk recomputes the Gram matrix for each v head."""
+    gram = 3 * 2 * 128 * 128 * 128
+    per_v = 3 * 2 * (128 * 128 * 128 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+    ns = [w.T] * w.B if lens is None else [int(n) for n in lens]
+    total = 0.0
+    for n in ns:
+        if n <= 0:
+            continue
+        chunks = -(-n // TC_CHUNK)
+        total += chunks * (gram * (3 if n > TC_CHUNK else 1) + 3 * per_v)
+    return total * w.L * 16
 
 
 def committed_traffic(workload: str, T: int):
@@ -427,7 +456,22 @@ def roofline_of(w: W.Workload, lens, mean_launch_s: float, traffic) -> dict:
         roof.update({"bound": "alu", "achieved": tf, "peak": ALU_PEAK_TFLOPS, "unit": "TFLOP/s",
                      "frac": tf / ALU_PEAK_TFLOPS, "peak_kind": ALU_PEAK_KIND, "hbm_gbs": achieved,
                      "hbm_frac": achieved / peak, "flops_per_launch": flops})
+    if w.T >= TC_MIN_T:
+        # the chunk kernel runs the definition's contractions on the tensor cores: their rate, for context
+        tflops = tc_mma_flops(w, lens) / mean_launch_s / 1e12
+        bf16 = measured_bf16_tflops()
+        roof.update({"tensor_tflops": tflops, "tensor_peak": bf16, "tensor_frac": tflops / bf16,
+                     "tensor_note": "BF16 MMA flops (three per product) of the chunk kernel, against the "
+                                    "measured dense BF16 peak (burst)"})
     return roof
+
+
+def measured_bf16_tflops() -> float:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1900.0
 
 
 def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
