@@ -185,32 +185,37 @@ __device__ __forceinline__ void load_hist(const Params& p, long long bl, int ch,
     h[2] = cs[2];
 }
 
-// Conv + SiLU of one channel for the chunk's tokens; the history rolls in h.
-__device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, int tc, float (&h)[3],
-                                           float (&out)[kC]) {
+// The conv history after a chunk of tc tokens: its last three raw inputs, the older
+// ones from the history before it (h on entry). Used alone for a channel whose conv
+// output is not needed.
+__device__ __forceinline__ void roll_history(const float* rows, int cc, int tc, float (&h)[3]) {
+    const float i0 = h[0], i1 = h[1], i2 = h[2];
 #pragma unroll
-    for (int t = 0; t < kC; ++t) {
-        out[t] = 0.0f;
-        if (t < tc) {
-            const float xt = rows[t * kUnitCh + cc];
-            out[t] = siluf_(conv4(w, h[0], h[1], h[2], xt));
-            h[0] = h[1];
-            h[1] = h[2];
-            h[2] = xt;
-        }
+    for (int k = 0; k < 3; ++k) {
+        const int tau = tc - 3 + k;  // token of history entry k; < 0 reaches into the old history
+        h[k] = tau >= 0 ? rows[max(tau, 0) * kUnitCh + cc] : (tau == -3 ? i0 : (tau == -2 ? i1 : i2));
     }
 }
 
-// The history roll of conv_chunk alone, for a channel whose conv output is not needed.
-__device__ __forceinline__ void roll_history(const float* rows, int cc, int tc, float (&h)[3]) {
+// Conv + SiLU of one channel over the chunk's tc tokens (zero past tc); h holds the
+// history before the chunk and leaves holding the one after it. The shifts are
+// unconditional and the result a select, so that the unrolled tokens interleave (a
+// shift under t < tc became a branch per token); rows past tc are re-reads of row
+// tc - 1, and the history after the chunk is read back from the rows.
+__device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, int tc, float (&h)[3],
+                                           float (&out)[kC]) {
+    float h0 = h[0], h1 = h[1], h2 = h[2];
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
-        if (t < tc) {
-            h[0] = h[1];
-            h[1] = h[2];
-            h[2] = rows[t * kUnitCh + cc];
-        }
+        const float xt = rows[max(min(t, tc - 1), 0) * kUnitCh + cc];
+        const float xc = conv4(w, h0, h1, h2, xt);
+        h0 = h1;
+        h1 = h2;
+        h2 = xt;
+        const float y = siluf_(xc);
+        out[t] = t < tc ? y : 0.0f;
     }
+    roll_history(rows, cc, tc, h);
 }
 
 // Pass A on one tile: red[n] = sum_i S[i][col] X[i][n] for this lane's column

@@ -230,3 +230,12 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// Waits until at most one of this thread's committed bulk async-groups is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+}  // namespace gdn

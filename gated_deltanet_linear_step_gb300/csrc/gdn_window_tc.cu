@@ -130,16 +130,18 @@ __device__ __forceinline__ float4 conv_taps(const TcParams& p, int l, int ch) {
 }
 
 // One token of the causal conv + SiLU of a channel: xc from the history (h0
-// oldest) and x; the history shifts only for a valid token. Returns SiLU(xc),
-// or 0 for an invalid one.
+// oldest) and x, then the history shifts. Returns SiLU(xc), or 0 for a token
+// past the window (whose x and history are then don't-cares: the history after
+// the window is read from the staged rows instead). The shift and the result
+// are unconditional moves and a select, so that the unrolled tokens interleave;
+// a predicated shift became a branch per token and serialised them.
 __device__ __forceinline__ float conv_step(float4 w, float& h0, float& h1, float& h2, float x, bool valid) {
     const float xc = conv4(w, h0, h1, h2, x);
-    if (valid) {
-        h0 = h1;
-        h1 = h2;
-        h2 = x;
-    }
-    return valid ? siluf_(xc) : 0.0f;
+    h0 = h1;
+    h1 = h2;
+    h2 = x;
+    const float s = siluf_(xc);
+    return valid ? s : 0.0f;
 }
 
 // Raw q/k input of staged channel c (q at [0, 128), k at [128, 256)) at token c0 + t (t in
@@ -153,6 +155,11 @@ __device__ __forceinline__ float qk_raw(const float* Rs, const float* Hs, int c0
 // row t + 3; before the window start (c0 == 0, t < 0) it is the staged conv history.
 __device__ __forceinline__ float v_raw(const float* Vs, const float* VHs, int c0, int col, int t) {
     return (c0 == 0 && t < 0) ? VHs[3 * col + 3 + t] : Vs[(t + 3) * kS + col];
+}
+
+// Valid tokens of sequence b: T, or its seq_len clamped to [0, T].
+__device__ __forceinline__ int unit_len(const TcParams& p, int b) {
+    return p.seq_len != nullptr ? min(max(__ldg(p.seq_len + b), 0), p.T) : p.T;
 }
 
 // Three BF16 products of two hi/lo operand pairs into d (accumulate = 0 only for the first).
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     float* L_s = reinterpret_cast<float*>(sm + kOffL);
     float* O_s = reinterpret_cast<float*>(sm + kOffO);
     float* Xs = reinterpret_cast<float*>(sm + kOffX);  // fp32 [64][64]; blocks above the diagonal hold temporaries
-    const float* Rs = reinterpret_cast<const float*>(sm + kOffS);       // staged q|k rows, then the fp32 state tile
+    const float* Rs = reinterpret_cast<const float*>(sm + kOffS);       // staged q|k rows
     const float* Hs = reinterpret_cast<const float*>(sm + kOffHist);    // staged q/k history
     const float* Vs = reinterpret_cast<const float*>(sm + kOffV);       // staged v rows (token t at row t + 3)
     const float* VHs = reinterpret_cast<const float*>(sm + kOffVHist);  // staged v history (window start)
@@ -220,6 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     uint32_t pend_bar = 0, pend_par = 0;  // (thread 0) the last MMA commit, drained if a wait gives up
     bool pend_mma = false;                // (thread 0) an MMA commit not yet waited for
     bool pend_qk = false, pend_s = false, pend_z = false, pend_v = false;  // copies issued, not yet waited for
+    bool qk_ahead = false, s_ahead = false;  // the next unit's first q|k rows / state tile already requested
     bool failed = false;
     bool give_up = (p.flags & kTestGiveUp) != 0;
 
@@ -232,6 +240,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         ph ^= 1u;
         tc_fence_after();
         return true;
+    };
+    // The chunk's q|k rows (1 KB per token) into the region S0^T later holds, the history before
+    // them beside it; by warp 1, after its bulk stores have read that region.
+    auto issue_qk = [&](long long xbl, int xg, int xc0, int xtc) {
+        if (warp == 1) {
+            bulk_wait_read();
+            if (lane == 0) mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>(xtc) * 1024u + 3072u);
+            __syncwarp();
+            for (int t = lane; t < xtc; t += 32) {
+                const float* row = p.qkv + (static_cast<size_t>(xbl) * p.T + xc0 + t) * kConvChannels;
+                bulk_load(base + kOffS + t * 1024, row + xg * kS, kS * 4, bar_qk);
+                bulk_load(base + kOffS + t * 1024 + 512, row + kKOffset + xg * kS, kS * 4, bar_qk);
+            }
+            if (lane == 0) {
+                if (xc0 == 0) {
+                    const float* cs = p.conv_state + static_cast<size_t>(xbl) * kConvChannels * (kDConv - 1);
+                    bulk_load(base + kOffHist, cs + xg * kS * 3, kS * 12, bar_qk);
+                    bulk_load(base + kOffHist + 1536, cs + (kKOffset + xg * kS) * 3, kS * 12, bar_qk);
+                } else {
+                    for (int r = 0; r < 3; ++r) {
+                        const float* row = p.qkv + (static_cast<size_t>(xbl) * p.T + xc0 - 3 + r) * kConvChannels;
+                        bulk_load(base + kOffHist + r * 1024, row + xg * kS, kS * 4, bar_qk);
+                        bulk_load(base + kOffHist + r * 1024 + 512, row + kKOffset + xg * kS, kS * 4, bar_qk);
+                    }
+                }
+            }
+        }
+        pend_qk = true;
+    };
+    // A state tile in two 32 KB halves: dims [0, 64) into the P and solve-matrix regions, [64, 128)
+    // into the v staging; by thread 32, once its state bulk store (if any) has read those regions
+    // (its last group, when y is written, holds y rows and may still be reading).
+    auto issue_s = [&](long long xbl, int xvh) {
+        if (tid == 32) {
+            if (write_y)
+                bulk_wait_read_one();
+            else
+                bulk_wait_read();
+            const float* src = p.state + (static_cast<size_t>(xbl) * kVHeads + xvh) * kTile;
+            mbar_arrive_expect_tx(bar_s, kTile * 4);
+            bulk_load(base + kOffP, src, kTile * 2, bar_s);
+            bulk_load(base + kOffV, src + kTile / 2, kTile * 2, bar_s);
+        }
+        pend_s = true;
     };
 
     const uint32_t idesc128 = mma_idesc(128), idesc64 = mma_idesc(64);
@@ -248,11 +300,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         const int g = static_cast<int>(u - bl * kKHeads);
         const int l = static_cast<int>(bl % p.L);
         const int b = static_cast<int>(bl / p.L);
-        int n = p.T;
-        if (p.seq_len != nullptr) n = min(max(__ldg(p.seq_len + b), 0), p.T);
+        const int n = unit_len(p, b);
         if (n == 0) continue;
         const bool multi = n > kC;
         if (write_y && tid < kS) nw_s[tid] = __ldg(p.ssm_norm + static_cast<size_t>(l) * kS + tid);
+        // the first chunk's q|k rows and the first v head's state tile, unless requested a unit ahead
+        if (!qk_ahead) issue_qk(bl, g, 0, min(n, kC));
+        if (!s_ahead) issue_s(bl, g * kGroup);
+        qk_ahead = s_ahead = false;
 
         // q (threads 0-127) or k (128-255) channel of this thread in the q/k preparation
         const bool prep_k = tid >= kS;
@@ -275,50 +330,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 const bool last = c0 + tc == n;
                 const int nh = c0 > 0 ? 3 : 0;  // history rows staged with the chunk's rows
 
-                // ---- v rows of this v head (and, at the window start, its conv history) by bulk copy
-                if (warp == 2) {
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>(tc + nh) * kS * 4 + (c0 == 0 ? kS * 12 : 0));
-                    __syncwarp();
-                    for (int i = lane; i < tc + nh; i += 32) {
-                        const int t = i - nh;
-                        bulk_load(base + kOffV + (t + 3) * kS * 4,
-                                  p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels + kVOffset + vh * kS,
-                                  kS * 4, bar_v);
-                    }
-                    if (lane == 0 && c0 == 0)
-                        bulk_load(base + kOffVHist,
-                                  p.conv_state + (static_cast<size_t>(bl) * kConvChannels + kVOffset + vh * kS) * 3,
-                                  kS * 12, bar_v);
-                }
-                pend_v = true;
-
                 if (h == 0 || multi) {
-                    // ---- q/k: the chunk's rows and the history before it by bulk copy (warp 1), then
-                    //      conv, SiLU and split into the [K;Q] rows, 8 tokens at a time
-                    if (warp == 1) {
-                        if (lane == 0) mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>(tc) * 1024u + 3072u);
-                        __syncwarp();
-                        for (int t = lane; t < tc; t += 32) {
-                            const float* row = p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels;
-                            bulk_load(base + kOffS + t * 1024, row + g * kS, kS * 4, bar_qk);
-                            bulk_load(base + kOffS + t * 1024 + 512, row + kKOffset + g * kS, kS * 4, bar_qk);
-                        }
-                        if (lane == 0) {
-                            if (c0 == 0) {
-                                const float* cs = p.conv_state + static_cast<size_t>(bl) * kConvChannels * (kDConv - 1);
-                                bulk_load(base + kOffHist, cs + g * kS * 3, kS * 12, bar_qk);
-                                bulk_load(base + kOffHist + 1536, cs + (kKOffset + g * kS) * 3, kS * 12, bar_qk);
-                            } else {
-                                for (int r = 0; r < 3; ++r) {
-                                    const float* row =
-                                        p.qkv + (static_cast<size_t>(bl) * p.T + c0 - 3 + r) * kConvChannels;
-                                    bulk_load(base + kOffHist + r * 1024, row + g * kS, kS * 4, bar_qk);
-                                    bulk_load(base + kOffHist + r * 1024 + 512, row + kKOffset + g * kS, kS * 4, bar_qk);
-                                }
-                            }
-                        }
-                    }
+                    // ---- q/k: the chunk's rows (requested earlier for a unit's first chunk), then conv,
+                    //      SiLU and split into the [K;Q] rows; the gates of the three v heads meanwhile
+                    if (c0 > 0 || h > 0) issue_qk(bl, g, c0, tc);
                     // gates of the three v heads for the chunk's tokens (warps 0-5: head warp / 2, tokens
                     // [32 (warp & 1), +32)), with in-warp prefix and suffix products of the decays
                     if (warp < 2 * kGroup) {
@@ -343,7 +358,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         beta_s[64 * hh + t] = bt;
                         dec_s[64 * hh + t] = dc;
                     }
-                    pend_qk = true;
                     if (!wait_all(bar_qk, ph_qk)) {
                         failed = true;
                         break;
@@ -436,17 +450,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                 }
 
-                // ---- the state tile by bulk copy (the region is free: the q/k rows are consumed, the
-                //      previous y is written); the gates are computed meanwhile
-                if (c0 == 0) {
-                    if (tid == 32) {
-                        mbar_arrive_expect_tx(bar_s, kTile * 4);
-                        bulk_load(base + kOffS, p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile, kTile * 4,
-                                  bar_s);
-                    }
-                    pend_s = true;
-                }
-                // ---- the state: S^T (hi, lo) for the MMA, A_{n-1} S into the update accumulator
+                // ---- the state: S^T (hi, lo) for the MMA, A_{n-1} S into the update accumulator. At
+                //      a window start the tile arrived by bulk copy in two halves (P and solve-matrix
+                //      regions, v staging); later chunks continue from tensor memory.
                 {
                     const int kh = warp >> 2;  // dims [64 kh, 64 kh + 64)
                     float sv[64];
@@ -456,9 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                             break;
                         }
                         pend_s = false;
+                        const float* half_s = reinterpret_cast<const float*>(sm + (kh ? kOffV : kOffP));
 #pragma unroll
-                        for (int k = 0; k < 64; ++k) sv[k] = Rs[(64 * kh + k) * kS + col];
-                        __syncthreads();  // the whole tile is read before its split overwrites it
+                        for (int k = 0; k < 64; ++k) sv[k] = half_s[k * kS + col];
                     } else {
                         uint32_t v[32];
                         tmem_ld32(tmem + kTmS + lane_off + 64 * kh, v);
@@ -468,6 +474,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 #pragma unroll
                         for (int k = 0; k < 32; ++k) sv[32 + k] = u2f(v[k]);
                     }
+                    // the y stores of the previous v head have read the region S0^T goes to; the tile's
+                    // halves are read before the v rows and the solve matrix replace them
+                    if (warp == 1) bulk_wait_read();
+                    __syncthreads();
+                    // ---- v rows of this v head (and, at the window start, its conv history) by bulk copy
+                    if (warp == 2) {
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(bar_v,
+                                                  static_cast<uint32_t>(tc + nh) * kS * 4 + (c0 == 0 ? kS * 12 : 0));
+                        __syncwarp();
+                        for (int i = lane; i < tc + nh; i += 32) {
+                            const int t = i - nh;
+                            bulk_load(base + kOffV + (t + 3) * kS * 4,
+                                      p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels + kVOffset +
+                                          vh * kS,
+                                      kS * 4, bar_v);
+                        }
+                        if (lane == 0 && c0 == 0)
+                            bulk_load(base + kOffVHist,
+                                      p.conv_state + (static_cast<size_t>(bl) * kConvChannels + kVOffset + vh * kS) * 3,
+                                      kS * 12, bar_v);
+                    }
+                    pend_v = true;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const uint32_t off = kOffS + kh * kBlk128 + sw128_offset(col, j);
@@ -501,23 +530,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     pend_par = ph_ab;
                 }
                 // ---- the next unit's inputs into L2, a third per v head: its state tile h and a third
-                //      of its first chunk's rows
+                //      of its first chunk's rows (warps 4-5)
                 if (c0 == 0) {
                     const long long nu = u + gridDim.x;
                     if (nu < p.n_units) {
                         const long long nbl = nu / kKHeads;
                         const int ng = static_cast<int>(nu - nbl * kKHeads);
-                        int nn = p.T;
-                        if (p.seq_len != nullptr) nn = min(max(__ldg(p.seq_len + nbl / p.L), 0), p.T);
-                        nn = min(nn, kC);
-                        if (tid == 128 && nn > 0)
+                        const int nn = min(unit_len(p, static_cast<int>(nbl / p.L)), kC);
+                        if (tid == 128 && nn > 0 && h > 0)
                             prefetch_l2(p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + h) * kTile,
                                         kTile * 4);
                         const int t = tid - 160 + h * 22;  // tokens [22 h, 22 h + 22)
                         if (tid >= 160 && tid < 160 + 22 && t < nn) {
                             const float* row = p.qkv + (static_cast<size_t>(nbl) * p.T + t) * kConvChannels;
-                            prefetch_l2(row + ng * kS, kS * 4);
-                            prefetch_l2(row + kKOffset + ng * kS, kS * 4);
                             prefetch_l2(row + kVOffset + ng * kGroup * kS, kGroup * kS * 4);
                             if (write_y)
                                 prefetch_l2(p.z + (static_cast<size_t>(nbl) * p.T + t) * kValueDim + ng * kGroup * kS,
@@ -526,148 +551,161 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                 }
 
+                // ---- two warp groups at once. Warps 0-3: the solve matrix and P from the Gram rows, then
+                //      the inverse X of I - Lneg by 16x16 blocks and X as the operand of d = X r.
+                //      Warps 4-7: the v conv and r_t = b_t (v_t - A_t S0^T k_t) into R^T.
+                bool group_late = false;
                 if (warp < 4) {
-                    // ---- solve matrix (k rows, warps 0-1) and P (q rows, warps 2-3) from the Gram rows,
-                    //      s from 63 down so that G(s, t) = a_{s+1} ... a_t builds up as one running product
-                    const int t = (32 * warp + lane) & (kC - 1);
-                    const bool is_q = warp >= 2;
-                    const bool valid_t = t < tc;
-                    const float rt = valid_t ? (is_q ? rq_s[t] : -beta_h[t] * rk_s[t]) : 0.0f;
-                    float pr = 1.0f;
+                    {
+                        // s from 63 down so that G(s, t) = a_{s+1} ... a_t builds up as one running product
+                        const int t = (32 * warp + lane) & (kC - 1);
+                        const bool is_q = warp >= 2;
+                        const bool valid_t = t < tc;
+                        const float rt = valid_t ? (is_q ? rq_s[t] : -beta_h[t] * rk_s[t]) : 0.0f;
+                        float pr = 1.0f;
 #pragma unroll
-                    for (int half = 1; half >= 0; --half) {
-                        uint32_t raw[32];
-                        tmem_ld32(tmem + kTmGram + lane_off + 32 * half, raw);
-                        float val[32];
+                        for (int half = 1; half >= 0; --half) {
+                            uint32_t raw[32];
+                            tmem_ld32(tmem + kTmGram + lane_off + 32 * half, raw);
+                            float val[32];
 #pragma unroll
-                        for (int i = 31; i >= 0; --i) {
-                            const int s = 32 * half + i;
-                            if (s < t) pr *= dec_h[s + 1];
-                            // L: s < t (negated, with beta_t); P: s <= t
-                            const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
-                            val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
-                        }
-                        if (!is_q) {
-                            float* Lr = L_s + t * kLStride + 32 * half;
+                            for (int i = 31; i >= 0; --i) {
+                                const int s = 32 * half + i;
+                                if (s < t) pr *= dec_h[s + 1];
+                                // L: s < t (negated, with beta_t); P: s <= t
+                                const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
+                                val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
+                            }
+                            if (!is_q) {
+                                float* Lr = L_s + t * kLStride + 32 * half;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                *reinterpret_cast<float4*>(Lr + 4 * j) =
-                                    make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
-                        } else {
+                                for (int j = 0; j < 8; ++j)
+                                    *reinterpret_cast<float4*>(Lr + 4 * j) =
+                                        make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const uint32_t off = kOffP + sw128_offset(t, 4 * half + j);
-                                store_split8(sm + off, sm + off + 64 * 128, val + 8 * j);
+                                for (int j = 0; j < 4; ++j) {
+                                    const uint32_t off = kOffP + sw128_offset(t, 4 * half + j);
+                                    store_split8(sm + off, sm + off + 64 * 128, val + 8 * j);
+                                }
                             }
                         }
                     }
-                }
-                fence_proxy_async_smem();
-                __syncthreads();  // the solve matrix and P are written
-                if (!wait_all(bar_ab, ph_ab)) {
-                    failed = true;
-                    break;
-                }
-                if (!wait_all(bar_v, ph_v)) {
-                    failed = true;
-                    break;
-                }
-                pend_v = false;
-                if (last && warp >= 4) {
-                    // the v history after the window: the last three raw inputs (the staging is reused later)
-                    v_hist[0] = v_raw(Vs, VHs, c0, col, tc - 3);
-                    v_hist[1] = v_raw(Vs, VHs, c0, col, tc - 2);
-                    v_hist[2] = v_raw(Vs, VHs, c0, col, tc - 1);
-                }
-
-                // ---- r_t = b_t (v_t - A_t S0^T k_t) into R^T (warps 4-7, with the v conv, 8 tokens at a
-                //      time), and the inverse X of the solve matrix I - Lneg by 16x16 blocks; both go where
-                //      S0^T was, and d = X r follows as one more MMA
-                {
-                    // warps 4-7 take tokens [0, 32), warps 0-3 tokens [32, 64); groups past tc are zero
-                    const int j0 = warp >= 4 ? 0 : kC / 16;
-                    float h0 = v_raw(Vs, VHs, c0, col, 8 * j0 - 3), h1 = v_raw(Vs, VHs, c0, col, 8 * j0 - 2),
-                          h2 = v_raw(Vs, VHs, c0, col, 8 * j0 - 1);
-                    const float4 w = conv_taps(p, l, v_ch);
+                    named_barrier(1, 128);
+                    if (tid < kC) {
+                        // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
+                        const int i = tid >> 4, j = tid & 15;
+                        float x[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            const float* Lr = L_s + (16 * i + r) * kLStride + 16 * i;
+                            float acc = 0.0f;
+#pragma unroll
+                            for (int m = 0; m < r; ++m) acc = fmaf(Lr[m], x[m], acc);
+                            x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
+                        }
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
+                    }
+                    named_barrier(1, 128);
+                    {
+                        // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj; thread
+                        // (r, c pair) of each 16x16 block
+                        const int r = tid >> 3, c = 2 * (tid & 7);
+#pragma unroll
+                        for (int dist = 1; dist < 4; ++dist) {
+                            for (int j = 0; j + dist < 4; ++j) {
+                                const int i = j + dist;
+                                float y0 = 0.0f, y1 = 0.0f;
+                                for (int k = j; k < i; ++k) {
+                                    const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
+#pragma unroll
+                                    for (int m = 0; m < 16; ++m) {
+                                        const float2 xv = *reinterpret_cast<const float2*>(Xs + (16 * k + m) * kC + 16 * j + c);
+                                        y0 = fmaf(Lr[m], xv.x, y0);
+                                        y1 = fmaf(Lr[m], xv.y, y1);
+                                    }
+                                }
+                                *reinterpret_cast<float2*>(Xs + (16 * j + r) * kC + 16 * i + c) = make_float2(y0, y1);
+                            }
+                            named_barrier(1, 128);
+                            for (int j = 0; j + dist < 4; ++j) {
+                                const int i = j + dist;
+                                float x0 = 0.0f, x1 = 0.0f;
+#pragma unroll
+                                for (int m = 0; m < 16; ++m) {
+                                    const float xm = Xs[(16 * i + r) * kC + 16 * i + m];
+                                    const float2 yv = *reinterpret_cast<const float2*>(Xs + (16 * j + m) * kC + 16 * i + c);
+                                    x0 = fmaf(xm, yv.x, x0);
+                                    x1 = fmaf(xm, yv.y, x1);
+                                }
+                                *reinterpret_cast<float2*>(Xs + (16 * i + r) * kC + 16 * j + c) = make_float2(x0, x1);
+                            }
+                            named_barrier(1, 128);
+                        }
+                    }
+                    {
+                        // X as the BF16 operand [t][s]; blocks above the diagonal are zero
+                        const int t = tid >> 1;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int j = 4 * (tid & 1) + q4;  // columns [8 j, 8 j + 8)
+                            float xv[8];
+                            const bool upper = (j >> 1) > (t >> 4);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
+                            const uint32_t off = kOffXop + sw128_offset(t, j);
+                            store_split8(sm + off, sm + off + 64 * 128, xv);
+                        }
+                    }
+                } else {
+                    // warps 4-7: the state MMA and the v rows, then r
+                    bool late = !mbar_wait_bounded(bar_ab, ph_ab);
+                    late = late || !mbar_wait_bounded(bar_v, ph_v);
+                    group_late = named_barrier_or(2, 128, late);
+                    if (!group_late) {
+                        tc_fence_after();
+                        if (last) {
+                            // the v history after the window: the last three raw inputs (the staging is reused later)
+                            v_hist[0] = v_raw(Vs, VHs, c0, col, tc - 3);
+                            v_hist[1] = v_raw(Vs, VHs, c0, col, tc - 2);
+                            v_hist[2] = v_raw(Vs, VHs, c0, col, tc - 1);
+                        }
+                        float h0 = v_raw(Vs, VHs, c0, col, -3), h1 = v_raw(Vs, VHs, c0, col, -2),
+                              h2 = v_raw(Vs, VHs, c0, col, -1);
+                        const float4 w = conv_taps(p, l, v_ch);
 #pragma unroll 1
-                    for (int j = j0; j < j0 + kC / 16; ++j) {
-                        float r8[8];
-                        if (8 * j < tc) {
-                            uint32_t a8[8];
-                            tmem_ld8(tmem + kTmAb + lane_off + 8 * j, a8);
+                        for (int j = 0; j < kC / 8; ++j) {
+                            float r8[8];
+                            if (8 * j < tc) {
+                                uint32_t a8[8];
+                                tmem_ld8(tmem + kTmAb + lane_off + 8 * j, a8);
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int t = 8 * j + i;
-                                const float v = conv_step(w, h0, h1, h2, Vs[(min(t, tc - 1) + 3) * kS + col], t < tc);
-                                r8[i] = beta_h[t] * (v - A_h[t] * rk_s[t] * u2f(a8[i]));
+                                for (int i = 0; i < 8; ++i) {
+                                    const int t = 8 * j + i;
+                                    const float v =
+                                        conv_step(w, h0, h1, h2, Vs[(min(t, tc - 1) + 3) * kS + col], t < tc);
+                                    r8[i] = beta_h[t] * (v - A_h[t] * rk_s[t] * u2f(a8[i]));
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) r8[i] = 0.0f;
                             }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) r8[i] = 0.0f;
+                            const uint32_t off = kOffR + sw128_offset(col, j);
+                            store_split8(sm + off, sm + off + kBlk128, r8);
                         }
-                        const uint32_t off = kOffR + sw128_offset(col, j);
-                        store_split8(sm + off, sm + off + kBlk128, r8);
-                    }
-                }
-                if (tid < kC) {
-                    // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
-                    const int i = tid >> 4, j = tid & 15;
-                    float x[16];
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const float* Lr = L_s + (16 * i + r) * kLStride + 16 * i;
-                        float acc = 0.0f;
-#pragma unroll
-                        for (int m = 0; m < r; ++m) acc = fmaf(Lr[m], x[m], acc);
-                        x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
-                }
-                __syncthreads();
-                {
-                    // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj
-                    const int r = tid >> 4, c = tid & 15;
-#pragma unroll
-                    for (int dist = 1; dist < 4; ++dist) {
-                        for (int j = 0; j + dist < 4; ++j) {
-                            const int i = j + dist;
-                            float y = 0.0f;
-                            for (int k = j; k < i; ++k) {
-                                const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
-#pragma unroll
-                                for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
-                            }
-                            Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
-                        }
-                        __syncthreads();
-                        for (int j = 0; j + dist < 4; ++j) {
-                            const int i = j + dist;
-                            float x = 0.0f;
-#pragma unroll
-                            for (int m = 0; m < 16; ++m)
-                                x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
-                            Xs[(16 * i + r) * kC + 16 * j + c] = x;
-                        }
-                        __syncthreads();
-                    }
-                }
-                {
-                    // X as the BF16 operand [t][s]; blocks above the diagonal are zero
-                    const int t = tid >> 2;
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int j = 2 * (tid & 3) + h2;  // columns [8 j, 8 j + 8)
-                        float xv[8];
-                        const bool upper = (j >> 1) > (t >> 4);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
-                        const uint32_t off = kOffXop + sw128_offset(t, j);
-                        store_split8(sm + off, sm + off + 64 * 128, xv);
                     }
                 }
                 fence_proxy_async_smem();
-                __syncthreads();
+                if (__syncthreads_or(group_late ? 1 : 0)) {
+                    failed = true;
+                    break;
+                }
+                // every thread follows the two waits' phases (warps 4-7 took them)
+                if (pend_bar == bar_ab) pend_mma = false;
+                ph_ab ^= 1u;
+                ph_v ^= 1u;
+                pend_v = false;
                 if (tid == 0) {
                     tc_fence_after();
 #pragma unroll
@@ -683,10 +721,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     failed = true;
                     break;
                 }
-                if (warp >= 4) {
-                    // ---- d, then the D^T and E^T rows (E: d scaled by G(s, n-1) and the k norm)
+                {
+                    // ---- d, then the D^T and E^T rows (E: d scaled by G(s, n-1) and the k norm); warps 4-7
+                    //      take tokens [0, 32), warps 0-3 [32, 64)
+                    const int j0 = warp >= 4 ? 0 : kC / 16;
 #pragma unroll 1
-                    for (int j = 0; j < kC / 8; ++j) {
+                    for (int j = j0; j < j0 + kC / 16; ++j) {
                         uint32_t d8[8];
                         tmem_ld8(tmem + kTmD + lane_off + 8 * j, d8);
                         float d[8], ev[8];
@@ -734,9 +774,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                       p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, bar_z);
                     }
                     pend_z = true;
-                }
-
-                if (write_y) {
                     // ---- o_t = A_t S0^T q_t + (D^T P^T)_t into o[t][col] for the y epilogue (warps 4-7:
                     //      tokens [0, 32), warps 0-3: [32, 64))
                     const int j0 = warp >= 4 ? 0 : kC / 16;
@@ -752,7 +789,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         }
                     }
                 }
-                if (last && write_state) {
+                const bool store_state = last && write_state;
+                if (store_state) {
                     // ---- the new state tile, dims [0, 64) into the P and solve-matrix regions, [64, 128)
                     //      into the v staging (both free now), for two 32 KB bulk stores
                     const int kh = warp >> 2;
@@ -768,10 +806,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 }
                 tc_fence_before();
                 __syncthreads();
-                if (last && write_state && tid == 32) {
-                    float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile;
-                    bulk_store(dst, base + kOffP, kTile * 2);
-                    bulk_store(dst + kTile / 2, base + kOffV, kTile * 2);
+                if (tid == 32) {
+                    // one bulk group for the state (possibly empty), committed before the y rows' group
+                    if (store_state) {
+                        float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile;
+                        bulk_store(dst, base + kOffP, kTile * 2);
+                        bulk_store(dst + kTile / 2, base + kOffV, kTile * 2);
+                    }
                     bulk_commit();
                 }
                 if (write_y) {
@@ -795,8 +836,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         bulk_commit();
                     }
                 }
-                // the bulk stores have read shared memory before it is rewritten
-                if (warp == 1) bulk_wait_read();
+                // ---- the next v head's state tile, or the next unit's first tile and q|k rows, requested
+                //      now: their regions are free once this v head's stores have read them
+                if (last) {
+                    if (h + 1 < kGroup) {
+                        issue_s(bl, vh + 1);
+                    } else {
+                        const long long nu = u + gridDim.x;
+                        if (nu < p.n_units) {
+                            const long long nbl = nu / kKHeads;
+                            const int ng = static_cast<int>(nu - nbl * kKHeads);
+                            const int nn = unit_len(p, static_cast<int>(nbl / p.L));
+                            if (nn > 0) {
+                                issue_s(nbl, ng * kGroup);
+                                issue_qk(nbl, ng, 0, min(nn, kC));
+                                s_ahead = qk_ahead = true;
+                            }
+                        }
+                    }
+                }
                 __syncthreads();  // o, z and the operand blocks are rewritten next
             }
             if (!failed && write_state && warp >= 4) {
@@ -817,7 +875,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 
     // MMAs and copies still in flight finish before the tensor memory is freed (bounded).
     if (tid == 0 && failed && pend_mma) (void)mbar_wait_bounded(pend_bar, pend_par);
-    if (tid == 32 && failed) {
+    if (tid == 32) {
+        // (a unit-ahead request that no unit consumed is drained too)
         if (pend_qk) (void)mbar_wait_bounded(bar_qk, ph_qk);
         if (pend_s) (void)mbar_wait_bounded(bar_s, ph_s);
         if (pend_z) (void)mbar_wait_bounded(bar_z, ph_z);
