@@ -29,8 +29,8 @@
 // inverted by 16x16 blocks: diagonal blocks by forward substitution, the blocks
 // below by block products, distance by distance.
 //
-// Work: one CTA (256 threads, 8 warps) per k head of a (sequence, layer), its
-// three v heads one after another; one CTA per SM (about 202 KB of shared memory
+// Work: one CTA (512 threads, 16 warps) per k head of a (sequence, layer), its
+// three v heads one after another; one CTA per SM (about 209 KB of shared memory
 // and all 512 tensor-memory columns), persistent over the units. For a single
 // chunk, the q/k preparation and the Gram matrix serve all three v heads.
 // Longer windows run the chunks of one v head in turn with its state in tensor
@@ -58,7 +58,7 @@ namespace {
 constexpr int kS = kHeadDim;                // 128
 constexpr int kTile = kS * kS;
 constexpr int kC = 64;                      // tokens per chunk
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 512;
 constexpr int kLStride = kC + 4;            // fp32 row stride of the solve matrix (bank spread)
 
 // Shared memory (bytes from a 1024-aligned base). Operand blocks are K-major,
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3;                    // the tensor-memory lanes this warp may access
+    const int wg = warp >> 2;                        // which of the four warps of its lane quarter
     const int col = 32 * quarter + lane;             // v column (tensor-memory lane) of this thread
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const bool write_state = (p.flags & kNoStateWrite) == 0;
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         if (!s_ahead) issue_s(bl, g * kGroup);
         qk_ahead = s_ahead = false;
 
-        // q (threads 0-127) or k (128-255) channel of this thread in the q/k preparation
+        // q (threads 0-127) or k (128-255) channel of this thread for the conv history
         const bool prep_k = tid >= kS;
         const int prep_col = tid & (kS - 1);
         const int prep_ch = (prep_k ? kKOffset : 0) + g * kS + prep_col;
@@ -322,8 +323,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
             const float* dec_h = dec_s + 64 * h;
             const float* A_h = A_s + 64 * h;
             const float* gl_h = gl_s + 64 * h;
-            float v_hist[3] = {0.f, 0.f, 0.f};  // (warps 4-7) the v history after the window
-            const int v_ch = kVOffset + vh * kS + col;  // (warps 4-7) the v channel of this thread's column
+            float v_hist[3] = {0.f, 0.f, 0.f};  // (warps 8-11) the v history after the window
+            const int v_ch = kVOffset + vh * kS + col;  // (warps 8-15) the v channel of this thread's column
 
             for (int c0 = 0; c0 < n && !failed; c0 += kC) {
                 const int tc = min(kC, n - c0);
@@ -365,9 +366,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     pend_qk = false;
                     {
                         // two adjacent channels per thread (q: tid & 64 == 0, k otherwise), tokens
-                        // [32 (tid >> 7), +32); groups past tc are zero rows
+                        // [16 (tid >> 7), +16); groups past tc are zero rows
                         const int pc = (tid & 64 ? kS : 0) + 2 * (tid & 63);  // staged channel of the pair
-                        const int t0 = 32 * (tid >> 7);
+                        const int t0 = 16 * (tid >> 7);
                         const int ch = (pc < kS ? 0 : kKOffset - kS) + g * kS + pc;
                         const float4 w0 = conv_taps(p, l, ch), w1 = conv_taps(p, l, ch + 1);
                         float a0 = qk_raw(Rs, Hs, c0, pc, t0 - 3), a1 = qk_raw(Rs, Hs, c0, pc, t0 - 2),
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         const int cpos = pc & (kS - 1);
                         const int kb = cpos >> 6, cc = (cpos & 63) >> 3, e = cpos & 7;
 #pragma unroll 1
-                        for (int j = 0; j < 4; ++j) {
+                        for (int j = 0; j < 2; ++j) {
                             const bool any = t0 + 8 * j < tc;
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                 *reinterpret_cast<uint32_t*>(sm + off + 2 * kBlk128) = lo;
                             }
                         }
-                        if (last) {
+                        if (last && tid < 2 * kS) {
                             // the history after the window: the last three raw inputs of channel tid
                             const int sc = prep_k ? kS + prep_col : prep_col;
                             qk_hist[0] = qk_raw(Rs, Hs, c0, sc, tc - 3);
@@ -454,25 +455,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 //      a window start the tile arrived by bulk copy in two halves (P and solve-matrix
                 //      regions, v staging); later chunks continue from tensor memory.
                 {
-                    const int kh = warp >> 2;  // dims [64 kh, 64 kh + 64)
-                    float sv[64];
+                    // thread (column col, dims [32 wg, 32 wg + 32))
+                    float sv[32];
                     if (c0 == 0) {
                         if (!wait_all(bar_s, ph_s)) {
                             failed = true;
                             break;
                         }
                         pend_s = false;
-                        const float* half_s = reinterpret_cast<const float*>(sm + (kh ? kOffV : kOffP));
+                        const float* half_s = reinterpret_cast<const float*>(sm + (wg >= 2 ? kOffV : kOffP));
 #pragma unroll
-                        for (int k = 0; k < 64; ++k) sv[k] = half_s[k * kS + col];
+                        for (int k = 0; k < 32; ++k) sv[k] = half_s[(32 * (wg & 1) + k) * kS + col];
                     } else {
                         uint32_t v[32];
-                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh, v);
+                        tmem_ld32(tmem + kTmS + lane_off + 32 * wg, v);
 #pragma unroll
                         for (int k = 0; k < 32; ++k) sv[k] = u2f(v[k]);
-                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh + 32, v);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) sv[32 + k] = u2f(v[k]);
                     }
                     // the y stores of the previous v head have read the region S0^T goes to; the tile's
                     // halves are read before the v rows and the solve matrix replace them
@@ -498,18 +496,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                     pend_v = true;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t off = kOffS + kh * kBlk128 + sw128_offset(col, j);
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t off = kOffS + (wg >> 1) * kBlk128 + sw128_offset(col, 4 * (wg & 1) + j);
                         store_split8(sm + off, sm + off + 2 * kBlk128, sv + 8 * j);
                     }
                     const float al = A_h[tc - 1];
                     uint32_t v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(al * sv[k]);
-                    tmem_st32(tmem + kTmS + lane_off + 64 * kh, v);
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(al * sv[32 + k]);
-                    tmem_st32(tmem + kTmS + lane_off + 64 * kh + 32, v);
+                    tmem_st32(tmem + kTmS + lane_off + 32 * wg, v);
                     tmem_st_wait();
                 }
                 fence_proxy_async_smem();
@@ -530,18 +525,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     pend_par = ph_ab;
                 }
                 // ---- the next unit's inputs into L2, a third per v head: its state tile h and a third
-                //      of its first chunk's rows (warps 4-5)
+                //      of its first chunk's rows (warps 12-13)
                 if (c0 == 0) {
                     const long long nu = u + gridDim.x;
                     if (nu < p.n_units) {
                         const long long nbl = nu / kKHeads;
                         const int ng = static_cast<int>(nu - nbl * kKHeads);
                         const int nn = min(unit_len(p, static_cast<int>(nbl / p.L)), kC);
-                        if (tid == 128 && nn > 0 && h > 0)
+                        if (tid == 384 && nn > 0 && h > 0)
                             prefetch_l2(p.state + (static_cast<size_t>(nbl) * kVHeads + ng * kGroup + h) * kTile,
                                         kTile * 4);
-                        const int t = tid - 160 + h * 22;  // tokens [22 h, 22 h + 22)
-                        if (tid >= 160 && tid < 160 + 22 && t < nn) {
+                        const int t = tid - 416 + h * 22;  // tokens [22 h, 22 h + 22)
+                        if (tid >= 416 && tid < 416 + 22 && t < nn) {
                             const float* row = p.qkv + (static_cast<size_t>(nbl) * p.T + t) * kConvChannels;
                             prefetch_l2(row + kVOffset + ng * kGroup * kS, kGroup * kS * 4);
                             if (write_y)
@@ -551,47 +546,49 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     }
                 }
 
-                // ---- two warp groups at once. Warps 0-3: the solve matrix and P from the Gram rows, then
+                // ---- two warp groups at once. Warps 0-7: the solve matrix and P from the Gram rows, then
                 //      the inverse X of I - Lneg by 16x16 blocks and X as the operand of d = X r.
-                //      Warps 4-7: the v conv and r_t = b_t (v_t - A_t S0^T k_t) into R^T.
+                //      Warps 8-15: the v conv and r_t = b_t (v_t - A_t S0^T k_t) into R^T.
                 bool group_late = false;
-                if (warp < 4) {
+                if (warp < 8) {
                     {
-                        // s from 63 down so that G(s, t) = a_{s+1} ... a_t builds up as one running product
-                        const int t = (32 * warp + lane) & (kC - 1);
-                        const bool is_q = warp >= 2;
+                        // row t of the Gram (k rows: warps 0-1 and 4-5, q rows: warps 2-3 and 6-7), columns
+                        // s in [32 (1 - wg), +32), s from the top so that G(s, t) = a_{s+1} ... a_t builds
+                        // up as one running product
+                        const int t = (32 * quarter + lane) & (kC - 1);
+                        const int half = 1 - wg;
+                        const bool is_q = quarter >= 2;
                         const bool valid_t = t < tc;
                         const float rt = valid_t ? (is_q ? rq_s[t] : -beta_h[t] * rk_s[t]) : 0.0f;
                         float pr = 1.0f;
+                        if (half == 0)
+                            for (int r = 33; r <= t; ++r) pr *= dec_h[r];  // a_33 ... a_t, the factors above s = 31
+                        uint32_t raw[32];
+                        tmem_ld32(tmem + kTmGram + lane_off + 32 * half, raw);
+                        float val[32];
 #pragma unroll
-                        for (int half = 1; half >= 0; --half) {
-                            uint32_t raw[32];
-                            tmem_ld32(tmem + kTmGram + lane_off + 32 * half, raw);
-                            float val[32];
+                        for (int i = 31; i >= 0; --i) {
+                            const int s = 32 * half + i;
+                            if (s < t) pr *= dec_h[s + 1];
+                            // L: s < t (negated, with beta_t); P: s <= t
+                            const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
+                            val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
+                        }
+                        if (!is_q) {
+                            float* Lr = L_s + t * kLStride + 32 * half;
 #pragma unroll
-                            for (int i = 31; i >= 0; --i) {
-                                const int s = 32 * half + i;
-                                if (s < t) pr *= dec_h[s + 1];
-                                // L: s < t (negated, with beta_t); P: s <= t
-                                const float gs = s < t ? pr : ((is_q && s == t) ? 1.0f : 0.0f);
-                                val[i] = rt * gs * u2f(raw[i]) * rk_s[s];
-                            }
-                            if (!is_q) {
-                                float* Lr = L_s + t * kLStride + 32 * half;
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<float4*>(Lr + 4 * j) =
+                                    make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
+                        } else {
 #pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    *reinterpret_cast<float4*>(Lr + 4 * j) =
-                                        make_float4(val[4 * j], val[4 * j + 1], val[4 * j + 2], val[4 * j + 3]);
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    const uint32_t off = kOffP + sw128_offset(t, 4 * half + j);
-                                    store_split8(sm + off, sm + off + 64 * 128, val + 8 * j);
-                                }
+                            for (int j = 0; j < 4; ++j) {
+                                const uint32_t off = kOffP + sw128_offset(t, 4 * half + j);
+                                store_split8(sm + off, sm + off + 64 * 128, val + 8 * j);
                             }
                         }
                     }
-                    named_barrier(1, 128);
+                    named_barrier(1, 256);
                     if (tid < kC) {
                         // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
                         const int i = tid >> 4, j = tid & 15;
@@ -607,49 +604,41 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 #pragma unroll
                         for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
                     }
-                    named_barrier(1, 128);
+                    named_barrier(1, 256);
                     {
                         // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj; thread
-                        // (r, c pair) of each 16x16 block
-                        const int r = tid >> 3, c = 2 * (tid & 7);
+                        // (r, c) of each 16x16 block
+                        const int r = tid >> 4, c = tid & 15;
 #pragma unroll
                         for (int dist = 1; dist < 4; ++dist) {
                             for (int j = 0; j + dist < 4; ++j) {
                                 const int i = j + dist;
-                                float y0 = 0.0f, y1 = 0.0f;
+                                float y = 0.0f;
                                 for (int k = j; k < i; ++k) {
                                     const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
 #pragma unroll
-                                    for (int m = 0; m < 16; ++m) {
-                                        const float2 xv = *reinterpret_cast<const float2*>(Xs + (16 * k + m) * kC + 16 * j + c);
-                                        y0 = fmaf(Lr[m], xv.x, y0);
-                                        y1 = fmaf(Lr[m], xv.y, y1);
-                                    }
+                                    for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
                                 }
-                                *reinterpret_cast<float2*>(Xs + (16 * j + r) * kC + 16 * i + c) = make_float2(y0, y1);
+                                Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
                             }
-                            named_barrier(1, 128);
+                            named_barrier(1, 256);
                             for (int j = 0; j + dist < 4; ++j) {
                                 const int i = j + dist;
-                                float x0 = 0.0f, x1 = 0.0f;
+                                float x = 0.0f;
 #pragma unroll
-                                for (int m = 0; m < 16; ++m) {
-                                    const float xm = Xs[(16 * i + r) * kC + 16 * i + m];
-                                    const float2 yv = *reinterpret_cast<const float2*>(Xs + (16 * j + m) * kC + 16 * i + c);
-                                    x0 = fmaf(xm, yv.x, x0);
-                                    x1 = fmaf(xm, yv.y, x1);
-                                }
-                                *reinterpret_cast<float2*>(Xs + (16 * i + r) * kC + 16 * j + c) = make_float2(x0, x1);
+                                for (int m = 0; m < 16; ++m)
+                                    x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
+                                Xs[(16 * i + r) * kC + 16 * j + c] = x;
                             }
-                            named_barrier(1, 128);
+                            named_barrier(1, 256);
                         }
                     }
                     {
                         // X as the BF16 operand [t][s]; blocks above the diagonal are zero
-                        const int t = tid >> 1;
+                        const int t = tid >> 2;
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int j = 4 * (tid & 1) + q4;  // columns [8 j, 8 j + 8)
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const int j = 2 * (tid & 3) + h2;  // columns [8 j, 8 j + 8)
                             float xv[8];
                             const bool upper = (j >> 1) > (t >> 4);
 #pragma unroll
@@ -659,23 +648,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         }
                     }
                 } else {
-                    // warps 4-7: the state MMA and the v rows, then r
+                    // warps 8-15: the state MMA and the v rows, then r; warps 8-11 tokens [0, 32), 12-15 [32, 64)
                     bool late = !mbar_wait_bounded(bar_ab, ph_ab);
                     late = late || !mbar_wait_bounded(bar_v, ph_v);
-                    group_late = named_barrier_or(2, 128, late);
+                    group_late = named_barrier_or(2, 256, late);
                     if (!group_late) {
                         tc_fence_after();
-                        if (last) {
+                        if (last && wg == 2) {
                             // the v history after the window: the last three raw inputs (the staging is reused later)
                             v_hist[0] = v_raw(Vs, VHs, c0, col, tc - 3);
                             v_hist[1] = v_raw(Vs, VHs, c0, col, tc - 2);
                             v_hist[2] = v_raw(Vs, VHs, c0, col, tc - 1);
                         }
-                        float h0 = v_raw(Vs, VHs, c0, col, -3), h1 = v_raw(Vs, VHs, c0, col, -2),
-                              h2 = v_raw(Vs, VHs, c0, col, -1);
+                        const int j0 = wg == 2 ? 0 : kC / 16;
+                        float h0 = v_raw(Vs, VHs, c0, col, 8 * j0 - 3), h1 = v_raw(Vs, VHs, c0, col, 8 * j0 - 2),
+                              h2 = v_raw(Vs, VHs, c0, col, 8 * j0 - 1);
                         const float4 w = conv_taps(p, l, v_ch);
 #pragma unroll 1
-                        for (int j = 0; j < kC / 8; ++j) {
+                        for (int j = j0; j < j0 + kC / 16; ++j) {
                             float r8[8];
                             if (8 * j < tc) {
                                 uint32_t a8[8];
@@ -701,7 +691,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     failed = true;
                     break;
                 }
-                // every thread follows the two waits' phases (warps 4-7 took them)
+                // every thread follows the two waits' phases (warps 8-15 took them)
                 if (pend_bar == bar_ab) pend_mma = false;
                 ph_ab ^= 1u;
                 ph_v ^= 1u;
@@ -722,11 +712,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     break;
                 }
                 {
-                    // ---- d, then the D^T and E^T rows (E: d scaled by G(s, n-1) and the k norm); warps 4-7
-                    //      take tokens [0, 32), warps 0-3 [32, 64)
-                    const int j0 = warp >= 4 ? 0 : kC / 16;
+                    // ---- d, then the D^T and E^T rows (E: d scaled by G(s, n-1) and the k norm); the four
+                    //      warps of a lane quarter take 16 tokens each
+                    const int j0 = 2 * wg;
 #pragma unroll 1
-                    for (int j = j0; j < j0 + kC / 16; ++j) {
+                    for (int j = j0; j < j0 + 2; ++j) {
                         uint32_t d8[8];
                         tmem_ld8(tmem + kTmD + lane_off + 8 * j, d8);
                         float d[8], ev[8];
@@ -774,11 +764,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                       p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, bar_z);
                     }
                     pend_z = true;
-                    // ---- o_t = A_t S0^T q_t + (D^T P^T)_t into o[t][col] for the y epilogue (warps 4-7:
-                    //      tokens [0, 32), warps 0-3: [32, 64))
-                    const int j0 = warp >= 4 ? 0 : kC / 16;
+                    // ---- o_t = A_t S0^T q_t + (D^T P^T)_t into o[t][col] for the y epilogue (16 tokens per
+                    //      warp of a lane quarter)
+                    const int j0 = 2 * wg;
 #pragma unroll 1
-                    for (int j = j0; j < j0 + kC / 16 && 8 * j < tc; ++j) {
+                    for (int j = j0; j < j0 + 2 && 8 * j < tc; ++j) {
                         uint32_t bq[8], pd[8];
                         tmem_ld8(tmem + kTmAb + lane_off + kC + 8 * j, bq);
                         tmem_ld8(tmem + kTmPd + lane_off + 8 * j, pd);
@@ -792,16 +782,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 const bool store_state = last && write_state;
                 if (store_state) {
                     // ---- the new state tile, dims [0, 64) into the P and solve-matrix regions, [64, 128)
-                    //      into the v staging (both free now), for two 32 KB bulk stores
-                    const int kh = warp >> 2;
-                    float* half_s = reinterpret_cast<float*>(sm + (kh ? kOffV : kOffP));
+                    //      into the v staging (both free now), for two 32 KB bulk stores; thread (column,
+                    //      dims [32 wg, +32))
+                    float* half_s = reinterpret_cast<float*>(sm + (wg >= 2 ? kOffV : kOffP));
+                    uint32_t v[32];
+                    tmem_ld32(tmem + kTmS + lane_off + 32 * wg, v);
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + kTmS + lane_off + 64 * kh + 32 * q, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) half_s[(32 * q + i) * kS + col] = u2f(v[i]);
-                    }
+                    for (int i = 0; i < 32; ++i) half_s[(32 * (wg & 1) + i) * kS + col] = u2f(v[i]);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before();
@@ -857,7 +844,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 }
                 __syncthreads();  // o, z and the operand blocks are rewritten next
             }
-            if (!failed && write_state && warp >= 4) {
+            if (!failed && write_state && warp >= 8 && wg == 2) {
                 float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + v_ch) * (kDConv - 1);
                 cs[0] = v_hist[0];
                 cs[1] = v_hist[1];
@@ -865,7 +852,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
             }
         }
         // The q/k history last: every v head's pass has read the old one.
-        if (!failed && write_state) {
+        if (!failed && write_state && tid < 2 * kS) {
             float* cs = p.conv_state + (static_cast<size_t>(bl) * kConvChannels + prep_ch) * (kDConv - 1);
             cs[0] = qk_hist[0];
             cs[1] = qk_hist[1];
