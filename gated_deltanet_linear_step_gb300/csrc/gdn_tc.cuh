@@ -239,3 +239,15 @@ __device__ __forceinline__ void bulk_wait_read_one() {
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// A 2-D tensor-map store of one box from shared memory, tracked by this thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+}  // namespace gdn

@@ -47,6 +47,7 @@
 // writes nothing more, waits (bounded) for the MMAs and copies it issued, frees
 // its tensor memory, sets the device error word and returns.
 
+#include <cstring>
 #include <mutex>
 
 #include "gdn_launch.h"
@@ -66,9 +67,8 @@ constexpr int kLStride = kC + 4;            // fp32 row stride of the solve matr
 constexpr uint32_t kBlk128 = 128 * 128;     // one 64-wide K block of 128 rows
 constexpr uint32_t kOffKQ = 0;              // [K;Q] rows (k tokens 0-63, q tokens 64-127) x 128 dims: hi, lo
 constexpr uint32_t kOffS = kOffKQ + 4 * kBlk128;    // S0^T: 128 columns x 128 dims: hi, lo
-// Before S0^T the region stages by bulk copy the chunk's raw q|k rows (1 KB per
-// token), then the state tile (fp32, 64 KB), which the threads read into
-// registers before writing its split over it. After the state MMA:
+// Before S0^T the region stages the chunk's raw q rows ([64][128] fp32) and k rows
+// (the same, 32 KB further), copied 8 tokens per tensor-map box. After the state MMA:
 constexpr uint32_t kOffR = kOffS;                   //   R^T, 128 x 64: hi, lo
 constexpr uint32_t kOffX = kOffS + 2 * kBlk128;     //   the inverse X, fp32 [64][64]
 constexpr uint32_t kOffXop = kOffX + 64 * 64 * 4;   //   X as the BF16 operand, 64 x 64: hi, lo
@@ -101,7 +101,12 @@ constexpr uint32_t kTmGram = 0, kTmAb = 128, kTmS = 256, kTmPd = 384, kTmD = 448
 
 __device__ unsigned int g_wtc_error = 0;
 
+constexpr int kBoxRows = 8;  // token rows per tensor-map box (4 KB of one 128-wide head)
+
 struct TcParams {
+    CUtensorMap tm_qkv;  // qkv as [B L T rows][10240] fp32, box {128, 8}
+    CUtensorMap tm_z;    // z as [B L T rows][6144], box {128, 8} (unused without y)
+    CUtensorMap tm_y;    // y, the same geometry (unused without y)
     const float* qkv;
     const float* z;
     const float* alpha;
@@ -145,10 +150,12 @@ __device__ __forceinline__ float conv_step(float4 w, float& h0, float& h1, float
 }
 
 // Raw q/k input of staged channel c (q at [0, 128), k at [128, 256)) at token c0 + t (t in
-// [-3, tc)): token t >= 0 is staged row t; before it, the staged history, which at the window
-// start is conv_state ([channel][3]) and otherwise the three qkv rows before c0.
+// [-3, tc)): token t >= 0 is row t of the staged q or k rows; before it, the staged history,
+// which at the window start is conv_state ([channel][3]) and otherwise the three qkv rows
+// before c0 (q and k halves of 1 KB rows).
 __device__ __forceinline__ float qk_raw(const float* Rs, const float* Hs, int c0, int c, int t) {
-    return t >= 0 ? Rs[t * 2 * kS + c] : (c0 == 0 ? Hs[3 * c + 3 + t] : Hs[(t + 3) * 2 * kS + c]);
+    return t >= 0 ? Rs[(c >> 7) * kC * kS + t * kS + (c & (kS - 1))]
+                  : (c0 == 0 ? Hs[3 * c + 3 + t] : Hs[(t + 3) * 2 * kS + c]);
 }
 
 // Raw v input of column col at token c0 + t (t in [-3, tc)) from the staged rows: token t is
@@ -207,7 +214,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     const bool silu_gate = (p.flags & kSiluGate) != 0;
     const bool gates_ready = (p.flags & kGatesReady) != 0;
 
+    const uint64_t pol_stream = evict_first_policy();  // rows read once per call
     if (tid == 0) {
+        prefetch_tensormap(&p.tm_qkv);
+        if (write_y) {
+            prefetch_tensormap(&p.tm_z);
+            prefetch_tensormap(&p.tm_y);
+        }
         mbar_init(bar_gram, 1);
         mbar_init(bar_ab, 1);
         mbar_init(bar_out, 1);
@@ -242,17 +255,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         tc_fence_after();
         return true;
     };
-    // The chunk's q|k rows (1 KB per token) into the region S0^T later holds, the history before
-    // them beside it; by warp 1, after its bulk stores have read that region.
+    // The chunk's q and k rows (8 tokens per tensor-map box) into the region S0^T later holds, the
+    // history before them beside it; by warp 1, after its bulk stores have read that region.
     auto issue_qk = [&](long long xbl, int xg, int xc0, int xtc) {
         if (warp == 1) {
             bulk_wait_read();
-            if (lane == 0) mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>(xtc) * 1024u + 3072u);
+            const int nb = (xtc + kBoxRows - 1) / kBoxRows;
+            if (lane == 0) mbar_arrive_expect_tx(bar_qk, static_cast<uint32_t>(nb) * 2u * kBoxRows * kS * 4 + 3072u);
             __syncwarp();
-            for (int t = lane; t < xtc; t += 32) {
-                const float* row = p.qkv + (static_cast<size_t>(xbl) * p.T + xc0 + t) * kConvChannels;
-                bulk_load(base + kOffS + t * 1024, row + xg * kS, kS * 4, bar_qk);
-                bulk_load(base + kOffS + t * 1024 + 512, row + kKOffset + xg * kS, kS * 4, bar_qk);
+            const int row0 = static_cast<int>(xbl * p.T + xc0);
+            if (lane < 2 * nb) {
+                const int j = lane >> 1, kseg = lane & 1;
+                tma_load_2d(base + kOffS + kseg * kC * kS * 4 + j * kBoxRows * kS * 4, &p.tm_qkv,
+                            (kseg ? kKOffset : 0) + xg * kS, row0 + kBoxRows * j, bar_qk, pol_stream);
             }
             if (lane == 0) {
                 if (xc0 == 0) {
@@ -385,7 +400,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                 const int t = t0 + 8 * j + i;
                                 float x0 = 0.0f, x1 = 0.0f;
                                 if (any) {
-                                    const float2 xv = *reinterpret_cast<const float2*>(Rs + min(t, tc - 1) * 2 * kS + pc);
+                                    const float2 xv = *reinterpret_cast<const float2*>(
+                                        Rs + (pc >> 7) * kC * kS + min(t, tc - 1) * kS + (pc & (kS - 1)));
                                     x0 = conv_step(w0, a0, a1, a2, xv.x, t < tc);
                                     x1 = conv_step(w1, b0, b1, b2, xv.y, t < tc);
                                 }
@@ -478,12 +494,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     __syncthreads();
                     // ---- v rows of this v head (and, at the window start, its conv history) by bulk copy
                     if (warp == 2) {
+                        const int nb = (tc + kBoxRows - 1) / kBoxRows;
                         if (lane == 0)
-                            mbar_arrive_expect_tx(bar_v,
-                                                  static_cast<uint32_t>(tc + nh) * kS * 4 + (c0 == 0 ? kS * 12 : 0));
+                            mbar_arrive_expect_tx(bar_v, static_cast<uint32_t>(nb) * kBoxRows * kS * 4 +
+                                                             static_cast<uint32_t>(nh) * kS * 4 + (c0 == 0 ? kS * 12 : 0));
                         __syncwarp();
-                        for (int i = lane; i < tc + nh; i += 32) {
-                            const int t = i - nh;
+                        const int row0 = static_cast<int>(bl * p.T + c0);
+                        if (lane < nb)
+                            tma_load_2d(base + kOffV + (3 + kBoxRows * lane) * kS * 4, &p.tm_qkv, kVOffset + vh * kS,
+                                        row0 + kBoxRows * lane, bar_v, pol_stream);
+                        if (lane >= 29 && nh > 0) {  // the three rows before the chunk, one copy each
+                            const int t = lane - 32;
                             bulk_load(base + kOffV + (t + 3) * kS * 4,
                                       p.qkv + (static_cast<size_t>(bl) * p.T + c0 + t) * kConvChannels + kVOffset +
                                           vh * kS,
@@ -757,11 +778,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                 if (write_y) {
                     // z rows of the chunk into the half of the region that E^T held
                     if (warp == 1) {
-                        if (lane == 0) mbar_arrive_expect_tx(bar_z, static_cast<uint32_t>(tc) * kS * 4);
+                        const int nb = (tc + kBoxRows - 1) / kBoxRows;
+                        if (lane == 0) mbar_arrive_expect_tx(bar_z, static_cast<uint32_t>(nb) * kBoxRows * kS * 4);
                         __syncwarp();
-                        for (int t = lane; t < tc; t += 32)
-                            bulk_load(base + kOffZ + t * kS * 4,
-                                      p.z + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS, kS * 4, bar_z);
+                        if (lane < nb)
+                            tma_load_2d(base + kOffZ + lane * kBoxRows * kS * 4, &p.tm_z, vh * kS,
+                                        static_cast<int>(bl * p.T + c0) + kBoxRows * lane, bar_z, pol_stream);
                     }
                     pend_z = true;
                     // ---- o_t = A_t S0^T q_t + (D^T P^T)_t into o[t][col] for the y epilogue (16 tokens per
@@ -817,7 +839,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     fence_proxy_async_smem();
                     __syncthreads();
                     if (warp == 1) {
-                        for (int t = lane; t < tc; t += 32)
+                        // full 8-token boxes by tensor map, the rows of a last partial box one by one
+                        const int full = tc / kBoxRows;
+                        if (lane < full)
+                            tma_store_2d(&p.tm_y, vh * kS, static_cast<int>(bl * p.T + c0) + kBoxRows * lane,
+                                         base + kOffO + lane * kBoxRows * kS * 4);
+                        const int t = kBoxRows * full + lane;
+                        if (lane < tc - kBoxRows * full)
                             bulk_store(p.y + (static_cast<size_t>(bl) * p.T + c0 + t) * kValueDim + vh * kS,
                                        base + kOffO + t * kS * 4, kS * 4);
                         bulk_commit();
@@ -882,6 +910,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
 std::mutex g_mutex;
 int g_sms[64] = {};
 
+// A [rows][cols] fp32 tensor map with boxes of 128 columns x 8 rows, no swizzle.
+cudaError_t encode_rows(CUtensorMap* tm, const float* base, int cols, cuuint64_t rows) {
+    if (tensor_map_encoder() == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kS), static_cast<cuuint32_t>(kBoxRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = tensor_map_encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_decode_window_tc(const StepArgs& a, cudaStream_t stream) {
@@ -904,6 +946,16 @@ cudaError_t launch_decode_window_tc(const StepArgs& a, cudaStream_t stream) {
         sms = g_sms[dev];
     }
     TcParams p;
+    memset(&p, 0, sizeof(p));
+    const cuuint64_t rows = static_cast<cuuint64_t>(a.B) * a.L * a.T;
+    e = encode_rows(&p.tm_qkv, a.qkv, kConvChannels, rows);
+    if (e != cudaSuccess) return e;
+    if ((a.flags & kNoY) == 0) {
+        e = encode_rows(&p.tm_z, a.z, kValueDim, rows);
+        if (e != cudaSuccess) return e;
+        e = encode_rows(&p.tm_y, a.y, kValueDim, rows);
+        if (e != cudaSuccess) return e;
+    }
     p.qkv = a.qkv;
     p.z = a.z;
     p.alpha = a.alpha;
