@@ -51,8 +51,10 @@
 
 #include <mutex>
 
-#include "gdn_device.cuh"
+#include <cstring>
+
 #include "gdn_launch.h"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -64,22 +66,21 @@ constexpr int kUnitCh = 2 * kS + kGroup * kS;  // 640 conv channels per unit
 constexpr int kC = 8;                           // tokens per chunk
 constexpr int kXStride = 20;                    // floats per row of X: 16 used, rows 80 B apart (no bank conflicts)
 
-// Per-chunk scalars (floats).
-constexpr int kMPart = 0;                      // [8][kC] sums of squares per warp (q: warps 0-3, k: 4-7)
+// Per-chunk scalars (floats). The gate inputs of the unit's three heads come first (tensor-map
+// boxes land 128-byte aligned): for alpha and beta of each token, and for the layer's dt and
+// ssm_a, the 16-byte-aligned run of 8 floats that starts at float gate_base(g) of the 48-wide row.
+constexpr int kMGin = 0;                       // [2 (alpha, beta)][kC][8], then [2 (dt, ssm_a)][8]
+constexpr int kMPart = kMGin + 2 * kC * 8 + 2 * 8;  // [8][kC] sums of squares per warp (q: warps 0-3, k: 4-7)
 constexpr int kMGram = kMPart + 8 * kC;        // [4][64] Gram partial sums of the four k warps
 constexpr int kMCoef = kMGram + 4 * 64;        // [3][64] G(s,t) k_s.k_t at 8s+t (s<t), G(t,s) k_t.q_s at 8s+t (t<=s)
 constexpr int kMBeta = kMCoef + kGroup * 64;   // [3][kC]
 constexpr int kMCum = kMBeta + kGroup * kC;    // [3][kC] A_t
 constexpr int kMGam = kMCum + kGroup * kC;     // [3][kC][kC] G(s, t) at [h][s][t]
 constexpr int kMRms = kMGam + kGroup * kC * kC;  // [3][4][kC] sums of o^2 per (head, warp, token)
-// The gate inputs of the unit's three heads, by bulk copy with the qkv rows: for alpha and beta
-// of each token, and for the layer's dt and ssm_a, the 16-byte-aligned run of 8 floats (at most
-// 32 bytes are copied) that starts at float gate_base(g) of the 48-wide row.
-constexpr int kMGin = kMRms + kGroup * 4 * kC;  // [2 (alpha, beta)][kC][8], then [2 (dt, ssm_a)][8]
-constexpr int kMFloats = kMGin + 2 * kC * 8 + 2 * 8;
+constexpr int kMFloats = kMRms + kGroup * 4 * kC;
 
 constexpr size_t kOffTiles = 0;
-constexpr size_t kOffRaw = size_t(kGroup) * kTileBytes;              // 196608: qkv rows [kC][640]
+constexpr size_t kOffRaw = size_t(kGroup) * kTileBytes;              // 196608: qkv rows [5 segments][kC][128]
 constexpr size_t kOffX = kOffRaw + size_t(kC) * kUnitCh * 4;         // 217088: X [128][kXStride]
 constexpr size_t kOffMisc = kOffX + size_t(kS) * kXStride * 4;       // 227328
 constexpr size_t kOffBars = kOffMisc + size_t(kMFloats) * 4;         // 231296
@@ -88,7 +89,7 @@ constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;               // 231328
 
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeds 227 KB");
 static_assert(kOffBars % 8 == 0 && kOffRaw % 16 == 0 && kOffX % 16 == 0 && (kXStride * 4) % 16 == 0, "alignment");
-static_assert((kMGin * 4) % 16 == 0, "the gate inputs take bulk copies");
+static_assert(kOffMisc % 128 == 0 && kOffRaw % 128 == 0, "tensor-map boxes land 128-byte aligned");
 static_assert(kThreads == 384 && kC == 8, "thread roles assume 384 threads and 8-token chunks");
 
 constexpr int kGateWarp = 11;  // loads alpha and beta and builds the decay tables
@@ -96,6 +97,9 @@ constexpr int kGateWarp = 11;  // loads alpha and beta and builds the decay tabl
 __device__ unsigned int g_chunk_error = 0;
 
 struct Params {
+    CUtensorMap tm_qkv;    // qkv as [B L T rows][10240] fp32, box {128, 8}
+    CUtensorMap tm_alpha;  // alpha as [B L T rows][48], box {8, 8}
+    CUtensorMap tm_beta;   // beta, the same
     const float* qkv;
     const float* z;
     const float* alpha;
@@ -143,36 +147,29 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes
 __device__ __forceinline__ int gate_base(int g) { return (kGroup * g) & ~3; }
 __device__ __forceinline__ uint32_t gate_bytes(int g) { return (kGroup * g - gate_base(g)) + kGroup <= 4 ? 16u : 32u; }
 
-// The bulk copies of one chunk's inputs (tokens c0 .. c0 + rows - 1 of unit x):
-// three per token for its q, k and v segments of qkv, one per token for the
-// heads' alpha and for their beta, and one each for the layer's dt and ssm_a.
-// Issued by the lanes of the calling warp (two rounds); lane 0 arms the
-// mbarrier with the byte count first (zero rows: the phase holds dt and ssm_a).
+// The copies of one chunk's inputs (tokens c0 .. c0 + rows - 1 of unit x), 8 token rows per
+// tensor-map box: the q and k segments and the three v heads of qkv (a box of 128 columns each,
+// into the segment-major rows [5][8][128]), the heads' alpha and beta (a box of 8 columns each),
+// and bulk copies of the layer's dt and ssm_a. Issued by the lanes of the calling warp; lane 0
+// arms the mbarrier with the byte count first (zero rows: the phase holds dt and ssm_a). Rows
+// past the chunk's tokens are read too (other tokens, or zeros past the tensor) and never used.
 __device__ __forceinline__ void issue_chunk(const Params& p, const Unit& x, int c0, int rows, uint32_t raw,
                                             uint32_t gin, uint32_t bar, int lane) {
     const int gb = gate_base(x.g);
     const uint32_t gbytes = gate_bytes(x.g);
-    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * (kUnitCh * 4 + 2 * gbytes) + 2 * gbytes);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (rows > 0 ? 5u * kC * kS * 4 + 2u * kC * 8 * 4 : 0u) + 2 * gbytes);
     __syncwarp();
-    const int n_copies = 5 * rows + 2;
-    for (int j = lane; j < n_copies; j += 32) {
-        if (j < 3 * rows) {
-            const int t = j / 3, part = j - 3 * (j / 3);
-            const float* xr = p.qkv + (static_cast<size_t>(x.bl) * p.T + c0 + t) * kConvChannels;
-            const uint32_t row = raw + t * kUnitCh * 4;
-            if (part == 0) bulk_load(row, xr + x.g * kS, kS * 4, bar);
-            if (part == 1) bulk_load(row + kS * 4, xr + kKOffset + x.g * kS, kS * 4, bar);
-            if (part == 2) bulk_load(row + 2 * kS * 4, xr + kVOffset + x.g * kGroup * kS, kGroup * kS * 4, bar);
-        } else if (j < 5 * rows) {
-            const int k = j - 3 * rows;  // alpha of token k / 2 (even k) or its beta (odd k)
-            const int t = k >> 1, which = k & 1;
-            const float* src = (which ? p.beta : p.alpha) + (static_cast<size_t>(x.bl) * p.T + c0 + t) * kVHeads + gb;
-            bulk_load(gin + ((which * kC + t) * 8) * 4, src, gbytes, bar);
-        } else {
-            const int which = j - 5 * rows;  // dt, then ssm_a
-            const float* src = (which ? p.ssm_a : p.dt) + static_cast<size_t>(x.l) * kVHeads + gb;
-            bulk_load(gin + (2 * kC * 8 + which * 8) * 4, src, gbytes, bar);
-        }
+    const int row0 = static_cast<int>(x.bl * p.T + c0);
+    const uint64_t pol = evict_first_policy();
+    if (rows > 0 && lane < 5) {
+        const int col = lane == 0 ? x.g * kS : (lane == 1 ? kKOffset + x.g * kS : kVOffset + (x.g * kGroup + lane - 2) * kS);
+        tma_load_2d(raw + lane * kC * kS * 4, &p.tm_qkv, col, row0, bar, pol);
+    }
+    if (rows > 0 && (lane == 5 || lane == 6))
+        tma_load_2d(gin + (lane - 5) * kC * 8 * 4, lane == 5 ? &p.tm_alpha : &p.tm_beta, gb, row0, bar, pol);
+    if (lane == 7 || lane == 8) {
+        const float* src = (lane == 8 ? p.ssm_a : p.dt) + static_cast<size_t>(x.l) * kVHeads + gb;
+        bulk_load(gin + (2 * kC * 8 + (lane - 7) * 8) * 4, src, gbytes, bar);
     }
 }
 
@@ -193,7 +190,8 @@ __device__ __forceinline__ void roll_history(const float* rows, int cc, int tc, 
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
         const int tau = tc - 3 + k;  // token of history entry k; < 0 reaches into the old history
-        h[k] = tau >= 0 ? rows[max(tau, 0) * kUnitCh + cc] : (tau == -3 ? i0 : (tau == -2 ? i1 : i2));
+        h[k] = tau >= 0 ? rows[(cc >> 7) * kC * kS + max(tau, 0) * kS + (cc & (kS - 1))]
+                        : (tau == -3 ? i0 : (tau == -2 ? i1 : i2));
     }
 }
 
@@ -207,7 +205,7 @@ __device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, 
     float h0 = h[0], h1 = h[1], h2 = h[2];
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
-        const float xt = rows[max(min(t, tc - 1), 0) * kUnitCh + cc];
+        const float xt = rows[(cc >> 7) * kC * kS + max(min(t, tc - 1), 0) * kS + (cc & (kS - 1))];
         const float xc = conv4(w, h0, h1, h2, xt);
         h0 = h1;
         h1 = h2;
@@ -758,6 +756,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
 std::mutex g_mutex;
 int g_sms[64] = {0};
 
+// A [rows][cols] fp32 tensor map with boxes of box_cols columns x kC rows, no swizzle.
+cudaError_t encode_rows(CUtensorMap* tm, const float* base, int cols, cuuint64_t rows, int box_cols) {
+    if (tensor_map_encoder() == nullptr) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), rows};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(kC)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = tensor_map_encoder()(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
+                                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_decode_chunked(const StepArgs& a, cudaStream_t stream) {
@@ -780,6 +792,14 @@ cudaError_t launch_decode_chunked(const StepArgs& a, cudaStream_t stream) {
         sms = g_sms[dev];
     }
     Params p;
+    memset(&p, 0, sizeof(p));
+    const cuuint64_t rows = static_cast<cuuint64_t>(a.B) * a.L * a.T;
+    e = encode_rows(&p.tm_qkv, a.qkv, kConvChannels, rows, kS);
+    if (e != cudaSuccess) return e;
+    e = encode_rows(&p.tm_alpha, a.alpha, kVHeads, rows, 8);
+    if (e != cudaSuccess) return e;
+    e = encode_rows(&p.tm_beta, a.beta, kVHeads, rows, 8);
+    if (e != cudaSuccess) return e;
     p.qkv = a.qkv;
     p.z = a.z;
     p.alpha = a.alpha;
