@@ -169,9 +169,9 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# Windows of 2-8 tokens run the kernel with the tiles in shared memory, 9-23 the register
-# window kernel, 24 or more the tensor-core chunk kernel (the library's dispatch).
-CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 8, 24, 64
+# Windows of 2-8 tokens run the kernel with the tiles in shared memory, 9-19 the register
+# window kernel, 20 or more the tensor-core chunk kernel (the library's dispatch).
+CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 8, 20, 64
 
 
 def kernel_sources(T: int) -> list:

@@ -608,7 +608,7 @@ cudaError_t device_setup(int* clusters) {
 #define GDN_CHUNK_MAX_T 8
 #endif
 #ifndef GDN_TC_MIN_T
-#define GDN_TC_MIN_T 24
+#define GDN_TC_MIN_T 20
 #endif
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
