@@ -117,11 +117,6 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
     const int n_ks = p.E / kBK;
     const int ks0 = n_ks * rank / kSplit;
     const int steps = n_ks * (rank + 1) / kSplit - ks0;
-    // The layer's dt and ssm_a for the epilogue: loaded now, kept in shared memory after the main loop.
-    float lw_val = 0.0f;
-    if (tid < 2 * kVHeads)
-        lw_val = __ldg((tid < kVHeads ? p.dt : p.ssm_a) + static_cast<size_t>(l) * kVHeads + tid % kVHeads);
-
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(rawf_bar(s), 1);
@@ -141,6 +136,15 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     bool have_acc = false;  // (warps 0-3) the accumulator holds this CTA's sums
+    // Launched with programmatic stream serialization, the next kernel in the stream may start its
+    // CTAs (and their set-up above) while this one finishes; every read of global memory below
+    // waits until the kernels before this one have completed and their writes are visible.
+    griddep_launch_dependents();
+    griddep_wait();
+    // The layer's dt and ssm_a for the epilogue: loaded now, kept in shared memory after the main loop.
+    float lw_val = 0.0f;
+    if (tid < 2 * kVHeads)
+        lw_val = __ldg((tid < kVHeads ? p.dt : p.ssm_a) + static_cast<size_t>(l) * kVHeads + tid % kVHeads);
 
     if (warp == 4) {
         if (lane == 0) {
@@ -364,13 +368,15 @@ cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream) {
     cfg.blockDim = dim3(kAbThreads, 1, 1);
     cfg.dynamicSmemBytes = kAbSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kSplit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, gdn_ab_gates_kernel, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

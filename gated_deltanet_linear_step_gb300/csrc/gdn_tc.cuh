@@ -251,3 +251,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int x, int y
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// Programmatic dependent launch: lets the next kernel in the stream begin launching (a no-op
+// unless it was launched with programmatic stream serialization) ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ... and waits until the kernels this one depends on have completed and their memory
+// operations are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+}  // namespace gdn
