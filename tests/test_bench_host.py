@@ -7,6 +7,8 @@ import os
 import subprocess
 import sys
 
+import numpy as np
+
 import bench
 import workloads as W
 
@@ -65,3 +67,35 @@ def test_clock_summary_keeps_the_timed_region():
     assert "note" not in s
     c.samples = [(9.9, 1500.0, 2070.0, 300.0, [])]
     assert "note" in c.summary()
+
+
+def test_kernel_sources_follow_the_library_dispatch():
+    """Each window length maps to the source of the kernel the library runs for it (the traffic
+    records are keyed to those sources)."""
+    import bench
+
+    names = lambda T: [os.path.basename(p) for p in bench.kernel_sources(T)]
+    assert names(1)[0] == "gdn_decode_t1.cu"
+    assert names(2)[0] == names(bench.CHUNK_MAX_T)[0] == "gdn_chunk.cu"
+    assert names(bench.CHUNK_MAX_T + 1)[0] == names(bench.TC_MIN_T - 1)[0] == "gdn_step.cu"
+    assert names(bench.TC_MIN_T)[0] == names(1024)[0] == "gdn_window_tc.cu"
+    # the thresholds are the library's defaults
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
+    assert f"#define GDN_CHUNK_MAX_T {bench.CHUNK_MAX_T}" in src
+    assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
+
+
+def test_tensor_core_flop_count():
+    """Per 64-token chunk: a Gram product per k head (three per v head past one chunk) and four
+    products per v head, each as three BF16 MMAs; sequences with no valid token cost nothing."""
+    import bench
+    import workloads as W
+
+    gram = 3 * 2 * 128 ** 3
+    per_v = 3 * 2 * (128 ** 3 + 2 * 128 * 64 * 64 + 128 * 128 * 64)
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=3, L=2, T=130)
+    lens = np.array([0, 64, 130], np.int32)
+    expect = (1 * (gram + 3 * per_v) + 3 * (3 * gram + 3 * per_v)) * 2 * 16
+    assert bench.tc_mma_flops(w, lens) == expect
+    assert bench.tc_mma_flops(w.scaled(T=64), None) == 3 * (gram + 3 * per_v) * 2 * 16
