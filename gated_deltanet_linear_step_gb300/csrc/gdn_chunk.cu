@@ -92,7 +92,8 @@ static_assert(kOffBars % 8 == 0 && kOffRaw % 16 == 0 && kOffX % 16 == 0 && (kXSt
 static_assert(kOffMisc % 128 == 0 && kOffRaw % 128 == 0, "tensor-map boxes land 128-byte aligned");
 static_assert(kThreads == 384 && kC == 8, "thread roles assume 384 threads and 8-token chunks");
 
-constexpr int kGateWarp = 11;  // loads alpha and beta and builds the decay tables
+constexpr int kGateWarp = 11;   // loads alpha and beta and builds the decay tables
+constexpr int kIssueWarp = 8;   // requests the chunks' inputs (a v-only warp: idle while q and k are normalised)
 
 __device__ unsigned int g_chunk_error = 0;
 
@@ -195,65 +196,92 @@ __device__ __forceinline__ void roll_history(const float* rows, int cc, int tc, 
     }
 }
 
-// Conv + SiLU of one channel over the chunk's tc tokens (zero past tc); h holds the
-// history before the chunk and leaves holding the one after it. The shifts are
-// unconditional and the result a select, so that the unrolled tokens interleave (a
-// shift under t < tc became a branch per token); rows past tc are re-reads of row
-// tc - 1, and the history after the chunk is read back from the rows.
-__device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, int tc, float (&h)[3],
-                                           float (&out)[kC]) {
+// Conv + SiLU of one channel over the chunk's tc tokens (zero past tc), TP >= tc of
+// them evaluated; h holds the history before the chunk and leaves holding the one
+// after it. The shifts are unconditional and the result a select, so that the
+// unrolled tokens interleave (a shift under t < tc became a branch per token);
+// rows past tc are re-reads of row tc - 1, and the history after the chunk is read
+// back from the rows.
+template <int TP>
+__device__ __forceinline__ void conv_tokens(float4 w, const float* rows, int cc, int tc, float (&h)[3],
+                                            float (&out)[kC]) {
     float h0 = h[0], h1 = h[1], h2 = h[2];
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
-        const float xt = rows[(cc >> 7) * kC * kS + max(min(t, tc - 1), 0) * kS + (cc & (kS - 1))];
-        const float xc = conv4(w, h0, h1, h2, xt);
-        h0 = h1;
-        h1 = h2;
-        h2 = xt;
-        const float y = siluf_(xc);
-        out[t] = t < tc ? y : 0.0f;
+        out[t] = 0.0f;
+        if (t < TP) {
+            const float xt = rows[(cc >> 7) * kC * kS + max(min(t, tc - 1), 0) * kS + (cc & (kS - 1))];
+            const float xc = conv4(w, h0, h1, h2, xt);
+            h0 = h1;
+            h1 = h2;
+            h2 = xt;
+            const float y = siluf_(xc);
+            out[t] = t < tc ? y : 0.0f;
+        }
     }
     roll_history(rows, cc, tc, h);
 }
 
+// conv_tokens with the even token count at or above tc (the SiLUs past it are not
+// evaluated: they bound the conv's time on the special-function units).
+__device__ __forceinline__ void conv_chunk(float4 w, const float* rows, int cc, int tc, float (&h)[3],
+                                           float (&out)[kC]) {
+    if (tc <= 2)
+        conv_tokens<2>(w, rows, cc, tc, h, out);
+    else if (tc <= 4)
+        conv_tokens<4>(w, rows, cc, tc, h, out);
+    else if (tc <= 6)
+        conv_tokens<6>(w, rows, cc, tc, h, out);
+    else
+        conv_tokens<8>(w, rows, cc, tc, h, out);
+}
+
 // Pass A on one tile: red[n] = sum_i S[i][col] X[i][n] for this lane's column
 // col = col0 + rb, n < NT (k^ at n < TP, q^ at TP <= n < 2 TP; NT = TP when
-// only S^T k is needed, a call that produces no y).
+// only S^T k is needed, a call that produces no y). The sums run in pairs of n
+// on the packed two-wide FMA (each half rounds as fmaf does), half the issue
+// slots of scalar FMAs.
 template <int NT>
 __device__ __forceinline__ void pass_a(const float* tile, const float* X, int col0, int rb, float (&red)[NT]) {
     static_assert(NT % 2 == 0, "X is read in pairs");
+    constexpr int NP = NT / 2;
     const int lane = threadIdx.x & 31;
-    float acc[4][NT];
+    float2 acc2[4][NP];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int n = 0; n < NT; ++n) acc[c][n] = 0.0f;
+        for (int m = 0; m < NP; ++m) acc2[c][m] = make_float2(0.0f, 0.0f);
 #pragma unroll 1
     for (int r = 0; r < 32; ++r) {
         const int i = 4 * r + rb;
         const float4 s = *reinterpret_cast<const float4*>(tile + i * kS + col0);
-        float xv[NT];
+        float2 xv[NP];
 #pragma unroll
-        for (int m = 0; m < NT / 4; ++m) {
+        for (int m = 0; m < NP / 2; ++m) {
             const float4 v = *reinterpret_cast<const float4*>(X + i * kXStride + 4 * m);
-            xv[4 * m] = v.x;
-            xv[4 * m + 1] = v.y;
-            xv[4 * m + 2] = v.z;
-            xv[4 * m + 3] = v.w;
+            xv[2 * m] = make_float2(v.x, v.y);
+            xv[2 * m + 1] = make_float2(v.z, v.w);
         }
-        if (NT % 4 != 0) {  // NT = 2 or 6 (only S^T k): the last pair
-            const float2 v = *reinterpret_cast<const float2*>(X + i * kXStride + NT - 2);
-            xv[NT - 2] = v.x;
-            xv[NT - 1] = v.y;
-        }
+        if (NP % 2 != 0)  // NT = 2 or 6 (only S^T k): the last pair
+            xv[NP - 1] = *reinterpret_cast<const float2*>(X + i * kXStride + NT - 2);
+        const float2 s0 = make_float2(s.x, s.x), s1 = make_float2(s.y, s.y);
+        const float2 s2 = make_float2(s.z, s.z), s3 = make_float2(s.w, s.w);
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-            acc[0][n] = fmaf(s.x, xv[n], acc[0][n]);
-            acc[1][n] = fmaf(s.y, xv[n], acc[1][n]);
-            acc[2][n] = fmaf(s.z, xv[n], acc[2][n]);
-            acc[3][n] = fmaf(s.w, xv[n], acc[3][n]);
+        for (int m = 0; m < NP; ++m) {
+            acc2[0][m] = __ffma2_rn(s0, xv[m], acc2[0][m]);
+            acc2[1][m] = __ffma2_rn(s1, xv[m], acc2[1][m]);
+            acc2[2][m] = __ffma2_rn(s2, xv[m], acc2[2][m]);
+            acc2[3][m] = __ffma2_rn(s3, xv[m], acc2[3][m]);
         }
     }
+    float acc[4][NT];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int m = 0; m < NP; ++m) {
+            acc[c][2 * m] = acc2[c][m].x;
+            acc[c][2 * m + 1] = acc2[c][m].y;
+        }
     // reduce-scatter over the four row sets (lane bits 3-4): the lane keeps column col0 + rb
     const bool b1 = (lane >> 4) & 1;
     const bool b0 = (lane >> 3) & 1;
@@ -324,39 +352,43 @@ constexpr int kToSmem = 0, kToHbm = 1, kDiscard = 2;
 template <int TP>
 __device__ __forceinline__ void update_tile(float* tile, const float* X, const float* M, int hh, int col0, int rb,
                                             int qd, int tc, const float (&d)[kC], int dst, float* gtile) {
+    static_assert(TP % 2 == 0, "k is read in pairs");
+    constexpr int NP = TP / 2;
     const float* gam = M + kMGam + hh * kC * kC;  // gam[s * kC + t] = G(s, t)
     float e[TP];
 #pragma unroll
     for (int s = 0; s < TP; ++s) e[s] = (s < tc) ? gam[s * kC + (tc - 1)] * d[s] : 0.0f;
-    float E[4][TP];
+    // e of the block's four columns, as pairs of tokens (s, s + 1) for the packed FMA
+    float2 E[4][NP];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int s = 0; s < TP; ++s) E[c][s] = __shfl_sync(0xffffffffu, e[s], (c << 3) | qd);
+        for (int m = 0; m < NP; ++m)
+            E[c][m] = make_float2(__shfl_sync(0xffffffffu, e[2 * m], (c << 3) | qd),
+                                  __shfl_sync(0xffffffffu, e[2 * m + 1], (c << 3) | qd));
     const float al = M[kMCum + hh * kC + tc - 1];
 #pragma unroll 2
     for (int r = 0; r < 32; ++r) {
         const int i = 4 * r + rb;
         float4* sp = reinterpret_cast<float4*>(tile + i * kS + col0);
         float4 s = *sp;
-        s.x *= al;
-        s.y *= al;
-        s.z *= al;
-        s.w *= al;
-        float kk[TP];
+        float2 kk[NP];
 #pragma unroll
-        for (int m = 0; m < TP / 2; ++m) {
-            const float2 k2 = *reinterpret_cast<const float2*>(X + i * kXStride + 2 * m);
-            kk[2 * m] = k2.x;
-            kk[2 * m + 1] = k2.y;
-        }
+        for (int m = 0; m < NP; ++m) kk[m] = *reinterpret_cast<const float2*>(X + i * kXStride + 2 * m);
+        // sum_s k_s e_s per column: token pairs on the packed FMA, the two halves added last
+        float2 a0 = __fmul2_rn(kk[0], E[0][0]), a1 = __fmul2_rn(kk[0], E[1][0]);
+        float2 a2 = __fmul2_rn(kk[0], E[2][0]), a3 = __fmul2_rn(kk[0], E[3][0]);
 #pragma unroll
-        for (int q = 0; q < TP; ++q) {
-            s.x = fmaf(kk[q], E[0][q], s.x);
-            s.y = fmaf(kk[q], E[1][q], s.y);
-            s.z = fmaf(kk[q], E[2][q], s.z);
-            s.w = fmaf(kk[q], E[3][q], s.w);
+        for (int m = 1; m < NP; ++m) {
+            a0 = __ffma2_rn(kk[m], E[0][m], a0);
+            a1 = __ffma2_rn(kk[m], E[1][m], a1);
+            a2 = __ffma2_rn(kk[m], E[2][m], a2);
+            a3 = __ffma2_rn(kk[m], E[3][m], a3);
         }
+        s.x = fmaf(s.x, al, a0.x + a0.y);
+        s.y = fmaf(s.y, al, a1.x + a1.y);
+        s.z = fmaf(s.z, al, a2.x + a2.y);
+        s.w = fmaf(s.w, al, a3.x + a3.y);
         if (dst == kToSmem)
             *sp = s;
         else if (dst == kToHbm)
@@ -431,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
     bool tile_pending = false;  // (leaders) a tile load was issued and has not been waited for
     bool stage_pending = false;  // (warp 0) a chunk's inputs were requested and not waited for
     {
-        if (warp == 0) {
+        if (warp == kIssueWarp) {
             issue_chunk(p, x, 0, min(kC, valid_len(p, x.b)), raw_s, gin_s, stage_bar, lane);
             stage_pending = true;
         }
@@ -495,6 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             // ---- conv + SiLU of this thread's channels; the gates and decay tables
             const int tcw = failed ? 0 : tc;
             float ov[kC], oq[kC];
+#pragma unroll
+            for (int t = 0; t < kC; ++t) oq[t] = 0.0f;  // (q threads without y convolve nothing)
             conv_chunk(wv, raw, vslot, tcw, hv, ov);
             if (has_qk && (write_y || tid >= kS)) conv_chunk(wq, raw, tid, tcw, hq, oq);
             else if (has_qk) roll_history(raw, tid, tcw, hq);  // no y: q is not needed, its history still rolls
@@ -512,14 +546,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     }
                 }
             }
-            if (has_qk && (write_y || tid >= kS)) {  // q (warps 0-3) and k (warps 4-7): per-warp sums of squares
+            if (has_qk && (write_y || tid >= kS)) {
+                // q (warps 0-3) and k (warps 4-7): per-warp sums of squares of the eight tokens, as a
+                // reduce-scatter over the warp (lanes 4 t .. 4 t + 3 end with token t's sum)
+                float sq[kC];
 #pragma unroll
-                for (int t = 0; t < kC; ++t) {
-                    if (t < tc) {
-                        const float ss = warp_sum(oq[t] * oq[t]);
-                        if (lane == 0) M[kMPart + warp * kC + t] = ss;
+                for (int t = 0; t < kC; ++t) sq[t] = oq[t] * oq[t];
+#pragma unroll
+                for (int m = 16, c = kC; m >= 4; m >>= 1, c >>= 1) {
+                    const bool up = (lane & m) != 0;
+#pragma unroll
+                    for (int j = 0; j < c / 2; ++j) {
+                        const float send = up ? sq[j] : sq[j + c / 2];
+                        const float keep = up ? sq[j + c / 2] : sq[j];
+                        sq[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
                     }
                 }
+                sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 2);
+                sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 1);
+                if ((lane & 3) == 0) M[kMPart + warp * kC + (lane >> 2)] = sq[0];
             }
             if (warp == kGateWarp) {
                 // lane (h, t): beta and decay, then A_t and G(s, t) from the head's decays by shuffles
@@ -552,18 +597,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             }
             __syncthreads();  // (A) the chunk's inputs have been read; sums of squares and gates are in place
 
-            // ---- the staging area takes the next chunk's inputs, or the next unit's first ones
-            if (warp == 0 && !failed) {
-                if (!last_chunk) {
-                    fence_proxy_async_smem();
-                    issue_chunk(p, x, c0 + kC, min(kC, n - c0 - kC), raw_s, gin_s, stage_bar, lane);
-                    stage_pending = true;
-                } else if (has_next) {
-                    fence_proxy_async_smem();
-                    issue_chunk(p, xn, 0, min(kC, n_next), raw_s, gin_s, stage_bar, lane);
-                    stage_pending = true;
-                }
-            }
             // ---- q^ and k^ (normalised; q scaled) into X; the k warps keep k^ for the Gram matrices
             const int tp = (tc + 1) & ~1;
             if (has_qk && tc > 0 && (write_y || tid >= kS)) {
@@ -585,36 +618,42 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             }
             __syncthreads();  // (B) X is in place
 
-            // ---- Gram matrices from the k warps: products at 8s+t (k_s.k_t for s<t, k_t.q_s for t<=s),
-            //      in two halves of 32, each reduce-scattered over the warp (lane L keeps product
-            //      32 half + L), partial sums per warp
-            if (warp >= 4 && warp < 8 && tc > 0) {
-                const int i = tid - kS;
-                float qv[kC];
+            // ---- Gram matrices: products at 8s+t (k_s.k_t for s<t, k_t.q_s for t<=s), s in [0, 4) by the q
+            //      warps 0-3 (k^ from X) and s in [4, 8) by the k warps 4-7 (q^ from X), 32 per warp, each
+            //      reduce-scattered over the warp (lane L keeps product 32 hf + L), partial sums per warp
+            if (warp < 8 && tc > 0) {
+                const int hf = warp >> 2;
+                const int i = tid & (kS - 1);
+                float kv[kC], qv[kC];
 #pragma unroll
-                for (int s = 0; s < kC; ++s) qv[s] = (s < tc) ? X[i * kXStride + tp + s] : 0.0f;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float pr[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int s = 4 * hf + (j >> 3), t = j & 7;
-                        pr[j] = (s < t) ? oq[s] * oq[t] : oq[t] * qv[s];
-                    }
-#pragma unroll
-                    for (int m = 16, c = 32; m >= 1; m >>= 1, c >>= 1) {
-                        const bool up = (lane & m) != 0;
-#pragma unroll
-                        for (int j = 0; j < c / 2; ++j) {
-                            const float send = up ? pr[j] : pr[j + c / 2];
-                            const float keep = up ? pr[j + c / 2] : pr[j];
-                            pr[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-                        }
-                    }
-                    M[kMGram + (warp - 4) * 64 + 32 * hf + lane] = pr[0];
+                for (int t = 0; t < kC; ++t) {
+                    const float xk = (t < tc) ? X[i * kXStride + t] : 0.0f;
+                    const float xq = (t < tc && write_y) ? X[i * kXStride + tp + t] : 0.0f;
+                    kv[t] = hf ? oq[t] : xk;
+                    qv[t] = hf ? xq : (write_y ? oq[t] : 0.0f);
                 }
+                float pr[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int sl = j >> 3, t = j & 7;  // s = 4 hf + sl
+                    const float ks = hf ? kv[4 + sl] : kv[sl];
+                    const float qs = hf ? qv[4 + sl] : qv[sl];
+                    pr[j] = (4 * hf + sl < t) ? ks * kv[t] : kv[t] * qs;
+                }
+#pragma unroll
+                for (int m = 16, c = 32; m >= 1; m >>= 1, c >>= 1) {
+                    const bool up = (lane & m) != 0;
+#pragma unroll
+                    for (int j = 0; j < c / 2; ++j) {
+                        const float send = up ? pr[j] : pr[j + c / 2];
+                        const float keep = up ? pr[j + c / 2] : pr[j];
+                        pr[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
+                }
+                M[kMGram + (warp & 3) * 64 + 32 * hf + lane] = pr[0];
             }
             __syncthreads();  // (C) the Gram partials are in place
+
 
             // ---- this group's coefficients; this unit's tile (first chunk)
             if (gtid < 64 && tc > 0) {
@@ -633,6 +672,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     failed = true;
                 }
                 give_up = false;
+            }
+            // ---- the staging area (free since barrier A) takes the next chunk's inputs, or the next unit's
+            //      first ones: requested once the tile has landed, when the copy engine has no tile
+            //      refill ahead of them (requested at barrier A they took a warp 1.4 us to issue)
+            if (warp == kIssueWarp && !failed) {
+                if (!last_chunk) {
+                    fence_proxy_async_smem();
+                    issue_chunk(p, x, c0 + kC, min(kC, n - c0 - kC), raw_s, gin_s, stage_bar, lane);
+                    stage_pending = true;
+                } else if (has_next) {
+                    fence_proxy_async_smem();
+                    issue_chunk(p, xn, 0, min(kC, n_next), raw_s, gin_s, stage_bar, lane);
+                    stage_pending = true;
+                }
             }
 
             // ---- pass A, then (after the group's coefficients are in place) the column recurrence
@@ -743,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             if (__syncthreads_or(failed ? 1 : 0)) {
                 // A wait gave up: record it, let every copy still in flight land (bounded), stop.
                 if (tid == 0) atomicOr(&g_chunk_error, kErrWaitTimeout);
-                if (warp == 0 && lane == 0 && stage_pending) (void)mbar_wait_bounded(stage_bar, stage_par);
+                if (warp == kIssueWarp && lane == 0 && stage_pending) (void)mbar_wait_bounded(stage_bar, stage_par);
                 if (group_leader && tile_pending) (void)mbar_wait_bounded(my_bar, tile_par);
                 return;
             }
