@@ -44,7 +44,9 @@
 // arrive while the tiles are worked on. A unit's last update writes the new
 // tile straight to HBM with streaming stores, so the slot is free once the
 // group has read it: its leader then requests the next unit's tile, which an
-// L2 prefetch issued a unit earlier has already brought into L2. The next
+// L2 prefetch issued with the next unit's inputs (about half a unit earlier,
+// once this unit's tiles have landed) has brought into L2; a prefetch a whole
+// unit ahead measured slower than none, its lines evicted before use. The next
 // unit's conv histories and taps are loaded into registers a unit ahead.
 // Waits are bounded; a wait that gives up stops the CTA after every copy it
 // issued has landed (bounded), with the device error word set.
@@ -685,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     fence_proxy_async_smem();
                     issue_chunk(p, xn, 0, min(kC, n_next), raw_s, gin_s, stage_bar, lane);
                     stage_pending = true;
+                    if (n_next > 0 && lane >= 16 && lane < 16 + kGroup)  // the next unit's tiles into L2
+                        bulk_prefetch_l2(tile_src(p, xn, lane - 16), kTileBytes);
                 }
             }
 
@@ -786,10 +790,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     mbar_arrive_expect_tx(my_bar, kTileBytes);
                     bulk_load_stream(my_tile_s, tile_src(p, xn, hh), kTileBytes, my_bar);
                     tile_pending = true;
-                }
-                if (u + 2 < u_end) {
-                    const Unit xnn = next_unit(p, xn);
-                    if (valid_len(p, xnn.b) > 0) bulk_prefetch_l2(tile_src(p, xnn, hh), kTileBytes);
                 }
             }
 
