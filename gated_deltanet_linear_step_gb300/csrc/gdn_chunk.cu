@@ -253,7 +253,7 @@ __device__ __forceinline__ void pass_a(const float* tile, const float* X, int co
     for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int m = 0; m < NP; ++m) acc2[c][m] = make_float2(0.0f, 0.0f);
-#pragma unroll 1
+#pragma unroll 4
     for (int r = 0; r < 32; ++r) {
         const int i = 4 * r + rb;
         const float4 s = *reinterpret_cast<const float4*>(tile + i * kS + col0);
@@ -493,10 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
     bool failed = false;
     bool give_up = (p.flags & kTestGiveUp) != 0;  // the first tile wait gives up (tests this path)
 
+    int n_carry = valid_len(p, x.b);  // this unit's token count, read a unit ahead
     for (long long u = u_begin; u < u_end; ++u) {
         const bool has_next = u + 1 < u_end;
         const Unit xn = has_next ? next_unit(p, x) : x;
-        const int n = valid_len(p, x.b);
+        const int n = n_carry;
         const int n_next = has_next ? valid_len(p, xn.b) : 0;
         const int vch = unit_channel(vslot, x.g);
         const int qkch = unit_channel(tid, x.g);
@@ -803,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             if (last_chunk) break;
         }
         x = xn;
+        n_carry = n_next;
     }
 }
 
