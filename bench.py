@@ -174,6 +174,17 @@ def measured_peaks():
 CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 8, 20, 64
 
 
+def kernel_name(T: int) -> str:
+    """The kernel a call with T tokens runs (the library's dispatch)."""
+    if T == 1:
+        return "gdn_decode_t1_kernel"
+    if T <= CHUNK_MAX_T:
+        return "gdn_chunk_kernel"
+    if T < TC_MIN_T:
+        return "gdn_window_kernel"
+    return "gdn_window_tc_kernel"
+
+
 def kernel_sources(T: int) -> list:
     """The sources of the kernel a call with T tokens runs."""
     if T == 1:
@@ -521,7 +532,7 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
     roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T))
     out = {"workload": name, "B": w.B, "L": w.L, "T": w.T, "steps": steps, "ms_per_step": ms,
            "value": updates / (ms / 1e3), "unit": UNIT,
-           "kernel": "gdn_decode_t1_kernel" if w.T == 1 else "gdn_window_kernel", "l2": l2, "roofline": roof}
+           "kernel": kernel_name(w.T), "l2": l2, "roofline": roof}
     del t, y, step
     torch.cuda.empty_cache()
     return out
