@@ -169,9 +169,10 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# Windows of 2-8 tokens run the kernel with the tiles in shared memory, 9-19 the register
-# window kernel, 20 or more the tensor-core chunk kernel (the library's dispatch).
-CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 8, 20, 64
+# The library's dispatch: windows of 2-24 tokens run the kernel with the tiles in shared memory, 25
+# or more the tensor-core chunk kernel; the register window kernel serves only builds with other
+# thresholds.
+CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
 
 
 def kernel_name(T: int) -> str:

@@ -602,13 +602,17 @@ cudaError_t device_setup(int* clusters) {
 }  // namespace
 
 // Windows of up to GDN_CHUNK_MAX_T tokens run the kernel with the tiles resident
-// in shared memory (gdn_chunk.cu); windows of GDN_TC_MIN_T tokens or more run
-// the tensor-core chunk kernel (gdn_window_tc.cu); any others gdn_window_kernel.
+// in shared memory (gdn_chunk.cu, chunks of 8 tokens); windows of GDN_TC_MIN_T
+// tokens or more run the tensor-core chunk kernel (gdn_window_tc.cu); any others
+// gdn_window_kernel. The defaults are the measured crossovers (16 sequences x 36
+// layers): the chunked kernel is the fastest up to 24 tokens, the tensor-core
+// kernel from there on, so no window falls to gdn_window_kernel unless a build
+// sets other thresholds (as timing comparisons do).
 #ifndef GDN_CHUNK_MAX_T
-#define GDN_CHUNK_MAX_T 8
+#define GDN_CHUNK_MAX_T 24
 #endif
 #ifndef GDN_TC_MIN_T
-#define GDN_TC_MIN_T 20
+#define GDN_TC_MIN_T 25
 #endif
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {

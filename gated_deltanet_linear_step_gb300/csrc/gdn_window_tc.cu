@@ -1,4 +1,5 @@
-// gdn_window_tc.cu - the decode step over windows of more than 8 tokens: chunks
+// gdn_window_tc.cu - the decode step over long windows (25 tokens or more in the
+// library's dispatch; the kernel itself takes any length of 2 or more): chunks
 // of up to 64 tokens whose contractions run on the tensor cores (tcgen05.mma
 // from shared memory into tensor memory), with the conv, the gates, the
 // inversion of the solve matrix and the epilogues on the CUDA cores.

@@ -37,16 +37,17 @@
  *    while the kernel runs surface at the caller's next synchronisation.
  *  - Outputs may not overlap any other buffer of the call (GDN_ERR_ALIAS).
  *    Inputs may overlap each other.
- *  - Arithmetic. One token (T = 1) and windows of up to 19 tokens run the
- *    definition in fp32 on the CUDA cores (windows of 2 to 8 tokens regroup
- *    its sums per column, exactly up to rounding). Windows of 20 tokens or
- *    more take chunks of 64 tokens whose contractions (S^T k, S^T q, the
- *    Gram matrices, the triangular solve's product and the state update)
- *    run on the tensor cores as three BF16 products of each fp32 operand's
- *    hi + lo halves, accumulated in fp32: each product carries a relative
- *    error of at most about 2^-16, and y and the state come out within about
- *    3e-5 of the exact result relative to their largest magnitude. The conv
- *    history (conv_state) is always an exact copy.
+ *  - Arithmetic. One token (T = 1) and windows of up to 24 tokens run the
+ *    definition in fp32 on the CUDA cores (windows of 2 to 24 tokens regroup
+ *    its sums per column in chunks of 8 tokens, exactly up to rounding).
+ *    Windows of 25 tokens or more take chunks of 64 tokens whose
+ *    contractions (S^T k, S^T q, the Gram matrices, the triangular solve's
+ *    product and the state update) run on the tensor cores as three BF16
+ *    products of each fp32 operand's hi + lo halves, accumulated in fp32:
+ *    each product carries a relative error of at most about 2^-16, and y and
+ *    the state come out within about 3e-5 of the exact result relative to
+ *    their largest magnitude. The conv history (conv_state) is always an
+ *    exact copy.
  */
 #ifndef GDN_H
 #define GDN_H

@@ -77,14 +77,21 @@ def test_kernel_sources_follow_the_library_dispatch():
     names = lambda T: [os.path.basename(p) for p in bench.kernel_sources(T)]
     assert names(1)[0] == "gdn_decode_t1.cu"
     assert names(2)[0] == names(bench.CHUNK_MAX_T)[0] == "gdn_chunk.cu"
-    assert names(bench.CHUNK_MAX_T + 1)[0] == names(bench.TC_MIN_T - 1)[0] == "gdn_step.cu"
     assert names(bench.TC_MIN_T)[0] == names(1024)[0] == "gdn_window_tc.cu"
+    # with the default thresholds no window runs the register kernel; with others it takes the gap
+    assert bench.CHUNK_MAX_T + 1 == bench.TC_MIN_T
+    saved = bench.CHUNK_MAX_T, bench.TC_MIN_T
+    try:
+        bench.CHUNK_MAX_T, bench.TC_MIN_T = 8, 20
+        assert names(9)[0] == names(19)[0] == "gdn_step.cu" and bench.kernel_name(12) == "gdn_window_kernel"
+    finally:
+        bench.CHUNK_MAX_T, bench.TC_MIN_T = saved
     # the kernel names the configs block reports, one per source
-    assert [bench.kernel_name(T) for T in (1, 2, bench.CHUNK_MAX_T + 1, bench.TC_MIN_T)] == [
-        "gdn_decode_t1_kernel", "gdn_chunk_kernel", "gdn_window_kernel", "gdn_window_tc_kernel"]
-    for T in (1, 2, bench.CHUNK_MAX_T + 1, bench.TC_MIN_T):
+    assert [bench.kernel_name(T) for T in (1, 2, bench.CHUNK_MAX_T, bench.TC_MIN_T)] == [
+        "gdn_decode_t1_kernel", "gdn_chunk_kernel", "gdn_chunk_kernel", "gdn_window_tc_kernel"]
+    for T in (1, 2, bench.TC_MIN_T):
         kernel_src = open(bench.kernel_sources(T)[0]).read()
-        assert f"void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
+        assert "void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()

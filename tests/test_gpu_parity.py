@@ -117,10 +117,10 @@ def _small(scale=dict(B=3, L=2, T=9), name="verify_b16_l36_t8_ragged"):
 
 def test_t_tokens_in_one_call_equal_t_single_calls(g):
     """One T-token call and T one-token calls agree to within the parity tolerance:
-    both follow the same definition, but the window kernel regroups it by chunks and
-    runs its products on the tensor cores with BF16 hi + lo operands (errors near
-    2e-5 of the largest value), while the single-token kernel sums in fp32 on the
-    CUDA cores."""
+    both follow the same definition, but the window kernels regroup it by chunks (in
+    fp32 up to 24 tokens; past that with the products on the tensor cores, BF16 hi + lo
+    operands, errors near 2e-5 of the largest value), while the single-token kernel
+    sums token by token."""
     w, h = _small(name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     a = U.to_device(h, dev)
@@ -138,9 +138,9 @@ def test_t_tokens_in_one_call_equal_t_single_calls(g):
     assert torch.equal(a["conv_state"], b["conv_state"])
 
 
-# (window length, prefix length): both calls of a case run the same kernel (windows of up to 8
-# tokens run the shared-memory kernel, 9 to 31 the register kernel, 32 or more the tensor-core
-# kernel, in chunks of 64), so they agree bit for bit.
+# (window length, prefix length): both calls of a case run the same kernel over the same chunks
+# (windows of up to 24 tokens run the shared-memory kernel in chunks of 8, 25 or more the
+# tensor-core kernel in chunks of 64), so they agree bit for bit.
 @pytest.mark.parametrize("T,P", [(8, 3), (12, 10), (40, 33), (70, 66)])
 def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
     w, h = _small(dict(B=3, L=2, T=T))
