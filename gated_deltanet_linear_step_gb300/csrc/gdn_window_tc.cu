@@ -287,14 +287,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
         pend_qk = true;
     };
     // A state tile in two 32 KB halves: dims [0, 64) into the P and solve-matrix regions, [64, 128)
-    // into the v staging; by thread 32, once its state bulk store (if any) has read those regions
-    // (its last group, when y is written, holds y rows and may still be reading).
+    // into the v staging, by thread 32 (no bulk copy reads those regions: the new state leaves from
+    // tensor memory by plain stores, the y rows from the region S0^T used).
     auto issue_s = [&](long long xbl, int xvh) {
         if (tid == 32) {
-            if (write_y)
-                bulk_wait_read_one();
-            else
-                bulk_wait_read();
             const float* src = p.state + (static_cast<size_t>(xbl) * kVHeads + xvh) * kTile;
             mbar_arrive_expect_tx(bar_s, kTile * 4);
             bulk_load(base + kOffP, src, kTile * 2, bar_s);
@@ -776,6 +772,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                     failed = true;
                     break;
                 }
+                // ---- the P, solve-matrix and v regions are free: after a v head's last chunk they take the
+                //      next state tile now, which then lands during the y epilogue (the next unit's first
+                //      tile after the unit's last v head; its q|k rows follow once y has left)
+                if (last) {
+                    if (h + 1 < kGroup) {
+                        issue_s(bl, vh + 1);
+                    } else {
+                        const long long nu = u + gridDim.x;
+                        if (nu < p.n_units) {
+                            const long long nbl = nu / kKHeads;
+                            const int ng = static_cast<int>(nu - nbl * kKHeads);
+                            if (unit_len(p, static_cast<int>(nbl / p.L)) > 0) {
+                                issue_s(nbl, ng * kGroup);
+                                s_ahead = true;
+                            }
+                        }
+                    }
+                }
                 if (write_y) {
                     // z rows of the chunk into the half of the region that E^T held
                     if (warp == 1) {
@@ -802,29 +816,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         }
                     }
                 }
-                const bool store_state = last && write_state;
-                if (store_state) {
-                    // ---- the new state tile, dims [0, 64) into the P and solve-matrix regions, [64, 128)
-                    //      into the v staging (both free now), for two 32 KB bulk stores; thread (column,
-                    //      dims [32 wg, +32))
-                    float* half_s = reinterpret_cast<float*>(sm + (wg >= 2 ? kOffV : kOffP));
+                if (last && write_state) {
+                    // ---- the new state tile from tensor memory straight to HBM: thread (column col, dims
+                    //      [32 wg, +32)); a warp's 32 lanes store 32 adjacent columns of a dim's row
                     uint32_t v[32];
                     tmem_ld32(tmem + kTmS + lane_off + 32 * wg, v);
+                    float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile + 32 * wg * kS + col;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) half_s[(32 * (wg & 1) + i) * kS + col] = u2f(v[i]);
-                    fence_proxy_async_smem();
+                    for (int i = 0; i < 32; ++i) __stcs(dst + i * kS, u2f(v[i]));
                 }
                 tc_fence_before();
                 __syncthreads();
-                if (tid == 32) {
-                    // one bulk group for the state (possibly empty), committed before the y rows' group
-                    if (store_state) {
-                        float* dst = p.state + (static_cast<size_t>(bl) * kVHeads + vh) * kTile;
-                        bulk_store(dst, base + kOffP, kTile * 2);
-                        bulk_store(dst + kTile / 2, base + kOffV, kTile * 2);
-                    }
-                    bulk_commit();
-                }
                 if (write_y) {
                     if (!wait_all(bar_z, ph_z)) {
                         failed = true;
@@ -852,22 +854,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                         bulk_commit();
                     }
                 }
-                // ---- the next v head's state tile, or the next unit's first tile and q|k rows, requested
-                //      now: their regions are free once this v head's stores have read them
-                if (last) {
-                    if (h + 1 < kGroup) {
-                        issue_s(bl, vh + 1);
-                    } else {
-                        const long long nu = u + gridDim.x;
-                        if (nu < p.n_units) {
-                            const long long nbl = nu / kKHeads;
-                            const int ng = static_cast<int>(nu - nbl * kKHeads);
-                            const int nn = unit_len(p, static_cast<int>(nbl / p.L));
-                            if (nn > 0) {
-                                issue_s(nbl, ng * kGroup);
-                                issue_qk(nbl, ng, 0, min(nn, kC));
-                                s_ahead = qk_ahead = true;
-                            }
+                // ---- after the unit's last v head, the next unit's first q|k rows, into the region the y
+                //      rows leave once their stores have read it
+                if (last && h + 1 == kGroup) {
+                    const long long nu = u + gridDim.x;
+                    if (nu < p.n_units) {
+                        const long long nbl = nu / kKHeads;
+                        const int ng = static_cast<int>(nu - nbl * kKHeads);
+                        const int nn = unit_len(p, static_cast<int>(nbl / p.L));
+                        if (nn > 0) {
+                            issue_qk(nbl, ng, 0, min(nn, kC));
+                            qk_ahead = true;
                         }
                     }
                 }
