@@ -606,63 +606,69 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                             }
                         }
                     }
-                    named_barrier(1, 256);
-                    if (tid < kC) {
-                        // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
-                        const int i = tid >> 4, j = tid & 15;
-                        float x[16];
+                    // X and its BF16 operand are written where S0^T lo was: the state MMA must have read it
+                    // (its commit is waited for here; the rhs warps wait for it too, before R^T)
+                    const bool ab_late = !mbar_wait_bounded(bar_ab, ph_ab);
+                    group_late = named_barrier_or(1, 256, ab_late);
+                    if (!group_late) {
+                        tc_fence_after();
+                        if (tid < kC) {
+                            // diagonal blocks: thread (i, j) solves column j of block i by forward substitution
+                            const int i = tid >> 4, j = tid & 15;
+                            float x[16];
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) {
-                            const float* Lr = L_s + (16 * i + r) * kLStride + 16 * i;
-                            float acc = 0.0f;
+                            for (int r = 0; r < 16; ++r) {
+                                const float* Lr = L_s + (16 * i + r) * kLStride + 16 * i;
+                                float acc = 0.0f;
 #pragma unroll
-                            for (int m = 0; m < r; ++m) acc = fmaf(Lr[m], x[m], acc);
-                            x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
+                                for (int m = 0; m < r; ++m) acc = fmaf(Lr[m], x[m], acc);
+                                x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
+                            }
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
                         }
+                        named_barrier(1, 256);
+                        {
+                            // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj; thread
+                            // (r, c) of each 16x16 block
+                            const int r = tid >> 4, c = tid & 15;
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
-                    }
-                    named_barrier(1, 256);
-                    {
-                        // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj; thread
-                        // (r, c) of each 16x16 block
-                        const int r = tid >> 4, c = tid & 15;
+                            for (int dist = 1; dist < 4; ++dist) {
+                                for (int j = 0; j + dist < 4; ++j) {
+                                    const int i = j + dist;
+                                    float y = 0.0f;
+                                    for (int k = j; k < i; ++k) {
+                                        const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
 #pragma unroll
-                        for (int dist = 1; dist < 4; ++dist) {
-                            for (int j = 0; j + dist < 4; ++j) {
-                                const int i = j + dist;
-                                float y = 0.0f;
-                                for (int k = j; k < i; ++k) {
-                                    const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
-#pragma unroll
-                                    for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
+                                        for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
+                                    }
+                                    Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
                                 }
-                                Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
-                            }
-                            named_barrier(1, 256);
-                            for (int j = 0; j + dist < 4; ++j) {
-                                const int i = j + dist;
-                                float x = 0.0f;
+                                named_barrier(1, 256);
+                                for (int j = 0; j + dist < 4; ++j) {
+                                    const int i = j + dist;
+                                    float x = 0.0f;
 #pragma unroll
-                                for (int m = 0; m < 16; ++m)
-                                    x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
-                                Xs[(16 * i + r) * kC + 16 * j + c] = x;
+                                    for (int m = 0; m < 16; ++m)
+                                        x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
+                                    Xs[(16 * i + r) * kC + 16 * j + c] = x;
+                                }
+                                named_barrier(1, 256);
                             }
-                            named_barrier(1, 256);
                         }
-                    }
-                    {
-                        // X as the BF16 operand [t][s]; blocks above the diagonal are zero
-                        const int t = tid >> 2;
+                        {
+                            // X as the BF16 operand [t][s]; blocks above the diagonal are zero
+                            const int t = tid >> 2;
 #pragma unroll
-                        for (int h2 = 0; h2 < 2; ++h2) {
-                            const int j = 2 * (tid & 3) + h2;  // columns [8 j, 8 j + 8)
-                            float xv[8];
-                            const bool upper = (j >> 1) > (t >> 4);
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                const int j = 2 * (tid & 3) + h2;  // columns [8 j, 8 j + 8)
+                                float xv[8];
+                                const bool upper = (j >> 1) > (t >> 4);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
-                            const uint32_t off = kOffXop + sw128_offset(t, j);
-                            store_split8(sm + off, sm + off + 64 * 128, xv);
+                                for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
+                                const uint32_t off = kOffXop + sw128_offset(t, j);
+                                store_split8(sm + off, sm + off + 64 * 128, xv);
+                            }
                         }
                     }
                 } else {
