@@ -38,6 +38,8 @@ SMALL = [
     ("decode_b64_l36_t1", dict(B=1, L=2, T=9)),
     ("decode_b64_l36_t1", dict(B=2, L=1, T=17)),
     ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=20)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=24)),   # three full 8-token chunks, the longest on that kernel
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=25)),   # the shortest window on the tensor-core kernel
     ("decode_b64_l36_t1", dict(B=2, L=1, T=40)),
     ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=1, L=1, T=64)),
     ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=70)),
@@ -198,7 +200,7 @@ def test_deterministic_and_batch_permutation_equivariant(g):
     assert torch.equal(c["conv_state"], a["conv_state"][perm])
 
 
-@pytest.mark.parametrize("T", [6, 40])
+@pytest.mark.parametrize("T", [6, 16, 40])
 def test_verify_window_then_commit(g, T):
     w, h = _small(dict(B=3, L=2, T=T))
     dev = torch.device("cuda:0")
