@@ -40,8 +40,10 @@
 // Overlap. Shared memory holds the three tiles, the chunk's raw qkv rows (with
 // the heads' alpha, beta, dt and ssm_a) and the normalised q and k (separate
 // from the raw rows), so the next chunk's inputs (or the next unit's first
-// ones) are requested as soon as the conv has read the current ones, and
-// arrive while the tiles are worked on. A unit's last update writes the new
+// ones) are requested, by a v-only warp, once the conv has read the current
+// ones and the unit's tiles have landed (the copy engine then has no tile
+// refill ahead of them), and arrive while the tiles are worked on. Pass A and
+// the update run on the packed two-wide FMA. A unit's last update writes the new
 // tile straight to HBM with streaming stores, so the slot is free once the
 // group has read it: its leader then requests the next unit's tile, which an
 // L2 prefetch issued with the next unit's inputs (about half a unit earlier,
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
     float hv[3], hq[3] = {0.f, 0.f, 0.f};  // conv histories of this thread's channels
     float4 wv, wq = make_float4(0.f, 0.f, 0.f, 0.f);  // conv taps of this thread's channels
     bool tile_pending = false;  // (leaders) a tile load was issued and has not been waited for
-    bool stage_pending = false;  // (warp 0) a chunk's inputs were requested and not waited for
+    bool stage_pending = false;  // (issue warp) a chunk's inputs were requested and not waited for
     {
         if (warp == kIssueWarp) {
             issue_chunk(p, x, 0, min(kC, valid_len(p, x.b)), raw_s, gin_s, stage_bar, lane);
