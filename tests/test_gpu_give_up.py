@@ -20,7 +20,8 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [1, 4, 12, 48], ids=["single_token", "short_window", "long_window", "tensor_core_window"])
+@pytest.mark.parametrize("T", [1, 4, 12, 48],
+                         ids=["single_token", "one_chunk_window", "multi_chunk_window", "tensor_core_window"])
 def test_a_wait_that_gives_up_drains_reports_and_leaves_the_context_usable(cuda_device, T):
     import gated_deltanet_linear_step_gb300 as g
 
