@@ -528,12 +528,42 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
         ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
         l2 = L2_NOTE_FLUSH
         del flush
+    # A window of T > 1 tokens (all valid) is also timed as T single-token calls over the same
+    # inputs, the alternative a caller without the window kernels has (same graph timing).
+    singles = None
+    if w.T > 1 and t["seq_len"] is None and working > 2 * L2_BYTES:
+        y1 = torch.empty(t["z"][:, :, :1].shape, device=dev)
+        calls = []
+        for tt in range(w.T):
+            one = dict(t)
+            for k in ("qkv", "z", "alpha", "beta"):
+                one[k] = t[k][:, :, tt:tt + 1].contiguous()
+            calls.append(make_step(g, one, y1))
+        for call in calls:
+            call()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                for call in calls:
+                    call()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms1 = a.elapsed_time(b) / steps
+        singles = {"calls_per_step": w.T, "ms_per_step": ms1, "value": valid_tokens(w, lens) / (ms1 / 1e3),
+                   "kernel": kernel_name(1)}
+        del graph, calls, y1
     assert g.gdn_read_device_error(device=dev) == 0, f"a kernel reported a device error on {name}"
     updates = valid_tokens(w, lens)
     roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T))
     out = {"workload": name, "B": w.B, "L": w.L, "T": w.T, "steps": steps, "ms_per_step": ms,
            "value": updates / (ms / 1e3), "unit": UNIT,
            "kernel": kernel_name(w.T), "l2": l2, "roofline": roof}
+    if singles is not None:
+        out["as_single_token_calls"] = singles
     del t, y, step
     torch.cuda.empty_cache()
     return out
