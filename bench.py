@@ -528,6 +528,20 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
         ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
         l2 = L2_NOTE_FLUSH
         del flush
+        # the same calls back to back from one captured graph, the working set left in L2 (reported
+        # beside, not the value; issued one by one from the host they would wait on the launches)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(steps):
+                step()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        warm_ms = a.elapsed_time(b) / steps
+        del graph
     # A window of T > 1 tokens (all valid) is also timed as T single-token calls over the same
     # inputs, the alternative a caller without the window kernels has (same graph timing).
     singles = None
@@ -564,6 +578,8 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
            "kernel": kernel_name(w.T), "l2": l2, "roofline": roof}
     if singles is not None:
         out["as_single_token_calls"] = singles
+    if working <= 2 * L2_BYTES:
+        out["warm_l2_ms_per_step"] = warm_ms
     del t, y, step
     torch.cuda.empty_cache()
     return out
