@@ -49,9 +49,15 @@
 // L2 prefetch issued with the next unit's inputs (about half a unit earlier,
 // once this unit's tiles have landed) has brought into L2; a prefetch a whole
 // unit ahead measured slower than none, its lines evicted before use. The next
-// unit's conv histories and taps are loaded into registers a unit ahead.
-// Waits are bounded; a wait that gives up stops the CTA after every copy it
-// issued has landed (bounded), with the device error word set.
+// unit's conv histories and taps are loaded into registers a unit ahead. No CTA
+// barrier closes a chunk: a group that has finished its update starts the next
+// chunk's conv while the others still store theirs (the gate tables alternate
+// between two copies so that the next chunk's do not overwrite the ones still
+// applied); the next chunk's first barrier gathers them.
+// Waits are bounded; a wait that gives up raises a shared abort flag (the
+// other threads' waits then return at once), and the CTA stops at the next
+// chunk's first barrier after every copy it issued has landed (bounded), with
+// the device error word set.
 
 #include <mutex>
 
@@ -81,15 +87,21 @@ constexpr int kMBeta = kMCoef + kGroup * 64;   // [3][kC]
 constexpr int kMCum = kMBeta + kGroup * kC;    // [3][kC] A_t
 constexpr int kMGam = kMCum + kGroup * kC;     // [3][kC][kC] G(s, t) at [h][s][t]
 constexpr int kMRms = kMGam + kGroup * kC * kC;  // [3][4][kC] sums of o^2 per (head, warp, token)
-constexpr int kMFloats = kMRms + kGroup * 4 * kC;
+// The gate tables (beta, A_t, G) of alternate chunks: kMBeta .. kMGam, then a second copy at kMGate2
+// with the same layout, so that the gate warp may fill the next chunk's while other groups still
+// apply the current one (no CTA barrier between a chunk's update and the next chunk's conv).
+constexpr int kMGateSpan = kMRms - kMBeta;
+constexpr int kMGate2 = kMRms + kGroup * 4 * kC;
+constexpr int kMFloats = kMGate2 + kMGateSpan;
 
 constexpr size_t kOffTiles = 0;
 constexpr size_t kOffRaw = size_t(kGroup) * kTileBytes;              // 196608: qkv rows [5 segments][kC][128]
 constexpr size_t kOffX = kOffRaw + size_t(kC) * kUnitCh * 4;         // 217088: X [128][kXStride]
 constexpr size_t kOffMisc = kOffX + size_t(kS) * kXStride * 4;       // 227328
-constexpr size_t kOffBars = kOffMisc + size_t(kMFloats) * 4;         // 231296
+constexpr size_t kOffBars = kOffMisc + size_t(kMFloats) * 4;         // 232256
 constexpr int kBarTile = 0, kBarStage = 3, kNumBars = 4;
-constexpr size_t kSmemBytes = kOffBars + kNumBars * 8;               // 231328
+constexpr size_t kOffAbort = kOffBars + kNumBars * 8;                // a wait gave up (set once, read by waits)
+constexpr size_t kSmemBytes = kOffAbort + 8;                         // 232296
 
 static_assert(kSmemBytes <= 232448, "shared memory budget exceeds 227 KB");
 static_assert(kOffBars % 8 == 0 && kOffRaw % 16 == 0 && kOffX % 16 == 0 && (kXStride * 4) % 16 == 0, "alignment");
@@ -175,6 +187,21 @@ __device__ __forceinline__ void issue_chunk(const Params& p, const Unit& x, int 
     if (lane == 7 || lane == 8) {
         const float* src = (lane == 8 ? p.ssm_a : p.dt) + static_cast<size_t>(x.l) * kVHeads + gb;
         bulk_load(gin + (2 * kC * 8 + (lane - 7) * 8) * 4, src, gbytes, bar);
+    }
+}
+
+// Waits for phase `parity` of the mbarrier: true once it completes; false at once if another
+// thread's wait gave up (the abort flag), or after kWaitLimitNs (the flag is then set).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            return false;
+        }
     }
 }
 
@@ -310,10 +337,10 @@ __device__ __forceinline__ void pass_a(const float* tile, const float* X, int co
 // per token from pass A's u_t = red[t] and w_t = red[TP + t], v_t, the gates
 // and the group's coefficients.
 template <int TP, bool WQ>
-__device__ __forceinline__ void solve_column(const float (&red)[WQ ? 2 * TP : TP], const float* M, int hh, int tc,
+__device__ __forceinline__ void solve_column(const float (&red)[WQ ? 2 * TP : TP], const float* M, int gofs2, int hh, int tc,
                                              const float (&v)[kC], float (&d)[kC], float (&o)[kC]) {
-    const float* cum = M + kMCum + hh * kC;
-    const float* bet = M + kMBeta + hh * kC;
+    const float* cum = M + kMCum + gofs2 + hh * kC;
+    const float* bet = M + kMBeta + gofs2 + hh * kC;
     const float* coef = M + kMCoef + hh * 64;
 #pragma unroll
     for (int t = 0; t < kC; ++t) {
@@ -337,13 +364,13 @@ __device__ __forceinline__ void solve_column(const float (&red)[WQ ? 2 * TP : TP
 // Pass A, a barrier of the tile's group (its coefficients are then in place),
 // and the column recurrence.
 template <int TP, bool WQ>
-__device__ __forceinline__ void pass_and_solve(const float* tile, const float* X, const float* M, int hh, int col0,
+__device__ __forceinline__ void pass_and_solve(const float* tile, const float* X, const float* M, int gofs2, int hh, int col0,
                                                int rb, int tc, const float (&v)[kC], float (&d)[kC],
                                                float (&o)[kC]) {
     float red[WQ ? 2 * TP : TP];
     pass_a<WQ ? 2 * TP : TP>(tile, X, col0, rb, red);
     named_barrier(1 + hh, kS);
-    solve_column<TP, WQ>(red, M, hh, tc, v, d, o);
+    solve_column<TP, WQ>(red, M, gofs2, hh, tc, v, d, o);
 }
 
 // The rank-tc update of the thread's 32 x 4 block: S = A_{tc-1} S_0 + sum_s k_s e_s^T,
@@ -354,11 +381,11 @@ __device__ __forceinline__ void pass_and_solve(const float* tile, const float* X
 constexpr int kToSmem = 0, kToHbm = 1, kDiscard = 2;
 
 template <int TP>
-__device__ __forceinline__ void update_tile(float* tile, const float* X, const float* M, int hh, int col0, int rb,
+__device__ __forceinline__ void update_tile(float* tile, const float* X, const float* M, int gofs2, int hh, int col0, int rb,
                                             int qd, int tc, const float (&d)[kC], int dst, float* gtile) {
     static_assert(TP % 2 == 0, "k is read in pairs");
     constexpr int NP = TP / 2;
-    const float* gam = M + kMGam + hh * kC * kC;  // gam[s * kC + t] = G(s, t)
+    const float* gam = M + kMGam + gofs2 + hh * kC * kC;  // gam[s * kC + t] = G(s, t)
     float e[TP];
 #pragma unroll
     for (int s = 0; s < TP; ++s) e[s] = (s < tc) ? gam[s * kC + (tc - 1)] * d[s] : 0.0f;
@@ -370,7 +397,7 @@ __device__ __forceinline__ void update_tile(float* tile, const float* X, const f
         for (int m = 0; m < NP; ++m)
             E[c][m] = make_float2(__shfl_sync(0xffffffffu, e[2 * m], (c << 3) | qd),
                                   __shfl_sync(0xffffffffu, e[2 * m + 1], (c << 3) | qd));
-    const float al = M[kMCum + hh * kC + tc - 1];
+    const float al = M[kMCum + gofs2 + hh * kC + tc - 1];
 #pragma unroll 2
     for (int r = 0; r < 32; ++r) {
         const int i = 4 * r + rb;
@@ -424,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
     float* X = reinterpret_cast<float*>(smem + kOffX);
     float* M = reinterpret_cast<float*>(smem + kOffMisc);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -456,6 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -492,10 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
     }
 
     uint32_t tile_par = 0, stage_par = 0;
+    bool break_out = false;  // (uniform) a wait gave up: leave the unit loop
     bool failed = false;
     bool give_up = (p.flags & kTestGiveUp) != 0;  // the first tile wait gives up (tests this path)
 
     int n_carry = valid_len(p, x.b);  // this unit's token count, read a unit ahead
+    uint32_t chunk_no = 0;            // chunks done: their parity picks the gate tables
     for (long long u = u_begin; u < u_end; ++u) {
         const bool has_next = u + 1 < u_end;
         const Unit xn = has_next ? next_unit(p, x) : x;
@@ -508,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
         for (int c0 = 0;; c0 += kC) {
             const int tc = max(0, min(kC, n - c0));
             const bool last_chunk = c0 + kC >= n;
+            const int gofs2 = (chunk_no++ & 1) ? kMGate2 - kMBeta : 0;  // this chunk's gate tables
             const size_t row0 = static_cast<size_t>(x.bl) * p.T + c0;  // (b, l, token c0) row index
 
             // ---- early loads: z for y, the norm weight
@@ -522,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             if (write_y && tc > 0) nw = __ldg(p.ssm_norm + static_cast<size_t>(x.l) * kS + scol);
 
             // ---- this chunk's inputs
-            if (mbar_wait_bounded(stage_bar, stage_par)) {
+            if (wait_or_abort(stage_bar, stage_par, abort_flag)) {
                 stage_par ^= 1u;
                 stage_pending = false;
             } else {
@@ -588,19 +620,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                     gam[r] = ar;
                 }
                 if (lane < kGroup * kC && gt < tc) {
-                    M[kMBeta + gh * kC + gt] = bt;
-                    M[kMCum + gh * kC + gt] = cum;
+                    M[kMBeta + gofs2 + gh * kC + gt] = bt;
+                    M[kMCum + gofs2 + gh * kC + gt] = cum;
                     float gp = 1.f;  // G(s, t) = a_{s+1} ... a_t, for s = t down to 0
 #pragma unroll
                     for (int s = kC - 1; s >= 0; --s) {
                         if (s <= gt) {
-                            M[kMGam + (gh * kC + s) * kC + gt] = gp;
+                            M[kMGam + gofs2 + (gh * kC + s) * kC + gt] = gp;
                             gp *= gam[s];
                         }
                     }
                 }
             }
-            __syncthreads();  // (A) the chunk's inputs have been read; sums of squares and gates are in place
+            // (A) the chunk's inputs have been read; sums of squares and gates are in place. Every group has
+            // finished the chunk before (no barrier follows a chunk): a wait of it that gave up stops the CTA.
+            if (__syncthreads_or(failed ? 1 : 0)) break_out = true;
+            if (break_out) break;
 
             // ---- q^ and k^ (normalised; q scaled) into X; the k warps keep k^ for the Gram matrices
             const int tp = (tc + 1) & ~1;
@@ -666,15 +701,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                 const float tot = M[kMGram + gtid] + M[kMGram + 64 + gtid] + M[kMGram + 128 + gtid] +
                                   M[kMGram + 192 + gtid];
                 const bool in = s < tc && t < tc;
-                const float gm = (s < t) ? M[kMGam + (hh * kC + s) * kC + t] : M[kMGam + (hh * kC + t) * kC + s];
+                const float gm = (s < t) ? M[kMGam + gofs2 + (hh * kC + s) * kC + t]
+                                         : M[kMGam + gofs2 + (hh * kC + t) * kC + s];
                 M[kMCoef + hh * 64 + gtid] = in ? gm * tot : 0.0f;
             }
             if (c0 == 0 && n > 0 && !failed) {
-                if (!give_up && mbar_wait_bounded(my_bar, tile_par)) {
+                if (!give_up && wait_or_abort(my_bar, tile_par, abort_flag)) {
                     tile_par ^= 1u;
                     tile_pending = false;
                 } else {
                     failed = true;
+                    *abort_flag = 1;  // the other groups' next waits return at once
                 }
                 give_up = false;
             }
@@ -703,22 +740,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             if (tc > 0 && warp_ok) {
                 if (write_y) {
                     if (tc <= 2)
-                        pass_and_solve<2, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<2, true>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else if (tc <= 4)
-                        pass_and_solve<4, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<4, true>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else if (tc <= 6)
-                        pass_and_solve<6, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<6, true>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else
-                        pass_and_solve<8, true>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<8, true>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                 } else {  // no y: only S^T k is needed
                     if (tc <= 2)
-                        pass_and_solve<2, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<2, false>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else if (tc <= 4)
-                        pass_and_solve<4, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<4, false>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else if (tc <= 6)
-                        pass_and_solve<6, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<6, false>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                     else
-                        pass_and_solve<8, false>(my_tile, X, M, hh, col0, rb, tc, ov, d, o);
+                        pass_and_solve<8, false>(my_tile, X, M, gofs2, hh, col0, rb, tc, ov, d, o);
                 }
             } else {
                 named_barrier(1 + hh, kS);
@@ -778,13 +815,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
             if (tc > 0 && warp_ok && dst != kDiscard) {
                 float* gtile = p.state + (static_cast<size_t>(x.bl) * kVHeads + x.g * kGroup + hh) * kTile;
                 if (tc <= 2)
-                    update_tile<2>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                    update_tile<2>(my_tile, X, M, gofs2, hh, col0, rb, qd, tc, d, dst, gtile);
                 else if (tc <= 4)
-                    update_tile<4>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                    update_tile<4>(my_tile, X, M, gofs2, hh, col0, rb, qd, tc, d, dst, gtile);
                 else if (tc <= 6)
-                    update_tile<6>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                    update_tile<6>(my_tile, X, M, gofs2, hh, col0, rb, qd, tc, d, dst, gtile);
                 else
-                    update_tile<8>(my_tile, X, M, hh, col0, rb, qd, tc, d, dst, gtile);
+                    update_tile<8>(my_tile, X, M, gofs2, hh, col0, rb, qd, tc, d, dst, gtile);
             }
             fence_proxy_async_smem();  // the slot's reads come before the refill's writes
             const bool group_failed = named_barrier_or(1 + hh, kS, failed);
@@ -796,17 +833,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                 }
             }
 
-            if (__syncthreads_or(failed ? 1 : 0)) {
-                // A wait gave up: record it, let every copy still in flight land (bounded), stop.
-                if (tid == 0) atomicOr(&g_chunk_error, kErrWaitTimeout);
-                if (warp == kIssueWarp && lane == 0 && stage_pending) (void)mbar_wait_bounded(stage_bar, stage_par);
-                if (group_leader && tile_pending) (void)mbar_wait_bounded(my_bar, tile_par);
-                return;
-            }
             if (last_chunk) break;
         }
+        if (break_out) break;
         x = xn;
         n_carry = n_next;
+    }
+    if (__syncthreads_or(failed ? 1 : 0)) {
+        // A wait gave up: record it, let every copy still in flight land (bounded), stop.
+        if (tid == 0) atomicOr(&g_chunk_error, kErrWaitTimeout);
+        if (warp == kIssueWarp && lane == 0 && stage_pending) (void)mbar_wait_bounded(stage_bar, stage_par);
+        if (group_leader && tile_pending) (void)mbar_wait_bounded(my_bar, tile_par);
     }
 }
 
