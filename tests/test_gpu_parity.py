@@ -80,6 +80,24 @@ FULL = {
 }
 
 
+def test_multi_chunk_window_at_full_layer_count(g):
+    """A 16-token window (two 8-token chunks on the shared-memory kernel) over 16 sequences and all
+    36 layers, in the launch configuration of the benchmarked windows, on sampled slices."""
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=16, T=16)
+    dev = torch.device("cuda:0")
+    t = W.device_inputs(w, dev, threads=16)
+    y = torch.full(t["z"].shape, float("nan"), device=dev)
+    U.run_step(g, t, y=y)
+    torch.cuda.synchronize()
+    for b, l in [(0, 0), (15, 35), (7, 18), (11, 3)]:
+        ry, rs, rc = U.oracle_slice(w, b, l)
+        gy, gs = y[b, l].cpu().numpy(), t["state"][b, l].cpu().numpy()
+        assert U.y_errors(gy, ry) <= U.TOL, (b, l)
+        assert U.state_errors(gs, rs) <= U.TOL, (b, l)
+        assert np.array_equal(t["conv_state"][b, l].cpu().numpy(), rc), (b, l)
+    assert torch.isfinite(t["state"]).all()
+
+
 @pytest.mark.parametrize("name", list(FULL))
 def test_full_size_workloads_on_sampled_slices(g, name):
     w = W.WORKLOADS[name]
