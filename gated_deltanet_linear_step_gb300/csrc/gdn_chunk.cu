@@ -40,14 +40,14 @@
 // Overlap. Shared memory holds the three tiles, the chunk's raw qkv rows (with
 // the heads' alpha, beta, dt and ssm_a) and the normalised q and k (separate
 // from the raw rows), so the next chunk's inputs (or the next unit's first
-// ones) are requested, by a v-only warp, once the conv has read the current
-// ones and the unit's tiles have landed (the copy engine then has no tile
-// refill ahead of them), and arrive while the tiles are worked on. Pass A and
+// ones) are requested, by a v-only warp, after the chunk's preparation (the
+// copy engine then has little of the tile refills left ahead of them), and
+// arrive while the tiles are worked on. Pass A and
 // the update run on the packed two-wide FMA. A unit's last update writes the new
 // tile straight to HBM with streaming stores, so the slot is free once the
 // group has read it: its leader then requests the next unit's tile, which an
 // L2 prefetch issued with the next unit's inputs (about half a unit earlier,
-// once this unit's tiles have landed) has brought into L2; a prefetch a whole
+// after this unit's preparation) has brought into L2; a prefetch a whole
 // unit ahead measured slower than none, its lines evicted before use. The next
 // unit's conv histories and taps are loaded into registers a unit ahead. No CTA
 // barrier closes a chunk: a group that has finished its update starts the next
@@ -705,19 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                                          : M[kMGam + gofs2 + (hh * kC + t) * kC + s];
                 M[kMCoef + hh * 64 + gtid] = in ? gm * tot : 0.0f;
             }
-            if (c0 == 0 && n > 0 && !failed) {
-                if (!give_up && wait_or_abort(my_bar, tile_par, abort_flag)) {
-                    tile_par ^= 1u;
-                    tile_pending = false;
-                } else {
-                    failed = true;
-                    *abort_flag = 1;  // the other groups' next waits return at once
-                }
-                give_up = false;
-            }
             // ---- the staging area (free since barrier A) takes the next chunk's inputs, or the next unit's
-            //      first ones: requested once the tile has landed, when the copy engine has no tile
-            //      refill ahead of them (requested at barrier A they took a warp 1.4 us to issue)
+            //      first ones: requested after the preparation, when the copy engine has little of the
+            //      tile refills left ahead of them (requested at barrier A they took a warp 1.4 us to issue)
             if (warp == kIssueWarp && !failed) {
                 if (!last_chunk) {
                     fence_proxy_async_smem();
@@ -732,6 +722,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_chunk_kernel(const __grid_con
                 }
             }
 
+            if (c0 == 0 && n > 0 && !failed) {
+                if (!give_up && wait_or_abort(my_bar, tile_par, abort_flag)) {
+                    tile_par ^= 1u;
+                    tile_pending = false;
+                } else {
+                    failed = true;
+                    *abort_flag = 1;  // the other groups' next waits return at once
+                }
+                give_up = false;
+            }
             // ---- pass A, then (after the group's coefficients are in place) the column recurrence
             const bool warp_ok = !__any_sync(0xffffffffu, failed);
             float d[kC], o[kC];
