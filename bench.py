@@ -169,16 +169,23 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# The library's dispatch: windows of 2-24 tokens run the kernel with the tiles in shared memory, 25
-# or more the tensor-core chunk kernel; the register window kernel serves only builds with other
-# thresholds.
+# The library's dispatch: one token runs the single-token kernel unless the launch has no more units
+# (sequence, layer, k head) than fill the SMs at one 3-CTA cluster per unit, which run the register
+# kernel; windows of 2-24 tokens run the kernel with the tiles in shared memory, 25 or more the
+# tensor-core chunk kernel (the register kernel takes windows only in builds with other thresholds).
 CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
 
 
-def kernel_name(T: int) -> str:
-    """The kernel a call with T tokens runs (the library's dispatch)."""
+def small_single_token(units: int | None, sms: int | None) -> bool:
+    """A single-token launch of `units` units that runs the register kernel on a GPU of `sms` SMs."""
+    return units is not None and sms is not None and 3 * units <= sms
+
+
+def kernel_name(T: int, units: int | None = None, sms: int | None = None) -> str:
+    """The kernel a call with T tokens over `units` units runs on `sms` SMs (the library's dispatch;
+    without the two counts, a launch larger than the GPU)."""
     if T == 1:
-        return "gdn_decode_t1_kernel"
+        return "gdn_window_kernel" if small_single_token(units, sms) else "gdn_decode_t1_kernel"
     if T <= CHUNK_MAX_T:
         return "gdn_chunk_kernel"
     if T < TC_MIN_T:
@@ -186,9 +193,11 @@ def kernel_name(T: int) -> str:
     return "gdn_window_tc_kernel"
 
 
-def kernel_sources(T: int) -> list:
-    """The sources of the kernel a call with T tokens runs."""
-    if T == 1:
+def kernel_sources(T: int, units: int | None = None, sms: int | None = None) -> list:
+    """The sources of the kernel a call with T tokens runs (arguments as for `kernel_name`)."""
+    if T == 1 and small_single_token(units, sms):
+        names = ("gdn_step.cu", "gdn_device.cuh")
+    elif T == 1:
         names = ("gdn_decode_t1.cu", "gdn_device.cuh")
     elif T <= CHUNK_MAX_T:
         names = ("gdn_chunk.cu", "gdn_device.cuh")
@@ -216,11 +225,11 @@ def tc_mma_flops(w: W.Workload, lens) -> float:
     return total * w.L * 16
 
 
-def committed_traffic(workload: str, T: int):
+def committed_traffic(workload: str, T: int, units: int | None = None, sms: int | None = None):
     """Per-launch DRAM bytes from a committed ncu summary (``profiles/*traffic*.txt``) taken on this
     workload and on the kernel source as it stands (its sha256 must match), else None."""
     digest = hashlib.sha256()
-    for path in kernel_sources(T):
+    for path in kernel_sources(T, units, sms):
         digest.update(open(path, "rb").read())
     want = digest.hexdigest()
     if not os.path.isdir(PROFILES):
@@ -496,6 +505,7 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
     y = torch.empty(t["z"].shape, device=dev)
     step = make_step(g, t, y)
     stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -568,14 +578,14 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
         torch.cuda.synchronize(dev)
         ms1 = a.elapsed_time(b) / steps
         singles = {"calls_per_step": w.T, "ms_per_step": ms1, "value": valid_tokens(w, lens) / (ms1 / 1e3),
-                   "kernel": kernel_name(1)}
+                   "kernel": kernel_name(1, w.B * w.L * 16, sms)}
         del graph, calls, y1
     assert g.gdn_read_device_error(device=dev) == 0, f"a kernel reported a device error on {name}"
     updates = valid_tokens(w, lens)
-    roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T))
+    roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T, w.B * w.L * 16, sms))
     out = {"workload": name, "B": w.B, "L": w.L, "T": w.T, "steps": steps, "ms_per_step": ms,
            "value": updates / (ms / 1e3), "unit": UNIT,
-           "kernel": kernel_name(w.T), "l2": l2, "roofline": roof}
+           "kernel": kernel_name(w.T, w.B * w.L * 16, sms), "l2": l2, "roofline": roof}
     if singles is not None:
         out["as_single_token_calls"] = singles
     if working <= 2 * L2_BYTES:
@@ -674,7 +684,9 @@ def run_gdn(args, w_global, world, rank, local):
         del pipe, host, y_host
 
     mean_launch_s = float(np.mean(launch_ms)) / 1000.0
-    roofline = roofline_of(w, lens, mean_launch_s, committed_traffic(w_global.name, w.T) if world == 1 else None)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    traffic = committed_traffic(w_global.name, w.T, w.B * w.L * 16, sms) if world == 1 else None
+    roofline = roofline_of(w, lens, mean_launch_s, traffic)
     del t, y, step
     torch.cuda.empty_cache()
 
@@ -948,11 +960,33 @@ def run_verify(args, w):
     n_keep = torch.from_numpy(keep).to(dev)
     y = torch.empty(t["z"].shape, device=dev)
 
-    def step():
+    def window():
         g.gdn_verify_window(t["qkv"], t["z"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"], t["ssm_norm"],
                             t["conv_state"], t["state"], y, seq_len=seq_len)
+
+    def commit():
         g.gdn_verify_commit(t["qkv"], t["alpha"], t["beta"], t["dt"], t["ssm_a"], t["conv_w"], t["conv_state"],
                             t["state"], n_keep)
+
+    def step():
+        window()
+        commit()
+
+    def alone_ms(fn):
+        # one call kind on its own, the same number of calls in a captured graph (the commit repeated
+        # on the state it advanced: the bytes and the work do not depend on the values)
+        for _ in range(3):
+            fn()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for _ in range(args.steps):
+                fn()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record()
+        gr.replay()
+        eb.record()
+        torch.cuda.synchronize(dev)
+        return ea.elapsed_time(eb) / args.steps
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -969,8 +1003,9 @@ def run_verify(args, w):
         b.record()
         torch.cuda.synchronize(dev)
         clocks.mark_end()
-    assert g.gdn_read_device_error(device=dev) == 0, "a kernel reported a device error"
     ms = a.elapsed_time(b) / args.steps
+    window_ms, commit_ms = alone_ms(window), alone_ms(commit)
+    assert g.gdn_read_device_error(device=dev) == 0, "a kernel reported a device error"
     drafted = int(lens.sum()) * L
     kept = int(keep.sum()) * L
     tile = 48 * 128 * 128 * 4
@@ -991,11 +1026,14 @@ def run_verify(args, w):
         "config": {"workload": w.name, "B": B, "L": L, "T": T, "drafted_per_layer": int(lens.sum()),
                    "kept_per_layer": int(keep.sum()),
                    "n_keep": "per sequence from U{0..len[b]}, numpy default_rng(seed + 1)",
-                   "timing": f"{args.steps} x (gdn_verify_window + gdn_verify_commit) in one captured CUDA graph"},
+                   "timing": f"{args.steps} x (gdn_verify_window + gdn_verify_commit) in one captured CUDA graph; "
+                             "then each call alone, the same number of times in its own graph"},
         "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_kind": peak_kind, "bytes_per_step": window_bytes + commit_bytes,
-                     "window_bytes": window_bytes, "commit_bytes": commit_bytes},
+                     "window_bytes": window_bytes, "commit_bytes": commit_bytes,
+                     "window_ms_alone": window_ms, "window_frac": window_bytes / (window_ms / 1e3) / 1e9 / peak,
+                     "commit_ms_alone": commit_ms, "commit_frac": commit_bytes / (commit_ms / 1e3) / 1e9 / peak},
     }), flush=True)
 
 

@@ -1,5 +1,6 @@
 // gdn_step.cu - the fused Gated DeltaNet decode step for GB300 (sm_103a),
-// multi-token form (T > 1), plus the dispatch of every call.
+// register-resident form (windows, and single-token launches too small to fill
+// the SMs), plus the dispatch of every call.
 //
 // One persistent kernel computes, for every (sequence b, layer l, token t), the
 // whole recurrent-mixer step listed in the header comment of the Winery-Strata
@@ -43,7 +44,8 @@
 // computes and writes nothing but still takes part in every cluster barrier,
 // waits (bounded) for its own copies, sets the device error word and returns.
 //
-// The single-token call runs gdn_decode_t1.cu instead.
+// A single-token call runs gdn_decode_t1.cu instead unless it is that small
+// (the dispatch at the end of this file).
 
 #include <mutex>
 
@@ -549,6 +551,7 @@ std::mutex g_mutex;
 struct DeviceSetup {
     bool ready = false;
     int clusters = 0;
+    int sms = 0;
 };
 DeviceSetup g_setup[64];
 
@@ -567,7 +570,7 @@ cudaLaunchConfig_t window_config(unsigned grid, cudaStream_t stream, cudaLaunchA
     return cfg;
 }
 
-cudaError_t device_setup(int* clusters) {
+cudaError_t device_setup(int* clusters, int* sms_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -593,21 +596,30 @@ cudaError_t device_setup(int* clusters) {
             n = (2 * sms) / kGroup;  // two CTAs per SM
         }
         d.clusters = n;
+        d.sms = sms;
         d.ready = true;
     }
     *clusters = d.clusters;
+    *sms_out = d.sms;
     return cudaSuccess;
 }
 
 }  // namespace
 
-// Windows of up to GDN_CHUNK_MAX_T tokens run the kernel with the tiles resident
-// in shared memory (gdn_chunk.cu, chunks of 8 tokens); windows of GDN_TC_MIN_T
-// tokens or more run the tensor-core chunk kernel (gdn_window_tc.cu); any others
-// gdn_window_kernel. The defaults are the measured crossovers (16 sequences x 36
-// layers): the chunked kernel is the fastest up to 24 tokens, the tensor-core
-// kernel from there on, so no window falls to gdn_window_kernel unless a build
-// sets other thresholds (as timing comparisons do).
+// One token runs the single-token kernel (gdn_decode_t1.cu: one CTA per SM, a
+// unit's three tiles on one SM), unless the launch has no more units than fill
+// the SMs at one CTA per v head: such a small launch (1 x 1 x 1 takes 16 units)
+// runs gdn_window_kernel, whose 3-CTA clusters spread a unit's three tiles over
+// three SMs (measured at 1 sequence x 1 layer: 10.8 us per call after an
+// L2-evicting write against 15.1 us, 5.4 us back to back against 10.8 us; at
+// 4 x 2 with 384 CTAs it was slower). Windows of up to GDN_CHUNK_MAX_T tokens
+// run the kernel with the tiles resident in shared memory (gdn_chunk.cu, chunks
+// of 8 tokens); windows of GDN_TC_MIN_T tokens or more run the tensor-core chunk
+// kernel (gdn_window_tc.cu); any others gdn_window_kernel. The defaults are the
+// measured crossovers (16 sequences x 36 layers): the chunked kernel is the
+// fastest up to 24 tokens, the tensor-core kernel from there on, so no window
+// falls to gdn_window_kernel unless a build sets other thresholds (as timing
+// comparisons do).
 #ifndef GDN_CHUNK_MAX_T
 #define GDN_CHUNK_MAX_T 24
 #endif
@@ -616,11 +628,18 @@ cudaError_t device_setup(int* clusters) {
 #endif
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
-    if (a.T == 1) return launch_decode_t1(a, stream);
-    if (a.T <= GDN_CHUNK_MAX_T) return launch_decode_chunked(a, stream);
-    if (a.T >= GDN_TC_MIN_T) return launch_decode_window_tc(a, stream);
-    int clusters = 0;
-    cudaError_t e = device_setup(&clusters);
+    const long long units = static_cast<long long>(a.B) * a.L * kKHeads;
+    int clusters = 0, sms = 0;
+    if (a.T == 1) {
+        cudaError_t e = device_setup(&clusters, &sms);
+        if (e != cudaSuccess) return e;
+        if (units * kGroup > sms) return launch_decode_t1(a, stream);
+    } else if (a.T <= GDN_CHUNK_MAX_T) {
+        return launch_decode_chunked(a, stream);
+    } else if (a.T >= GDN_TC_MIN_T) {
+        return launch_decode_window_tc(a, stream);
+    }
+    cudaError_t e = device_setup(&clusters, &sms);
     if (e != cudaSuccess) return e;
     Params p;
     p.qkv = a.qkv;
@@ -639,7 +658,7 @@ cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     p.L = a.L;
     p.T = a.T;
     p.flags = a.flags;
-    p.n_units = static_cast<long long>(a.B) * a.L * kKHeads;
+    p.n_units = units;
     const long long n_cl = p.n_units < clusters ? p.n_units : clusters;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = window_config(static_cast<unsigned>(n_cl * kGroup), stream, attr);

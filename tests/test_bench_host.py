@@ -75,6 +75,7 @@ def test_kernel_sources_follow_the_library_dispatch():
     import bench
 
     names = lambda T: [os.path.basename(p) for p in bench.kernel_sources(T)]
+    names_small = lambda units, sms: [os.path.basename(p) for p in bench.kernel_sources(1, units, sms)]
     assert names(1)[0] == "gdn_decode_t1.cu"
     assert names(2)[0] == names(bench.CHUNK_MAX_T)[0] == "gdn_chunk.cu"
     assert names(bench.TC_MIN_T)[0] == names(1024)[0] == "gdn_window_tc.cu"
@@ -92,11 +93,18 @@ def test_kernel_sources_follow_the_library_dispatch():
     for T in (1, 2, bench.TC_MIN_T):
         kernel_src = open(bench.kernel_sources(T)[0]).read()
         assert "void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
+    # a single-token launch with no more units than fill the SMs at one 3-CTA cluster per unit runs the
+    # register kernel (1 x 1 x 1: 16 units on 48 CTAs); one CTA more than the SMs, the single-token kernel
+    assert bench.kernel_name(1, 16, 152) == "gdn_window_kernel" and names_small(16, 152)[0] == "gdn_step.cu"
+    assert bench.kernel_name(1, 50, 152) == "gdn_window_kernel"
+    assert bench.kernel_name(1, 51, 152) == "gdn_decode_t1_kernel" and names_small(51, 152)[0] == "gdn_decode_t1.cu"
+    assert bench.kernel_name(2, 16, 152) == "gdn_chunk_kernel"
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
     assert f"#define GDN_CHUNK_MAX_T {bench.CHUNK_MAX_T}" in src
     assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
+    assert "if (units * kGroup > sms) return launch_decode_t1(a, stream);" in src
 
 
 def test_tensor_core_flop_count():

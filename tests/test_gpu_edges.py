@@ -31,11 +31,11 @@ def test_longest_window_matches_oracle(cuda_device):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("T", [1, 5, 40])
-def test_negative_and_all_zero_lengths_change_nothing(cuda_device, T):
+@pytest.mark.parametrize("L,T", [(2, 1), (1, 1), (2, 5), (2, 40)])
+def test_negative_and_all_zero_lengths_change_nothing(cuda_device, L, T):
     import gated_deltanet_linear_step_gb300 as g
 
-    w, h = _case(3, 2, T)
+    w, h = _case(3, L, T)
     t = U.to_device(h, cuda_device)
     for lens in ([-7, 0, -1], [0, 0, 0]):
         t["seq_len"] = torch.tensor(lens, dtype=torch.int32, device=cuda_device)
@@ -48,23 +48,25 @@ def test_negative_and_all_zero_lengths_change_nothing(cuda_device, T):
         assert torch.equal(t["conv_state"].cpu(), torch.from_numpy(h["conv_state"]))
 
 
-def test_single_token_call_with_lengths(cuda_device):
-    """T = 1 runs the batched-decode kernel; a length of 0 leaves its sequence untouched and the
-    others match the oracle."""
+@pytest.mark.parametrize("B,L", [(4, 2), (3, 1)])
+def test_single_token_call_with_lengths(cuda_device, B, L):
+    """T = 1 runs the batched-decode kernel (4 x 2: 128 units) or, on a launch small enough to give
+    each v head its own SM (3 x 1: 48 units on 144 CTAs), the 3-CTA cluster kernel; a length of 0
+    leaves its sequence untouched and the others match the oracle."""
     import gated_deltanet_linear_step_gb300 as g
 
-    w, h = _case(4, 2, 1, name="decode_b64_l36_t1")
-    h["seq_len"] = np.array([1, 0, 1, 0], np.int32)
+    w, h = _case(B, L, 1, name="decode_b64_l36_t1")
+    h["seq_len"] = np.array([1, 0, 1, 0][:B], np.int32)
     t = U.to_device(h, cuda_device)
     sentinel = torch.full(t["z"].shape, -3.0, device=cuda_device)
     y = U.run_step(g, t, y=sentinel.clone())
     assert g.gdn_read_device_error() == 0
     ry, rs, rc = U.oracle_full(h)
     gy = y.cpu().numpy()
-    for b in (1, 3):
+    for b in range(1, B, 2):
         assert np.all(gy[b] == -3.0)
         assert np.array_equal(t["state"][b].cpu().numpy(), h["state"][b])
-    keep = [0, 2]
+    keep = list(range(0, B, 2))
     assert U.y_errors(gy[keep], ry[keep]) <= U.TOL
     assert U.state_errors(t["state"].cpu().numpy(), rs) <= U.TOL
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)

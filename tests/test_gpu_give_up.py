@@ -20,12 +20,13 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [1, 4, 12, 48],
-                         ids=["single_token", "one_chunk_window", "multi_chunk_window", "tensor_core_window"])
-def test_a_wait_that_gives_up_drains_reports_and_leaves_the_context_usable(cuda_device, T):
+@pytest.mark.parametrize("B,L,T", [(4, 3, 1), (1, 1, 1), (4, 3, 4), (4, 3, 12), (4, 3, 48)],
+                         ids=["single_token", "single_token_small_launch", "one_chunk_window", "multi_chunk_window",
+                              "tensor_core_window"])
+def test_a_wait_that_gives_up_drains_reports_and_leaves_the_context_usable(cuda_device, B, L, T):
     import gated_deltanet_linear_step_gb300 as g
 
-    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=4, L=3, T=T)
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
     h = W.host_inputs(w, threads=8)
     # an ordinary call first, so module loading is not part of the timed call
     warm = U.to_device(h, cuda_device)
