@@ -169,16 +169,21 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# The library's dispatch: one token runs the single-token kernel unless the launch has no more units
-# (sequence, layer, k head) than fill the SMs at one 3-CTA cluster per unit, which run the register
-# kernel; windows of 2-24 tokens run the kernel with the tiles in shared memory, 25 or more the
-# tensor-core chunk kernel (the register kernel takes windows only in builds with other thresholds).
+# The library's dispatch: one token runs the single-token kernel, or the register kernel's 3-CTA
+# clusters for launches of up to 6 units (sequence, layer, k head) per SM whose rounds of one unit per
+# cluster cost no more (measured rounds: 7.1 us against 10.7 us); windows of 2-24 tokens run the
+# kernel with the tiles in shared memory, 25 or more the tensor-core chunk kernel (the register kernel
+# takes windows only in builds with other thresholds).
 CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
 
 
 def small_single_token(units: int | None, sms: int | None) -> bool:
-    """A single-token launch of `units` units that runs the register kernel on a GPU of `sms` SMs."""
-    return units is not None and sms is not None and 3 * units <= sms
+    """A single-token launch of `units` units that runs the register kernel on a GPU of `sms` SMs:
+    at most 6 units per SM, and 2 ceil(units / C) <= 3 ceil(units / sms), C = 2 sms // 3 clusters."""
+    if units is None or sms is None or units > 6 * sms:
+        return False
+    c = 2 * sms // 3
+    return 2 * -(-units // c) <= 3 * -(-units // sms)
 
 
 def kernel_name(T: int, units: int | None = None, sms: int | None = None) -> str:

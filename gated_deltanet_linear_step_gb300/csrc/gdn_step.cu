@@ -607,12 +607,16 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 }  // namespace
 
 // One token runs the single-token kernel (gdn_decode_t1.cu: one CTA per SM, a
-// unit's three tiles on one SM), unless the launch has no more units than fill
-// the SMs at one CTA per v head: such a small launch (1 x 1 x 1 takes 16 units)
-// runs gdn_window_kernel, whose 3-CTA clusters spread a unit's three tiles over
-// three SMs (measured at 1 sequence x 1 layer: 10.8 us per call after an
-// L2-evicting write against 15.1 us, 5.4 us back to back against 10.8 us; at
-// 4 x 2 with 384 CTAs it was slower). Windows of up to GDN_CHUNK_MAX_T tokens
+// unit's three tiles on one SM, units taken in rounds of one per SM) or, for
+// launches of up to 6 units per SM, gdn_window_kernel (3-CTA clusters, one CTA
+// per tile, two CTAs per SM: rounds of one unit per cluster, 2/3 as many units
+// as SMs) when its rounds cost no more (single_token_on_clusters). Measured per
+// round at these sizes: about 10.7 us for the single-token kernel, 7.1 us for the
+// clusters, so the clusters take a launch when 2 ceil(u / C) <= 3 ceil(u / S);
+// 1 x 1 x 1 (16 units): 0.0054 against 0.0108 ms back to back; B x 1 x 1 with B =
+// 4, 10, 24, 48: 0.0078 / 0.0137 / 0.0254 / 0.0617 against 0.0113 / 0.0206 /
+// 0.0308 / 0.0664 ms; B = 7, 8 (one round against two) and 64 or more they lose.
+// Windows of up to GDN_CHUNK_MAX_T tokens
 // run the kernel with the tiles resident in shared memory (gdn_chunk.cu, chunks
 // of 8 tokens); windows of GDN_TC_MIN_T tokens or more run the tensor-core chunk
 // kernel (gdn_window_tc.cu); any others gdn_window_kernel. The defaults are the
@@ -627,13 +631,20 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 #define GDN_TC_MIN_T 25
 #endif
 
+// Whether a single-token launch of `units` units runs on the 3-CTA clusters (see above).
+bool single_token_on_clusters(long long units, int sms) {
+    if (units > 6LL * sms) return false;
+    const long long c = 2LL * sms / kGroup;  // clusters at two CTAs per SM
+    return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);
+}
+
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long units = static_cast<long long>(a.B) * a.L * kKHeads;
     int clusters = 0, sms = 0;
     if (a.T == 1) {
         cudaError_t e = device_setup(&clusters, &sms);
         if (e != cudaSuccess) return e;
-        if (units * kGroup > sms) return launch_decode_t1(a, stream);
+        if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);
     } else if (a.T <= GDN_CHUNK_MAX_T) {
         return launch_decode_chunked(a, stream);
     } else if (a.T >= GDN_TC_MIN_T) {

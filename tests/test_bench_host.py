@@ -93,18 +93,23 @@ def test_kernel_sources_follow_the_library_dispatch():
     for T in (1, 2, bench.TC_MIN_T):
         kernel_src = open(bench.kernel_sources(T)[0]).read()
         assert "void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
-    # a single-token launch with no more units than fill the SMs at one 3-CTA cluster per unit runs the
-    # register kernel (1 x 1 x 1: 16 units on 48 CTAs); one CTA more than the SMs, the single-token kernel
-    assert bench.kernel_name(1, 16, 152) == "gdn_window_kernel" and names_small(16, 152)[0] == "gdn_step.cu"
-    assert bench.kernel_name(1, 50, 152) == "gdn_window_kernel"
-    assert bench.kernel_name(1, 51, 152) == "gdn_decode_t1_kernel" and names_small(51, 152)[0] == "gdn_decode_t1.cu"
+    # single-token launches: the register kernel's 3-CTA clusters where their rounds (101 units on 152
+    # SMs) cost no more than the single-token kernel's (152 units), at 7.1 against 10.7 us a round
+    on_clusters = {16: True, 96: True, 101: True, 102: False, 112: False, 128: False, 152: False, 160: True,
+                   256: True, 384: True, 576: True, 768: True, 909: True, 912: False, 1024: False, 36864: False}
+    for units, want in on_clusters.items():
+        assert bench.small_single_token(units, 152) == want, units
+        assert bench.kernel_name(1, units, 152) == ("gdn_window_kernel" if want else "gdn_decode_t1_kernel")
+    assert names_small(16, 152)[0] == "gdn_step.cu" and names_small(128, 152)[0] == "gdn_decode_t1.cu"
     assert bench.kernel_name(2, 16, 152) == "gdn_chunk_kernel"
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
     assert f"#define GDN_CHUNK_MAX_T {bench.CHUNK_MAX_T}" in src
     assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
-    assert "if (units * kGroup > sms) return launch_decode_t1(a, stream);" in src
+    assert "if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);" in src
+    assert "if (units > 6LL * sms) return false;" in src
+    assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
 
 
 def test_tensor_core_flop_count():

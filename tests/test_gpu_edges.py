@@ -31,7 +31,7 @@ def test_longest_window_matches_oracle(cuda_device):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("L,T", [(2, 1), (1, 1), (2, 5), (2, 40)])
+@pytest.mark.parametrize("L,T", [(3, 1), (1, 1), (2, 5), (2, 40)])  # one token: 3 x 3 single-token kernel, 3 x 1 clusters
 def test_negative_and_all_zero_lengths_change_nothing(cuda_device, L, T):
     import gated_deltanet_linear_step_gb300 as g
 
@@ -50,9 +50,9 @@ def test_negative_and_all_zero_lengths_change_nothing(cuda_device, L, T):
 
 @pytest.mark.parametrize("B,L", [(4, 2), (3, 1)])
 def test_single_token_call_with_lengths(cuda_device, B, L):
-    """T = 1 runs the batched-decode kernel (4 x 2: 128 units) or, on a launch small enough to give
-    each v head its own SM (3 x 1: 48 units on 144 CTAs), the 3-CTA cluster kernel; a length of 0
-    leaves its sequence untouched and the others match the oracle."""
+    """T = 1 runs the batched-decode kernel (4 x 2: 128 units) or, on a smaller launch (3 x 1: 48
+    units, one round of clusters), the 3-CTA cluster kernel; a length of 0 leaves its sequence
+    untouched and the others match the oracle."""
     import gated_deltanet_linear_step_gb300 as g
 
     w, h = _case(B, L, 1, name="decode_b64_l36_t1")
@@ -72,17 +72,18 @@ def test_single_token_call_with_lengths(cuda_device, B, L):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("T,name", [(1, "decode_b64_l36_t1"), (5, "verify_b16_l36_t8_ragged"),
-                                    (20, "verify_b16_l36_t8_ragged"), (40, "verify_b16_l36_t8_ragged")])
+@pytest.mark.parametrize("L,T,name", [(3, 1, "decode_b64_l36_t1"), (1, 1, "decode_b64_l36_t1"),
+                                      (2, 5, "verify_b16_l36_t8_ragged"), (2, 20, "verify_b16_l36_t8_ragged"),
+                                      (2, 40, "verify_b16_l36_t8_ragged")])
 @pytest.mark.parametrize("gate", ["sigmoid", "silu"])
-def test_saturated_activations_match_oracle(cuda_device, T, name, gate):
+def test_saturated_activations_match_oracle(cuda_device, L, T, name, gate):
     """Inputs scaled so that SiLU, sigmoid and softplus see arguments far beyond +-88, where e^-x
     overflows or underflows in fp32: SiLU must go to x or 0, sigmoid to 1 or 0, beta to 0 or 1 and
-    decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel and the three
-    multi-token kernels."""
+    decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel (3 x 3 x 1), the 3-CTA
+    cluster kernel (3 x 1 x 1) and the window kernels."""
     import gated_deltanet_linear_step_gb300 as g
 
-    w, h = _case(3, 2, T, name=name)
+    w, h = _case(3, L, T, name=name)
     for k, f in (("qkv", 120.0), ("conv_state", 120.0), ("z", 150.0), ("alpha", 60.0), ("beta", 60.0)):
         h[k] = (h[k] * np.float32(f)).astype(np.float32)
     t = U.to_device(h, cuda_device)

@@ -29,8 +29,10 @@ def g(cuda_device):
 
 SMALL = [
     ("decode_b1_l1_t1", {}),                         # one token, 16 units: the 3-CTA cluster kernel
-    ("decode_b64_l36_t1", dict(B=1, L=3)),           # one token, 48 units on 144 CTAs: still that kernel
-    ("decode_b64_l36_t1", dict(B=3, L=2)),           # one token, 96 units: the single-token kernel
+    ("decode_b64_l36_t1", dict(B=1, L=3)),           # one token, 48 units: that kernel
+    ("decode_b64_l36_t1", dict(B=3, L=2)),           # one token, 96 units: that kernel
+    ("decode_b64_l36_t1", dict(B=4, L=2)),           # one token, 128 units: the single-token kernel
+    ("decode_b64_l36_t1", dict(B=10, L=1)),          # one token, 160 units: the clusters again, two rounds
     ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=2, L=2)),
     ("verify_b16_l36_t8_ragged", dict(B=6, L=2)),
     ("decode_b1_l36_t64_zero_state", dict(L=2)),
@@ -293,11 +295,11 @@ def test_bad_arguments_raise_and_launch_nothing(g):
     assert torch.equal(t["state"], before) and torch.all(y == 0)
 
 
-@pytest.mark.parametrize("B,L,T", [(3, 2, 1), (1, 2, 1), (3, 2, 4), (3, 2, 12), (3, 2, 40), (3, 2, 70)])
+@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 2, 1), (3, 2, 4), (3, 2, 12), (3, 2, 40), (3, 2, 70)])
 def test_no_y_and_no_state_write_flags_match_the_full_call(g, B, L, T):
     """FLAG_NO_Y gives the full call's state and conv_state bit for bit and writes no y;
-    FLAG_NO_STATE_WRITE gives its y bit for bit and leaves both states untouched. (1 x 2 x 1 is a
-    single-token launch small enough for the 3-CTA cluster kernel.)"""
+    FLAG_NO_STATE_WRITE gives its y bit for bit and leaves both states untouched. (One token: 4 x 2
+    runs the single-token kernel, 1 x 2 the 3-CTA cluster kernel.)"""
     w, h = _small(dict(B=B, L=L, T=T), name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     full = U.to_device(h, dev)
