@@ -541,10 +541,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) gdn_window_kernel(const __grid
         // Copies still in flight land before the CTA leaves (bounded), and so do the stores.
         if (tile_pending) (void)mbar_wait_bounded(tile_bar, tile_par);
         if (z_pending) (void)mbar_wait_bounded(z_bar, z_par);
-        bulk_wait_all();
+        bulk_wait_read();  // the last store has read the slot (its writes land on their own)
         if (failed) atomicOr(&g_device_error, kErrWaitTimeout);
     }
-    cluster_sync();  // the three CTAs of a cluster leave together
+    // No cluster barrier before leaving: no CTA touches another's shared memory, and the three CTAs
+    // of a cluster take the same cluster barriers in the loop, so none is left waiting on one that
+    // has gone.
 }
 
 std::mutex g_mutex;
