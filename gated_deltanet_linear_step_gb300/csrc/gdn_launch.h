@@ -119,8 +119,8 @@ cudaError_t launch_ab_gates(const AbArgs& a, cudaStream_t stream);
 // Reads and clears the alpha/beta kernel's device error word.
 cudaError_t read_ab_error(uint32_t* out);
 
-// Launches the fused decode step on `stream`: the single-token kernel when
-// T == 1, the multi-token kernel otherwise. Returns the launch status.
+// Launches the fused decode step on `stream`, choosing the kernel by T and the
+// launch's size (the dispatch rules are in gdn_step.cu). Returns the launch status.
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream);
 
 // The single-token kernel (gdn_decode_t1.cu); requires a.T == 1.
