@@ -172,8 +172,9 @@ def measured_peaks():
 # The library's dispatch: one token runs the single-token kernel, or the register kernel's 3-CTA
 # clusters for launches of up to 6 units (sequence, layer, k head) per SM whose rounds of one unit per
 # cluster cost no more (measured rounds: 7.1 us against 10.7 us); windows of 2-24 tokens run the
-# kernel with the tiles in shared memory, 25 or more the tensor-core chunk kernel (the register kernel
-# takes windows only in builds with other thresholds).
+# kernel with the tiles in shared memory, or the clusters when all units fit one round of them
+# (units <= 2 SMs / 3); 25 tokens or more the tensor-core chunk kernel (the register kernel takes
+# larger windows only in builds with other thresholds).
 CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
 
 
@@ -186,13 +187,19 @@ def small_single_token(units: int | None, sms: int | None) -> bool:
     return 2 * -(-units // c) <= 3 * -(-units // sms)
 
 
+def small_window(units: int | None, sms: int | None) -> bool:
+    """A window of 2 to CHUNK_MAX_T tokens over `units` units that runs on the 3-CTA clusters: all
+    its units fit one round of them (units <= 2 sms // 3)."""
+    return units is not None and sms is not None and units <= 2 * sms // 3
+
+
 def kernel_name(T: int, units: int | None = None, sms: int | None = None) -> str:
     """The kernel a call with T tokens over `units` units runs on `sms` SMs (the library's dispatch;
     without the two counts, a launch larger than the GPU)."""
     if T == 1:
         return "gdn_window_kernel" if small_single_token(units, sms) else "gdn_decode_t1_kernel"
     if T <= CHUNK_MAX_T:
-        return "gdn_chunk_kernel"
+        return "gdn_window_kernel" if small_window(units, sms) else "gdn_chunk_kernel"
     if T < TC_MIN_T:
         return "gdn_window_kernel"
     return "gdn_window_tc_kernel"
@@ -204,6 +211,8 @@ def kernel_sources(T: int, units: int | None = None, sms: int | None = None) -> 
         names = ("gdn_step.cu", "gdn_device.cuh")
     elif T == 1:
         names = ("gdn_decode_t1.cu", "gdn_device.cuh")
+    elif T <= CHUNK_MAX_T and small_window(units, sms):
+        names = ("gdn_step.cu", "gdn_device.cuh")
     elif T <= CHUNK_MAX_T:
         names = ("gdn_chunk.cu", "gdn_device.cuh")
     elif T < TC_MIN_T:

@@ -618,14 +618,18 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 // 1 x 1 x 1 (16 units): 0.0054 against 0.0108 ms back to back; B x 1 x 1 with B =
 // 4, 10, 24, 48: 0.0078 / 0.0137 / 0.0254 / 0.0617 against 0.0113 / 0.0206 /
 // 0.0308 / 0.0664 ms; B = 7, 8 (one round against two) and 64 or more they lose.
-// Windows of up to GDN_CHUNK_MAX_T tokens
-// run the kernel with the tiles resident in shared memory (gdn_chunk.cu, chunks
-// of 8 tokens); windows of GDN_TC_MIN_T tokens or more run the tensor-core chunk
-// kernel (gdn_window_tc.cu); any others gdn_window_kernel. The defaults are the
+// Windows of up to GDN_CHUNK_MAX_T tokens run the kernel with the tiles resident
+// in shared memory (gdn_chunk.cu, chunks of 8 tokens), unless all their units fit
+// one round of 3-CTA clusters (units <= 2 SMs / 3, window_on_clusters): such a
+// launch runs gdn_window_kernel, one v head per CTA (1 x 1 x 8: 0.0090 against
+// 0.0150 ms back to back; 4 x 1 x 8: 0.0133 against 0.0155; 4 x 1 x 16: 0.0212
+// against 0.0275; at 8 x 1 x 8, two rounds, 0.0210 against 0.0163). Windows of
+// GDN_TC_MIN_T tokens or more run the tensor-core chunk kernel
+// (gdn_window_tc.cu); any others gdn_window_kernel. The defaults are the
 // measured crossovers (16 sequences x 36 layers): the chunked kernel is the
-// fastest up to 24 tokens, the tensor-core kernel from there on, so no window
-// falls to gdn_window_kernel unless a build sets other thresholds (as timing
-// comparisons do).
+// fastest up to 24 tokens, the tensor-core kernel from there on, so no larger
+// window falls to gdn_window_kernel unless a build sets other thresholds (as
+// timing comparisons do).
 #ifndef GDN_CHUNK_MAX_T
 #define GDN_CHUNK_MAX_T 24
 #endif
@@ -640,6 +644,9 @@ bool single_token_on_clusters(long long units, int sms) {
     return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);
 }
 
+// Whether a window of at most GDN_CHUNK_MAX_T tokens over `units` units runs on the 3-CTA clusters.
+bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }
+
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long units = static_cast<long long>(a.B) * a.L * kKHeads;
     int clusters = 0, sms = 0;
@@ -648,7 +655,9 @@ cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);
     } else if (a.T <= GDN_CHUNK_MAX_T) {
-        return launch_decode_chunked(a, stream);
+        cudaError_t e = device_setup(&clusters, &sms);
+        if (e != cudaSuccess) return e;
+        if (!window_on_clusters(units, sms)) return launch_decode_chunked(a, stream);
     } else if (a.T >= GDN_TC_MIN_T) {
         return launch_decode_window_tc(a, stream);
     }

@@ -101,7 +101,11 @@ def test_kernel_sources_follow_the_library_dispatch():
         assert bench.small_single_token(units, 152) == want, units
         assert bench.kernel_name(1, units, 152) == ("gdn_window_kernel" if want else "gdn_decode_t1_kernel")
     assert names_small(16, 152)[0] == "gdn_step.cu" and names_small(128, 152)[0] == "gdn_decode_t1.cu"
-    assert bench.kernel_name(2, 16, 152) == "gdn_chunk_kernel"
+    # windows of 2-24 tokens: the clusters when all units fit one round of them (101 on 152 SMs)
+    assert bench.kernel_name(2, 16, 152) == bench.kernel_name(24, 101, 152) == "gdn_window_kernel"
+    assert bench.kernel_name(8, 102, 152) == bench.kernel_name(8, 9216, 152) == "gdn_chunk_kernel"
+    assert bench.kernel_name(25, 16, 152) == "gdn_window_tc_kernel"
+    assert os.path.basename(bench.kernel_sources(8, 64, 152)[0]) == "gdn_step.cu"
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
@@ -109,6 +113,8 @@ def test_kernel_sources_follow_the_library_dispatch():
     assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
     assert "if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);" in src
     assert "if (units > 6LL * sms) return false;" in src
+    assert "if (!window_on_clusters(units, sms)) return launch_decode_chunked(a, stream);" in src
+    assert "bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }" in src
     assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
 
 

@@ -47,11 +47,13 @@ def test_ab_gates_match_oracle(cuda_device, B, L, T, E):
     assert _rows_rel_err(beta.cpu().numpy(), rb) <= U.TOL
 
 
-@pytest.mark.parametrize("T", [1, 4, 36])
-def test_step_fed_by_ab_gates_matches_oracle(cuda_device, T):
+# 2 x 2: the 3-CTA cluster kernel for one token and four; 4 x 2: the single-token kernel and the
+# shared-memory window kernel; 36 tokens: the tensor-core kernel
+@pytest.mark.parametrize("B,T", [(2, 1), (4, 1), (2, 4), (4, 4), (2, 36)])
+def test_step_fed_by_ab_gates_matches_oracle(cuda_device, B, T):
     import gated_deltanet_linear_step_gb300 as g
 
-    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=2, L=2, T=T)
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=2, T=T)
     h = W.host_inputs(w, threads=8)
     ha = W.host_ab_inputs(w)
     t = U.to_device(h, cuda_device)

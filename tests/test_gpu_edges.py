@@ -31,7 +31,9 @@ def test_longest_window_matches_oracle(cuda_device):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-@pytest.mark.parametrize("L,T", [(3, 1), (1, 1), (2, 5), (2, 40)])  # one token: 3 x 3 single-token kernel, 3 x 1 clusters
+# one token: 3 x 3 the single-token kernel, 3 x 1 the clusters; five tokens: 3 x 2 the clusters, 3 x 3 the
+# shared-memory kernel
+@pytest.mark.parametrize("L,T", [(3, 1), (1, 1), (2, 5), (3, 5), (2, 40)])
 def test_negative_and_all_zero_lengths_change_nothing(cuda_device, L, T):
     import gated_deltanet_linear_step_gb300 as g
 
@@ -73,14 +75,15 @@ def test_single_token_call_with_lengths(cuda_device, B, L):
 
 
 @pytest.mark.parametrize("L,T,name", [(3, 1, "decode_b64_l36_t1"), (1, 1, "decode_b64_l36_t1"),
-                                      (2, 5, "verify_b16_l36_t8_ragged"), (2, 20, "verify_b16_l36_t8_ragged"),
-                                      (2, 40, "verify_b16_l36_t8_ragged")])
+                                      (2, 5, "verify_b16_l36_t8_ragged"), (3, 5, "verify_b16_l36_t8_ragged"),
+                                      (3, 20, "verify_b16_l36_t8_ragged"), (2, 40, "verify_b16_l36_t8_ragged")])
 @pytest.mark.parametrize("gate", ["sigmoid", "silu"])
 def test_saturated_activations_match_oracle(cuda_device, L, T, name, gate):
     """Inputs scaled so that SiLU, sigmoid and softplus see arguments far beyond +-88, where e^-x
     overflows or underflows in fp32: SiLU must go to x or 0, sigmoid to 1 or 0, beta to 0 or 1 and
     decay to 0 or 1, as in the fp64 oracle. Covers the single-token kernel (3 x 3 x 1), the 3-CTA
-    cluster kernel (3 x 1 x 1) and the window kernels."""
+    cluster kernel (3 x 1 x 1, 3 x 2 x 5), the shared-memory kernel (3 x 3 x 5 and 20) and the
+    tensor-core kernel."""
     import gated_deltanet_linear_step_gb300 as g
 
     w, h = _case(3, L, T, name=name)

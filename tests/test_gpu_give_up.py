@@ -20,9 +20,9 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 1, 1), (4, 3, 4), (4, 3, 12), (4, 3, 48)],
-                         ids=["single_token", "single_token_small_launch", "one_chunk_window", "multi_chunk_window",
-                              "tensor_core_window"])
+@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 1, 1), (4, 3, 4), (1, 1, 4), (4, 3, 12), (4, 3, 48)],
+                         ids=["single_token", "single_token_small_launch", "one_chunk_window",
+                              "window_small_launch", "multi_chunk_window", "tensor_core_window"])
 def test_a_wait_that_gives_up_drains_reports_and_leaves_the_context_usable(cuda_device, B, L, T):
     import gated_deltanet_linear_step_gb300 as g
 

@@ -11,11 +11,13 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T", [1, 3])
-def test_graph_replay_equals_direct_calls(cuda_device, T):
+# 3 x 2: the 3-CTA cluster kernel (one token and three); 4 x 2: the single-token kernel, the
+# shared-memory window kernel
+@pytest.mark.parametrize("B,T", [(3, 1), (4, 1), (3, 3), (4, 3)])
+def test_graph_replay_equals_direct_calls(cuda_device, B, T):
     import gated_deltanet_linear_step_gb300 as g
 
-    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=3, L=2, T=T)
+    w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=2, T=T)
     h = W.host_inputs(w, threads=8)
     direct = U.to_device(h, cuda_device)
     graphed = U.to_device(h, cuda_device)

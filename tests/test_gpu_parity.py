@@ -34,14 +34,20 @@ SMALL = [
     ("decode_b64_l36_t1", dict(B=4, L=2)),           # one token, 128 units: the single-token kernel
     ("decode_b64_l36_t1", dict(B=10, L=1)),          # one token, 160 units: the clusters again, two rounds
     ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=2, L=2)),
-    ("verify_b16_l36_t8_ragged", dict(B=6, L=2)),
-    ("decode_b1_l36_t64_zero_state", dict(L=2)),
-    ("decode_b64_l36_t1", dict(B=2, L=1, T=2)),
+    ("verify_b16_l36_t8_ragged", dict(B=6, L=2)),   # windows of 2-24 tokens over more than 101 units: the
+    ("decode_b1_l36_t64_zero_state", dict(L=2)),    # shared-memory kernel in 8-token chunks; up to 101, the
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=2)),     # 3-CTA cluster kernel (one round of clusters)
+    ("decode_b64_l36_t1", dict(B=2, L=4, T=2)),
     ("decode_b64_l36_t1", dict(B=2, L=1, T=3)),
+    ("decode_b64_l36_t1", dict(B=2, L=4, T=3)),
     ("decode_b64_l36_t1", dict(B=1, L=2, T=9)),
+    ("decode_b64_l36_t1", dict(B=1, L=8, T=9)),
     ("decode_b64_l36_t1", dict(B=2, L=1, T=17)),
+    ("decode_b64_l36_t1", dict(B=2, L=4, T=17)),
     ("verify_b16_l36_t8_ragged", dict(B=5, L=1, T=20)),
-    ("decode_b64_l36_t1", dict(B=2, L=1, T=24)),   # three full 8-token chunks, the longest on that kernel
+    ("verify_b16_l36_t8_ragged", dict(B=5, L=2, T=20)),
+    ("decode_b64_l36_t1", dict(B=2, L=1, T=24)),
+    ("decode_b64_l36_t1", dict(B=2, L=4, T=24)),   # three full 8-token chunks, the longest on that kernel
     ("decode_b64_l36_t1", dict(B=2, L=1, T=25)),   # the shortest window on the tensor-core kernel
     ("decode_b64_l36_t1", dict(B=2, L=1, T=40)),
     ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=1, L=1, T=64)),
@@ -62,8 +68,9 @@ def test_small_cases_match_oracle_elementwise(g, name, scale):
     assert np.array_equal(t["conv_state"].cpu().numpy(), rc)
 
 
-def test_silu_gate_variant_matches_oracle(g):
-    w = W.WORKLOADS["verify_b16_l36_t8_ragged"].scaled(B=3, L=2)
+@pytest.mark.parametrize("L", [2, 3])  # 96 units: the 3-CTA clusters; 144: the shared-memory kernel
+def test_silu_gate_variant_matches_oracle(g, L):
+    w = W.WORKLOADS["verify_b16_l36_t8_ragged"].scaled(B=3, L=L)
     h = W.host_inputs(w, threads=8)
     t = U.to_device(h, torch.device("cuda:0"))
     y = U.run_step(g, t, flags=g.FLAG_SILU_GATE)
@@ -138,13 +145,14 @@ def _small(scale=dict(B=3, L=2, T=9), name="verify_b16_l36_t8_ragged"):
     return w, W.host_inputs(w, threads=8)
 
 
-def test_t_tokens_in_one_call_equal_t_single_calls(g):
+@pytest.mark.parametrize("L", [2, 3])
+def test_t_tokens_in_one_call_equal_t_single_calls(g, L):
     """One T-token call and T one-token calls agree to within the parity tolerance:
     both follow the same definition, but the window kernels regroup it by chunks (in
     fp32 up to 24 tokens; past that with the products on the tensor cores, BF16 hi + lo
     operands, errors near 2e-5 of the largest value), while the single-token kernel
     sums token by token."""
-    w, h = _small(name="decode_b64_l36_t1")
+    w, h = _small(dict(B=3, L=L, T=9), name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     a = U.to_device(h, dev)
     ya = U.run_step(g, a)
@@ -161,12 +169,13 @@ def test_t_tokens_in_one_call_equal_t_single_calls(g):
     assert torch.equal(a["conv_state"], b["conv_state"])
 
 
-# (window length, prefix length): both calls of a case run the same kernel over the same chunks
-# (windows of up to 24 tokens run the shared-memory kernel in chunks of 8, 25 or more the
-# tensor-core kernel in chunks of 64), so they agree bit for bit.
-@pytest.mark.parametrize("T,P", [(8, 3), (12, 10), (40, 33), (70, 66)])
-def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
-    w, h = _small(dict(B=3, L=2, T=T))
+# (window length, prefix length, layers): both calls of a case run the same kernel over the same
+# chunks, so they agree bit for bit: up to 24 tokens the 3-CTA cluster kernel at 2 layers (the
+# prefix call's single sequence too), the shared-memory kernel in chunks of 8 at 7 layers (112 units
+# for the single sequence); 25 or more the tensor-core kernel in chunks of 64.
+@pytest.mark.parametrize("T,P,L", [(8, 3, 2), (8, 3, 7), (12, 10, 2), (12, 10, 7), (40, 33, 2), (70, 66, 2)])
+def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P, L):
+    w, h = _small(dict(B=3, L=L, T=T))
     dev = torch.device("cuda:0")
     lens = torch.tensor([0, P, T], dtype=torch.int32, device=dev)
     a = U.to_device(h, dev)
@@ -203,8 +212,9 @@ def test_ragged_equals_prefix_and_leaves_invalid_steps_untouched(g, T, P):
     assert U.state_errors(a["state"].cpu().numpy(), rs) <= U.TOL
 
 
-def test_deterministic_and_batch_permutation_equivariant(g):
-    w, h = _small(dict(B=4, L=2, T=3), name="decode_b64_l36_t1")
+@pytest.mark.parametrize("L", [2, 1])  # 128 units: the shared-memory kernel; 64: the 3-CTA clusters
+def test_deterministic_and_batch_permutation_equivariant(g, L):
+    w, h = _small(dict(B=4, L=L, T=3), name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     a = U.to_device(h, dev)
     ya = U.run_step(g, a)
@@ -221,9 +231,9 @@ def test_deterministic_and_batch_permutation_equivariant(g):
     assert torch.equal(c["conv_state"], a["conv_state"][perm])
 
 
-@pytest.mark.parametrize("T", [6, 16, 40])
-def test_verify_window_then_commit(g, T):
-    w, h = _small(dict(B=3, L=2, T=T))
+@pytest.mark.parametrize("T,L", [(6, 2), (6, 3), (16, 2), (16, 3), (40, 2)])
+def test_verify_window_then_commit(g, T, L):
+    w, h = _small(dict(B=3, L=L, T=T))
     dev = torch.device("cuda:0")
     win = U.to_device(h, dev)
     y = torch.full(win["z"].shape, float("nan"), device=dev)
@@ -249,8 +259,9 @@ def test_verify_window_then_commit(g, T):
     assert np.array_equal(win["conv_state"].cpu().numpy(), rc)
 
 
-def test_outputs_have_untouched_guard_regions(g):
-    w, h = _small(dict(B=1, L=1, T=3), name="decode_b64_l36_t1")
+@pytest.mark.parametrize("B,L", [(1, 1), (4, 2)])  # the 3-CTA clusters, the shared-memory kernel
+def test_outputs_have_untouched_guard_regions(g, B, L):
+    w, h = _small(dict(B=B, L=L, T=3), name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     t = U.to_device(h, dev)
     pad = 64  # floats = 256 bytes on each side
@@ -295,11 +306,13 @@ def test_bad_arguments_raise_and_launch_nothing(g):
     assert torch.equal(t["state"], before) and torch.all(y == 0)
 
 
-@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 2, 1), (3, 2, 4), (3, 2, 12), (3, 2, 40), (3, 2, 70)])
+@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 2, 1), (3, 2, 4), (4, 2, 4), (3, 2, 12), (4, 2, 12), (3, 2, 40),
+                                   (3, 2, 70)])
 def test_no_y_and_no_state_write_flags_match_the_full_call(g, B, L, T):
     """FLAG_NO_Y gives the full call's state and conv_state bit for bit and writes no y;
     FLAG_NO_STATE_WRITE gives its y bit for bit and leaves both states untouched. (One token: 4 x 2
-    runs the single-token kernel, 1 x 2 the 3-CTA cluster kernel.)"""
+    runs the single-token kernel, 1 x 2 the 3-CTA cluster kernel; windows up to 24 tokens: 3 x 2 the
+    cluster kernel, 4 x 2 the shared-memory kernel.)"""
     w, h = _small(dict(B=B, L=L, T=T), name="decode_b64_l36_t1")
     dev = torch.device("cuda:0")
     full = U.to_device(h, dev)

@@ -12,13 +12,14 @@ from tests import parity_util as U
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 2, 1), (2, 2, 3), (2, 2, 20), (2, 2, 40), (2, 2, 70)])
+@pytest.mark.parametrize("B,L,T", [(4, 2, 1), (1, 2, 1), (2, 2, 3), (4, 2, 3), (2, 2, 20), (4, 2, 20), (2, 2, 40),
+                                   (2, 2, 70)])
 def test_every_v_head_of_a_k_head_sees_the_old_conv_history(cuda_device, B, L, T):
     """The q/k conv history of head g is read by the work of all three v heads 3g..3g+2 and
     rolled once. Old history entries 1000x larger than any new input make a read of the
-    rolled history by any of the three show up as a y error far above the tolerance. (One token:
-    4 x 2 runs the single-token kernel, 1 x 2 the 3-CTA cluster kernel, where the three v heads are
-    on three CTAs.)"""
+    rolled history by any of the three show up as a y error far above the tolerance. (4 x 2 runs
+    the single-token kernel for one token and the shared-memory kernel for windows; 1 x 2 x 1 and
+    2 x 2 x 3 the 3-CTA cluster kernel, where the three v heads are on three CTAs.)"""
     import gated_deltanet_linear_step_gb300 as g
 
     w = W.WORKLOADS["decode_b64_l36_t1"].scaled(B=B, L=L, T=T)
