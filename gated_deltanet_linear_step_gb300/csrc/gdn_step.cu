@@ -638,14 +638,14 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 #endif
 
 // Whether a single-token launch of `units` units runs on the 3-CTA clusters (see above).
-bool single_token_on_clusters(long long units, int sms) {
+static bool single_token_on_clusters(long long units, int sms) {
     if (units > 6LL * sms) return false;
     const long long c = 2LL * sms / kGroup;  // clusters at two CTAs per SM
     return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);
 }
 
 // Whether a window of at most GDN_CHUNK_MAX_T tokens over `units` units runs on the 3-CTA clusters.
-bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }
+static bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long units = static_cast<long long>(a.B) * a.L * kKHeads;

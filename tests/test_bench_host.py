@@ -114,7 +114,7 @@ def test_kernel_sources_follow_the_library_dispatch():
     assert "if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);" in src
     assert "if (units > 6LL * sms) return false;" in src
     assert "if (!window_on_clusters(units, sms)) return launch_decode_chunked(a, stream);" in src
-    assert "bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }" in src
+    assert "static bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }" in src
     assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
 
 
