@@ -172,34 +172,40 @@ def measured_peaks():
 # The library's dispatch: one token runs the single-token kernel, or the register kernel's 3-CTA
 # clusters for launches of up to 6 units (sequence, layer, k head) per SM whose rounds of one unit per
 # cluster cost no more (measured rounds: 7.1 us against 10.7 us); windows of 2-24 tokens run the
-# kernel with the tiles in shared memory, or the clusters when all units fit one round of them
-# (units <= 2 SMs / 3); 25 tokens or more the tensor-core chunk kernel (the register kernel takes
-# larger windows only in builds with other thresholds).
+# kernel with the tiles in shared memory, or the clusters when all units fit one round of them;
+# 25 tokens or more the tensor-core chunk kernel (the register kernel takes larger windows only in
+# builds with other thresholds). The library counts the clusters that can run at once by the
+# occupancy query (97 on a 152-SM GB300); without it the functions below assume 2 SMs / 3.
 CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
 
 
-def small_single_token(units: int | None, sms: int | None) -> bool:
+def clusters_at_once(sms: int, clusters: int | None = None) -> int:
+    """3-CTA clusters that run at once: the occupancy query's count when known, else 2 sms // 3."""
+    return clusters if clusters is not None else 2 * sms // 3
+
+
+def small_single_token(units: int | None, sms: int | None, clusters: int | None = None) -> bool:
     """A single-token launch of `units` units that runs the register kernel on a GPU of `sms` SMs:
-    at most 6 units per SM, and 2 ceil(units / C) <= 3 ceil(units / sms), C = 2 sms // 3 clusters."""
+    at most 6 units per SM, and 2 ceil(units / C) <= 3 ceil(units / sms), C clusters at once."""
     if units is None or sms is None or units > 6 * sms:
         return False
-    c = 2 * sms // 3
+    c = clusters_at_once(sms, clusters)
     return 2 * -(-units // c) <= 3 * -(-units // sms)
 
 
-def small_window(units: int | None, sms: int | None) -> bool:
+def small_window(units: int | None, sms: int | None, clusters: int | None = None) -> bool:
     """A window of 2 to CHUNK_MAX_T tokens over `units` units that runs on the 3-CTA clusters: all
-    its units fit one round of them (units <= 2 sms // 3)."""
-    return units is not None and sms is not None and units <= 2 * sms // 3
+    its units fit one round of them."""
+    return units is not None and sms is not None and units <= clusters_at_once(sms, clusters)
 
 
-def kernel_name(T: int, units: int | None = None, sms: int | None = None) -> str:
+def kernel_name(T: int, units: int | None = None, sms: int | None = None, clusters: int | None = None) -> str:
     """The kernel a call with T tokens over `units` units runs on `sms` SMs (the library's dispatch;
-    without the two counts, a launch larger than the GPU)."""
+    without the counts, a launch larger than the GPU)."""
     if T == 1:
-        return "gdn_window_kernel" if small_single_token(units, sms) else "gdn_decode_t1_kernel"
+        return "gdn_window_kernel" if small_single_token(units, sms, clusters) else "gdn_decode_t1_kernel"
     if T <= CHUNK_MAX_T:
-        return "gdn_window_kernel" if small_window(units, sms) else "gdn_chunk_kernel"
+        return "gdn_window_kernel" if small_window(units, sms, clusters) else "gdn_chunk_kernel"
     if T < TC_MIN_T:
         return "gdn_window_kernel"
     return "gdn_window_tc_kernel"

@@ -611,16 +611,17 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 // One token runs the single-token kernel (gdn_decode_t1.cu: one CTA per SM, a
 // unit's three tiles on one SM, units taken in rounds of one per SM) or, for
 // launches of up to 6 units per SM, gdn_window_kernel (3-CTA clusters, one CTA
-// per tile, two CTAs per SM: rounds of one unit per cluster, 2/3 as many units
-// as SMs) when its rounds cost no more (single_token_on_clusters). Measured per
-// round at these sizes: about 10.7 us for the single-token kernel, 7.1 us for the
-// clusters, so the clusters take a launch when 2 ceil(u / C) <= 3 ceil(u / S);
+// per tile, two CTAs per SM: rounds of one unit per cluster, C units a round, C
+// the clusters the occupancy query lets run at once, 97 on 152 SMs) when its
+// rounds cost no more (single_token_on_clusters). Measured per round at these
+// sizes: about 10.7 us for the single-token kernel, 7.1 us for the clusters, so
+// the clusters take a launch when 2 ceil(u / C) <= 3 ceil(u / S);
 // 1 x 1 x 1 (16 units): 0.0054 against 0.0108 ms back to back; B x 1 x 1 with B =
 // 4, 10, 24, 48: 0.0078 / 0.0137 / 0.0254 / 0.0617 against 0.0113 / 0.0206 /
 // 0.0308 / 0.0664 ms; B = 7, 8 (one round against two) and 64 or more they lose.
 // Windows of up to GDN_CHUNK_MAX_T tokens run the kernel with the tiles resident
 // in shared memory (gdn_chunk.cu, chunks of 8 tokens), unless all their units fit
-// one round of 3-CTA clusters (units <= 2 SMs / 3, window_on_clusters): such a
+// one round of 3-CTA clusters (units <= C, window_on_clusters): such a
 // launch runs gdn_window_kernel, one v head per CTA (1 x 1 x 8: 0.0090 against
 // 0.0150 ms back to back; 4 x 1 x 8: 0.0133 against 0.0155; 4 x 1 x 16: 0.0212
 // against 0.0275; at 8 x 1 x 8, two rounds, 0.0210 against 0.0163). Windows of
@@ -637,15 +638,17 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 #define GDN_TC_MIN_T 25
 #endif
 
-// Whether a single-token launch of `units` units runs on the 3-CTA clusters (see above).
-static bool single_token_on_clusters(long long units, int sms) {
-    if (units > 6LL * sms) return false;
-    const long long c = 2LL * sms / kGroup;  // clusters at two CTAs per SM
+// Whether a single-token launch of `units` units runs on the 3-CTA clusters, `clusters` of which
+// run at once (see above).
+static bool single_token_on_clusters(long long units, int sms, int clusters) {
+    if (units > 6LL * sms || clusters <= 0) return false;
+    const long long c = clusters;
     return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);
 }
 
-// Whether a window of at most GDN_CHUNK_MAX_T tokens over `units` units runs on the 3-CTA clusters.
-static bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }
+// Whether a window of at most GDN_CHUNK_MAX_T tokens over `units` units runs on the 3-CTA clusters:
+// all its units in one round of them.
+static bool window_on_clusters(long long units, int clusters) { return units <= clusters; }
 
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long units = static_cast<long long>(a.B) * a.L * kKHeads;
@@ -653,11 +656,11 @@ cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     if (a.T == 1) {
         cudaError_t e = device_setup(&clusters, &sms);
         if (e != cudaSuccess) return e;
-        if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);
+        if (!single_token_on_clusters(units, sms, clusters)) return launch_decode_t1(a, stream);
     } else if (a.T <= GDN_CHUNK_MAX_T) {
         cudaError_t e = device_setup(&clusters, &sms);
         if (e != cudaSuccess) return e;
-        if (!window_on_clusters(units, sms)) return launch_decode_chunked(a, stream);
+        if (!window_on_clusters(units, clusters)) return launch_decode_chunked(a, stream);
     } else if (a.T >= GDN_TC_MIN_T) {
         return launch_decode_window_tc(a, stream);
     }

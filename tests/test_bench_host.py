@@ -101,6 +101,9 @@ def test_kernel_sources_follow_the_library_dispatch():
         assert bench.small_single_token(units, 152) == want, units
         assert bench.kernel_name(1, units, 152) == ("gdn_window_kernel" if want else "gdn_decode_t1_kernel")
     assert names_small(16, 152)[0] == "gdn_step.cu" and names_small(128, 152)[0] == "gdn_decode_t1.cu"
+    # with the 97 clusters the occupancy query gives on a 152-SM GB300, 400 units need a fifth round
+    assert bench.small_single_token(400, 152) and not bench.small_single_token(400, 152, clusters=97)
+    assert bench.small_window(97, 152, clusters=97) and not bench.small_window(98, 152, clusters=97)
     # windows of 2-24 tokens: the clusters when all units fit one round of them (101 on 152 SMs)
     assert bench.kernel_name(2, 16, 152) == bench.kernel_name(24, 101, 152) == "gdn_window_kernel"
     assert bench.kernel_name(8, 102, 152) == bench.kernel_name(8, 9216, 152) == "gdn_chunk_kernel"
@@ -111,10 +114,11 @@ def test_kernel_sources_follow_the_library_dispatch():
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
     assert f"#define GDN_CHUNK_MAX_T {bench.CHUNK_MAX_T}" in src
     assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
-    assert "if (!single_token_on_clusters(units, sms)) return launch_decode_t1(a, stream);" in src
-    assert "if (units > 6LL * sms) return false;" in src
-    assert "if (!window_on_clusters(units, sms)) return launch_decode_chunked(a, stream);" in src
-    assert "static bool window_on_clusters(long long units, int sms) { return units <= 2LL * sms / kGroup; }" in src
+    assert "if (!single_token_on_clusters(units, sms, clusters)) return launch_decode_t1(a, stream);" in src
+    assert "if (units > 6LL * sms || clusters <= 0) return false;" in src
+    assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
+    assert "if (!window_on_clusters(units, clusters)) return launch_decode_chunked(a, stream);" in src
+    assert "static bool window_on_clusters(long long units, int clusters) { return units <= clusters; }" in src
     assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
 
 
