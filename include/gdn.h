@@ -48,6 +48,10 @@
  *    the state come out within about 3e-5 of the exact result relative to
  *    their largest magnitude. The conv history (conv_state) is always an
  *    exact copy.
+ *  - Which kernel runs depends on T and on the launch's size (B x L; see
+ *    gdn_decode_step). A sequence's y and state can therefore differ in
+ *    their last bits between calls of different sizes, always within the
+ *    accuracy above; calls of one size are deterministic.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -106,6 +110,13 @@ typedef enum gdn_status {
  *   B, L >= 1; 1 <= T <= GDN_MAX_T.
  *
  * The state tiles stay on chip across the T tokens and are written back once.
+ * The kernel is chosen by T and by the number of units, B x L x 16 (a unit is
+ * a sequence, a layer and a k head with its three v heads): one token runs a
+ * kernel that keeps a unit's three tiles on one SM, or, when the launch is
+ * small enough that its rounds of units cost less there, 3-CTA clusters with
+ * one v head per CTA; up to 24 tokens a kernel with a unit's tiles resident in
+ * shared memory (chunks of 8 tokens), or the clusters when all units fit one
+ * round of them; from 25 tokens the tensor-core chunk kernel.
  */
 gdn_status gdn_decode_step(const float* qkv, const float* z, const float* alpha, const float* beta,
                            const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,
