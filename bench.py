@@ -171,12 +171,12 @@ def measured_peaks():
 
 # The library's dispatch: one token runs the single-token kernel, or the register kernel's 3-CTA
 # clusters for launches of up to 6 units (sequence, layer, k head) per SM whose rounds of one unit per
-# cluster cost no more (measured rounds: 7.1 us against 10.7 us); windows of 2-24 tokens run the
+# cluster cost no more (measured rounds: 7.1 us against 10.7 us); windows of 2-23 tokens run the
 # kernel with the tiles in shared memory, or the clusters when all units fit one round of them;
-# 25 tokens or more the tensor-core chunk kernel (the register kernel takes larger windows only in
+# 24 tokens or more the tensor-core chunk kernel (the register kernel takes larger windows only in
 # builds with other thresholds). The library counts the clusters that can run at once by the
 # occupancy query (97 on a 152-SM GB300); without it the functions below assume 2 SMs / 3.
-CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 24, 25, 64
+CHUNK_MAX_T, TC_MIN_T, TC_CHUNK = 23, 24, 64
 
 
 def clusters_at_once(sms: int, clusters: int | None = None) -> int:

@@ -628,14 +628,14 @@ cudaError_t device_setup(int* clusters, int* sms_out) {
 // GDN_TC_MIN_T tokens or more run the tensor-core chunk kernel
 // (gdn_window_tc.cu); any others gdn_window_kernel. The defaults are the
 // measured crossovers (16 sequences x 36 layers): the chunked kernel is the
-// fastest up to 24 tokens, the tensor-core kernel from there on, so no larger
+// fastest up to 23 tokens, the tensor-core kernel from there on, so no larger
 // window falls to gdn_window_kernel unless a build sets other thresholds (as
 // timing comparisons do).
 #ifndef GDN_CHUNK_MAX_T
-#define GDN_CHUNK_MAX_T 24
+#define GDN_CHUNK_MAX_T 23
 #endif
 #ifndef GDN_TC_MIN_T
-#define GDN_TC_MIN_T 25
+#define GDN_TC_MIN_T 24
 #endif
 
 // Whether a single-token launch of `units` units runs on the 3-CTA clusters, `clusters` of which

@@ -1,4 +1,4 @@
-// gdn_window_tc.cu - the decode step over long windows (25 tokens or more in the
+// gdn_window_tc.cu - the decode step over long windows (24 tokens or more in the
 // library's dispatch; the kernel itself takes any length of 2 or more): chunks
 // of up to 64 tokens whose contractions run on the tensor cores (tcgen05.mma
 // from shared memory into tensor memory), with the conv, the gates, the
@@ -31,7 +31,7 @@
 // below by block products, distance by distance.
 //
 // Work: one CTA (512 threads, 16 warps) per k head of a (sequence, layer), its
-// three v heads one after another; one CTA per SM (about 209 KB of shared memory
+// three v heads one after another; one CTA per SM (about 226 KB of shared memory
 // and all 512 tensor-memory columns), persistent over the units. For a single
 // chunk, the q/k preparation and the Gram matrix serve all three v heads.
 // Longer windows run the chunks of one v head in turn with its state in tensor
@@ -71,8 +71,7 @@ constexpr uint32_t kOffS = kOffKQ + 4 * kBlk128;    // S0^T: 128 columns x 128 d
 // Before S0^T the region stages the chunk's raw q rows ([64][128] fp32) and k rows
 // (the same, 32 KB further), copied 8 tokens per tensor-map box. After the state MMA:
 constexpr uint32_t kOffR = kOffS;                   //   R^T, 128 x 64: hi, lo
-constexpr uint32_t kOffX = kOffS + 2 * kBlk128;     //   the inverse X, fp32 [64][64]
-constexpr uint32_t kOffXop = kOffX + 64 * 64 * 4;   //   X as the BF16 operand, 64 x 64: hi, lo
+constexpr uint32_t kOffXop = kOffS + 3 * kBlk128;   //   X as the BF16 operand, 64 x 64: hi, lo
 constexpr uint32_t kOffDT = kOffS;                  // then D^T (128 x 64: hi, lo)
 constexpr uint32_t kOffET = kOffS + 2 * kBlk128;    //   and E^T (128 x 64: hi, lo)
 constexpr uint32_t kOffO = kOffS;                   // then o, fp32 [64][128], for the y epilogue,
@@ -87,12 +86,15 @@ constexpr uint32_t kOffTab = kOffHist + 3072;
 constexpr int kTabBeta = 0, kTabDec = 192, kTabA = 384, kTabGl = 576, kTabRk = 768, kTabRq = 832, kTabNorm = 896,
               kTabTot = 1024;
 constexpr uint32_t kOffBar = kOffTab + 1032 * 4;
-constexpr uint32_t kSmemUsed = kOffBar + 80;
+constexpr int kXStride = kC + 4;                    // fp32 row stride of the inverse X (bank spread)
+constexpr uint32_t kOffX = kOffBar + 80;            // the inverse X, fp32 [64][kXStride], in a region of its own
+constexpr uint32_t kSmemUsed = kOffX + kC * kXStride * 4;
 constexpr uint32_t kTcSmem = kSmemUsed + 1024;     // room to align the base
 
 static_assert(kOffS % 1024 == 0 && kOffP % 1024 == 0, "operand blocks are 1024-aligned");
 static_assert(kC * kS * 4 <= 2 * kBlk128, "o and z fit where S0^T was");
-static_assert(kOffXop + 2 * 64 * 128 <= kOffS + 4 * kBlk128, "R^T and X fit where S0^T was");
+static_assert(kOffXop + 2 * 64 * 128 <= kOffS + 4 * kBlk128, "R^T and X's operand fit where S0^T was");
+static_assert(kOffX % 16 == 0, "X rows are read as float4");
 static_assert(kC * 1024 <= 4 * kBlk128 && kTile * 4 <= 4 * kBlk128, "the staged rows and tile fit there too");
 static_assert(kOffV % 16 == 0 && kOffVHist % 16 == 0 && kOffHist % 16 == 0, "bulk copy destinations");
 static_assert(kTcSmem <= 232448, "one CTA per SM");
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
     float* tot_s = tab + kTabTot;
     float* L_s = reinterpret_cast<float*>(sm + kOffL);
     float* O_s = reinterpret_cast<float*>(sm + kOffO);
-    float* Xs = reinterpret_cast<float*>(sm + kOffX);  // fp32 [64][64]; blocks above the diagonal hold temporaries
+    float* Xs = reinterpret_cast<float*>(sm + kOffX);  // fp32 [64][kXStride]; blocks above the diagonal hold temporaries
     const float* Rs = reinterpret_cast<const float*>(sm + kOffS);       // staged q|k rows
     const float* Hs = reinterpret_cast<const float*>(sm + kOffHist);    // staged q/k history
     const float* Vs = reinterpret_cast<const float*>(sm + kOffV);       // staged v rows (token t at row t + 3)
@@ -625,33 +627,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                 x[r] = r > j ? acc : (r == j ? 1.0f : 0.0f);
                             }
 #pragma unroll
-                            for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kC + 16 * i + j] = x[r];
+                            for (int r = 0; r < 16; ++r) Xs[(16 * i + r) * kXStride + 16 * i + j] = x[r];
                         }
                         named_barrier(1, 256);
                         {
-                            // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj; thread
-                            // (r, c) of each 16x16 block
-                            const int r = tid >> 4, c = tid & 15;
+                            // below the diagonal, by distance: X_ij = X_ii sum_{k=j}^{i-1} Lneg_ik X_kj. Thread
+                            // (block j = tid / 64, row r, columns [c4, c4 + 4)) of the distance's blocks: rows of
+                            // Lneg and X_ii and four columns of X read as float4, each value used four times
+                            const int jb = tid >> 6, r = (tid >> 2) & 15, c4 = 4 * (tid & 3);
 #pragma unroll
                             for (int dist = 1; dist < 4; ++dist) {
-                                for (int j = 0; j + dist < 4; ++j) {
-                                    const int i = j + dist;
-                                    float y = 0.0f;
-                                    for (int k = j; k < i; ++k) {
-                                        const float* Lr = L_s + (16 * i + r) * kLStride + 16 * k;
+                                if (jb + dist < 4) {
+                                    const int j = jb, i = j + dist;
+                                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                                        for (int m = 0; m < 16; ++m) y = fmaf(Lr[m], Xs[(16 * k + m) * kC + 16 * j + c], y);
+                                    for (int k = 0; k < 3; ++k) {
+                                        if (j + k < i) {
+                                            const int kb = j + k;
+                                            const float* Lr = L_s + (16 * i + r) * kLStride + 16 * kb;
+#pragma unroll
+                                            for (int m = 0; m < 16; m += 4) {
+                                                const float4 l4 = *reinterpret_cast<const float4*>(Lr + m);
+                                                const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                                                for (int e = 0; e < 4; ++e) {
+                                                    const float4 x4 = *reinterpret_cast<const float4*>(
+                                                        Xs + (16 * kb + m + e) * kXStride + 16 * j + c4);
+                                                    y.x = fmaf(lv[e], x4.x, y.x);
+                                                    y.y = fmaf(lv[e], x4.y, y.y);
+                                                    y.z = fmaf(lv[e], x4.z, y.z);
+                                                    y.w = fmaf(lv[e], x4.w, y.w);
+                                                }
+                                            }
+                                        }
                                     }
-                                    Xs[(16 * j + r) * kC + 16 * i + c] = y;  // temporary in block (j, i)
+                                    // temporary in block (j, i)
+                                    *reinterpret_cast<float4*>(Xs + (16 * j + r) * kXStride + 16 * i + c4) = y;
                                 }
                                 named_barrier(1, 256);
-                                for (int j = 0; j + dist < 4; ++j) {
-                                    const int i = j + dist;
-                                    float x = 0.0f;
+                                if (jb + dist < 4) {
+                                    const int j = jb, i = j + dist;
+                                    const float* Dr = Xs + (16 * i + r) * kXStride + 16 * i;
+                                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                                    for (int m = 0; m < 16; ++m)
-                                        x = fmaf(Xs[(16 * i + r) * kC + 16 * i + m], Xs[(16 * j + m) * kC + 16 * i + c], x);
-                                    Xs[(16 * i + r) * kC + 16 * j + c] = x;
+                                    for (int m = 0; m < 16; m += 4) {
+                                        const float4 d4 = *reinterpret_cast<const float4*>(Dr + m);
+                                        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e) {
+                                            const float4 t4 = *reinterpret_cast<const float4*>(
+                                                Xs + (16 * j + m + e) * kXStride + 16 * i + c4);
+                                            x.x = fmaf(dv[e], t4.x, x.x);
+                                            x.y = fmaf(dv[e], t4.y, x.y);
+                                            x.z = fmaf(dv[e], t4.z, x.z);
+                                            x.w = fmaf(dv[e], t4.w, x.w);
+                                        }
+                                    }
+                                    *reinterpret_cast<float4*>(Xs + (16 * i + r) * kXStride + 16 * j + c4) = x;
                                 }
                                 named_barrier(1, 256);
                             }
@@ -665,7 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gdn_window_tc_kernel(const __gr
                                 float xv[8];
                                 const bool upper = (j >> 1) > (t >> 4);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kC + 8 * j + e];
+                                for (int e = 0; e < 8; ++e) xv[e] = upper ? 0.0f : Xs[t * kXStride + 8 * j + e];
                                 const uint32_t off = kOffXop + sw128_offset(t, j);
                                 store_split8(sm + off, sm + off + 64 * 128, xv);
                             }

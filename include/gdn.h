@@ -37,10 +37,10 @@
  *    while the kernel runs surface at the caller's next synchronisation.
  *  - Outputs may not overlap any other buffer of the call (GDN_ERR_ALIAS).
  *    Inputs may overlap each other.
- *  - Arithmetic. One token (T = 1) and windows of up to 24 tokens run the
- *    definition in fp32 on the CUDA cores (windows of 2 to 24 tokens regroup
+ *  - Arithmetic. One token (T = 1) and windows of up to 23 tokens run the
+ *    definition in fp32 on the CUDA cores (windows of 2 to 23 tokens regroup
  *    its sums per column in chunks of 8 tokens, exactly up to rounding).
- *    Windows of 25 tokens or more take chunks of 64 tokens whose
+ *    Windows of 24 tokens or more take chunks of 64 tokens whose
  *    contractions (S^T k, S^T q, the Gram matrices, the triangular solve's
  *    product and the state update) run on the tensor cores as three BF16
  *    products of each fp32 operand's hi + lo halves, accumulated in fp32:
@@ -114,9 +114,9 @@ typedef enum gdn_status {
  * a sequence, a layer and a k head with its three v heads): one token runs a
  * kernel that keeps a unit's three tiles on one SM, or, when the launch is
  * small enough that its rounds of units cost less there, 3-CTA clusters with
- * one v head per CTA; up to 24 tokens a kernel with a unit's tiles resident in
+ * one v head per CTA; up to 23 tokens a kernel with a unit's tiles resident in
  * shared memory (chunks of 8 tokens), or the clusters when all units fit one
- * round of them; from 25 tokens the tensor-core chunk kernel.
+ * round of them; from 24 tokens the tensor-core chunk kernel.
  */
 gdn_status gdn_decode_step(const float* qkv, const float* z, const float* alpha, const float* beta,
                            const float* dt, const float* ssm_a, const float* conv_w, const float* ssm_norm,

@@ -104,10 +104,10 @@ def test_kernel_sources_follow_the_library_dispatch():
     # with the 97 clusters the occupancy query gives on a 152-SM GB300, 400 units need a fifth round
     assert bench.small_single_token(400, 152) and not bench.small_single_token(400, 152, clusters=97)
     assert bench.small_window(97, 152, clusters=97) and not bench.small_window(98, 152, clusters=97)
-    # windows of 2-24 tokens: the clusters when all units fit one round of them (101 on 152 SMs)
-    assert bench.kernel_name(2, 16, 152) == bench.kernel_name(24, 101, 152) == "gdn_window_kernel"
+    # windows of 2-23 tokens: the clusters when all units fit one round of them (101 on 152 SMs)
+    assert bench.kernel_name(2, 16, 152) == bench.kernel_name(23, 101, 152) == "gdn_window_kernel"
     assert bench.kernel_name(8, 102, 152) == bench.kernel_name(8, 9216, 152) == "gdn_chunk_kernel"
-    assert bench.kernel_name(25, 16, 152) == "gdn_window_tc_kernel"
+    assert bench.kernel_name(24, 16, 152) == "gdn_window_tc_kernel"
     assert os.path.basename(bench.kernel_sources(8, 64, 152)[0]) == "gdn_step.cu"
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
