@@ -93,7 +93,8 @@ def test_kernel_sources_follow_the_library_dispatch():
     for T in (1, 2, bench.TC_MIN_T):
         kernel_src = open(bench.kernel_sources(T)[0]).read()
         assert "void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
-    # single-token launches: the register kernel's 3-CTA clusters where their rounds (101 units on 152
+    # single-token launches: the register kernel's 3-CTA clusters where their rounds (101 units on 152 SMs
+    # when the occupancy count is not given, 2 SMs / 3)
     # SMs) cost no more than the single-token kernel's (152 units), at 7.1 against 10.7 us a round
     on_clusters = {16: True, 96: True, 101: True, 102: False, 112: False, 128: False, 152: False, 160: True,
                    256: True, 384: True, 576: True, 768: True, 909: True, 912: False, 1024: False, 36864: False}
@@ -104,7 +105,7 @@ def test_kernel_sources_follow_the_library_dispatch():
     # with the 97 clusters the occupancy query gives on a 152-SM GB300, 400 units need a fifth round
     assert bench.small_single_token(400, 152) and not bench.small_single_token(400, 152, clusters=97)
     assert bench.small_window(97, 152, clusters=97) and not bench.small_window(98, 152, clusters=97)
-    # windows of 2-23 tokens: the clusters when all units fit one round of them (101 on 152 SMs)
+    # windows of 2-23 tokens: the clusters when all units fit one round of them (101 on 152 SMs by default)
     assert bench.kernel_name(2, 16, 152) == bench.kernel_name(23, 101, 152) == "gdn_window_kernel"
     assert bench.kernel_name(8, 102, 152) == bench.kernel_name(8, 9216, 152) == "gdn_chunk_kernel"
     assert bench.kernel_name(24, 16, 152) == "gdn_window_tc_kernel"

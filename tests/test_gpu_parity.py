@@ -35,7 +35,7 @@ SMALL = [
     ("decode_b64_l36_t1", dict(B=10, L=1)),          # one token, 160 units: the clusters again, two rounds
     ("decode_b128_l36_t1_beta_hi_decay_hi", dict(B=2, L=2)),
     ("verify_b16_l36_t8_ragged", dict(B=6, L=2)),   # windows of 2-23 tokens over more than 97 units: the
-    ("decode_b1_l36_t64_zero_state", dict(L=2)),    # shared-memory kernel in 8-token chunks; up to 101, the
+    ("decode_b1_l36_t64_zero_state", dict(L=2)),    # shared-memory kernel in 8-token chunks; up to 97, the
     ("decode_b64_l36_t1", dict(B=2, L=1, T=2)),     # 3-CTA cluster kernel (one round of clusters)
     ("decode_b64_l36_t1", dict(B=2, L=4, T=2)),
     ("decode_b64_l36_t1", dict(B=2, L=1, T=3)),
