@@ -94,8 +94,8 @@ def test_kernel_sources_follow_the_library_dispatch():
         kernel_src = open(bench.kernel_sources(T)[0]).read()
         assert "void __launch_bounds__" in kernel_src and bench.kernel_name(T) in kernel_src
     # single-token launches: the register kernel's 3-CTA clusters where their rounds (101 units on 152 SMs
-    # when the occupancy count is not given, 2 SMs / 3)
-    # SMs) cost no more than the single-token kernel's (152 units), at 7.1 against 10.7 us a round
+    # when the occupancy count is not given: 2 SMs / 3) cost no more than the single-token kernel's (152
+    # units), at 7.1 against 10.7 us a round
     on_clusters = {16: True, 96: True, 101: True, 102: False, 112: False, 128: False, 152: False, 160: True,
                    256: True, 384: True, 576: True, 768: True, 909: True, 912: False, 1024: False, 36864: False}
     for units, want in on_clusters.items():
