@@ -211,8 +211,17 @@ def kernel_name(T: int, units: int | None = None, sms: int | None = None, cluste
     return "gdn_window_tc_kernel"
 
 
-def kernel_sources(T: int, units: int | None = None, sms: int | None = None) -> list:
-    """The sources of the kernel a call with T tokens runs (arguments as for `kernel_name`)."""
+SOURCES_OF = {"gdn_decode_t1_kernel": ("gdn_decode_t1.cu", "gdn_device.cuh"),
+              "gdn_window_kernel": ("gdn_step.cu", "gdn_device.cuh"),
+              "gdn_chunk_kernel": ("gdn_chunk.cu", "gdn_device.cuh"),
+              "gdn_window_tc_kernel": ("gdn_window_tc.cu", "gdn_tc.cuh", "gdn_device.cuh")}
+
+
+def kernel_sources(T: int, units: int | None = None, sms: int | None = None, kernel: str | None = None) -> list:
+    """The sources of the kernel a call with T tokens runs (arguments as for `kernel_name`; `kernel`,
+    the library's own answer, decides when given)."""
+    if kernel is not None:
+        return [os.path.join(ROOT, "gated_deltanet_linear_step_gb300", "csrc", f) for f in SOURCES_OF[kernel]]
     if T == 1 and small_single_token(units, sms):
         names = ("gdn_step.cu", "gdn_device.cuh")
     elif T == 1:
@@ -245,11 +254,12 @@ def tc_mma_flops(w: W.Workload, lens) -> float:
     return total * w.L * 16
 
 
-def committed_traffic(workload: str, T: int, units: int | None = None, sms: int | None = None):
+def committed_traffic(workload: str, T: int, units: int | None = None, sms: int | None = None,
+                      kernel: str | None = None):
     """Per-launch DRAM bytes from a committed ncu summary (``profiles/*traffic*.txt``) taken on this
     workload and on the kernel source as it stands (its sha256 must match), else None."""
     digest = hashlib.sha256()
-    for path in kernel_sources(T, units, sms):
+    for path in kernel_sources(T, units, sms, kernel):
         digest.update(open(path, "rb").read())
     want = digest.hexdigest()
     if not os.path.isdir(PROFILES):
@@ -525,7 +535,6 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
     y = torch.empty(t["z"].shape, device=dev)
     step = make_step(g, t, y)
     stream = torch.cuda.current_stream(dev)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -598,14 +607,15 @@ def measure_workload(g, name: str, steps: int, warmup: int, dev) -> dict:
         torch.cuda.synchronize(dev)
         ms1 = a.elapsed_time(b) / steps
         singles = {"calls_per_step": w.T, "ms_per_step": ms1, "value": valid_tokens(w, lens) / (ms1 / 1e3),
-                   "kernel": kernel_name(1, w.B * w.L * 16, sms)}
+                   "kernel": g.gdn_dispatch_kernel(w.B, w.L, 1, device=dev)}
         del graph, calls, y1
     assert g.gdn_read_device_error(device=dev) == 0, f"a kernel reported a device error on {name}"
     updates = valid_tokens(w, lens)
-    roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T, w.B * w.L * 16, sms))
+    kernel = g.gdn_dispatch_kernel(w.B, w.L, w.T, device=dev)  # the library's own choice
+    roof = roofline_of(w, lens, ms / 1e3, committed_traffic(name, w.T, kernel=kernel))
     out = {"workload": name, "B": w.B, "L": w.L, "T": w.T, "steps": steps, "ms_per_step": ms,
            "value": updates / (ms / 1e3), "unit": UNIT,
-           "kernel": kernel_name(w.T, w.B * w.L * 16, sms), "l2": l2, "roofline": roof}
+           "kernel": kernel, "l2": l2, "roofline": roof}
     if singles is not None:
         out["as_single_token_calls"] = singles
     if working <= 2 * L2_BYTES:
@@ -704,8 +714,8 @@ def run_gdn(args, w_global, world, rank, local):
         del pipe, host, y_host
 
     mean_launch_s = float(np.mean(launch_ms)) / 1000.0
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    traffic = committed_traffic(w_global.name, w.T, w.B * w.L * 16, sms) if world == 1 else None
+    kernel = g.gdn_dispatch_kernel(w.B, w.L, w.T, device=dev)
+    traffic = committed_traffic(w_global.name, w.T, kernel=kernel) if world == 1 else None
     roofline = roofline_of(w, lens, mean_launch_s, traffic)
     del t, y, step
     torch.cuda.empty_cache()

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     gdn_decode_step,
     gdn_decode_step_ex,
     gdn_decode_step_varlen,
+    gdn_dispatch_kernel,
     gdn_get_geometry,
     gdn_in_proj,
     gdn_in_proj_noalloc,

@@ -89,6 +89,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gdn_read_device_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
+        lib.gdn_dispatch_kernel.argtypes = [_I, _I, _I]
+        lib.gdn_dispatch_kernel.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -407,6 +409,19 @@ def gdn_step_inputs_packed(x, packed, dt, ssm_a, qkv, z, gate, beta, workspace, 
     with torch.cuda.device(dev):
         _check(lib.gdn_step_inputs_packed(_ptr(x, "x", (B, L, T, E), device=dev), pp, nbytes, *p,
                                           int(workspace.numel()), B, L, T, E, _stream_handle(stream, dev)))
+
+
+DISPATCH_KERNELS = {1: "gdn_decode_t1_kernel", 2: "gdn_window_kernel", 3: "gdn_chunk_kernel", 4: "gdn_window_tc_kernel"}
+
+
+def gdn_dispatch_kernel(B: int, L: int, T: int, device=None) -> str:
+    """Name of the kernel a decode call of B x L x T runs on the device (launches nothing)."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        k = load_library().gdn_dispatch_kernel(int(B), int(L), int(T))
+    if k < 0:
+        raise GdnError(5 if B >= 1 and L >= 1 and 1 <= T else 2, gdn_last_error())
+    return DISPATCH_KERNELS[k]
 
 
 def gdn_get_geometry() -> dict:

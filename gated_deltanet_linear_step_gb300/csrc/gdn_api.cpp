@@ -429,6 +429,22 @@ gdn_status gdn_in_proj_noalloc(const float* x, const uint16_t* w_qkv, const uint
 
 const char* gdn_last_error(void) { return t_last_error.c_str(); }
 
+int gdn_dispatch_kernel(int B, int L, int T) {
+    const char* fn = "gdn_dispatch_kernel";
+    if (B < 1 || L < 1 || T < 1 || T > gdn::kMaxT) {
+        fail(GDN_ERR_SHAPE, "%s: B=%d, L=%d and T=%d must be >= 1 (T <= %d)", fn, B, L, T, gdn::kMaxT);
+        return -1;
+    }
+    gdn::DecodeKernel k;
+    const cudaError_t e = gdn::decode_kernel_for(B, L, T, &k);
+    if (e != cudaSuccess) {
+        fail(GDN_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+        return -1;
+    }
+    t_last_error.clear();
+    return static_cast<int>(k);
+}
+
 gdn_status gdn_get_geometry(int32_t out[8]) {
     if (out == nullptr) return fail(GDN_ERR_NULL, "gdn_get_geometry: out is NULL");
     out[0] = gdn::kHeadDim;

@@ -123,6 +123,12 @@ cudaError_t read_ab_error(uint32_t* out);
 // launch's size (the dispatch rules are in gdn_step.cu). Returns the launch status.
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream);
 
+// The kernels a decode call can run (values as gdn_dispatch_kernel returns them).
+enum class DecodeKernel : int { kSingleToken = 1, kClusters = 2, kChunked = 3, kTensorCore = 4 };
+
+// The kernel launch_decode_step would run for B x L x T on the current device.
+cudaError_t decode_kernel_for(int B, int L, int T, DecodeKernel* out);
+
 // The single-token kernel (gdn_decode_t1.cu); requires a.T == 1.
 cudaError_t launch_decode_t1(const StepArgs& a, cudaStream_t stream);
 

@@ -650,22 +650,38 @@ static bool single_token_on_clusters(long long units, int sms, int clusters) {
 // all its units in one round of them.
 static bool window_on_clusters(long long units, int clusters) { return units <= clusters; }
 
+// The kernel a launch of `units` units and T tokens runs, by the rules above.
+static DecodeKernel choose_kernel(long long units, int T, int sms, int clusters) {
+    if (T == 1)
+        return single_token_on_clusters(units, sms, clusters) ? DecodeKernel::kClusters : DecodeKernel::kSingleToken;
+    if (T <= GDN_CHUNK_MAX_T)
+        return window_on_clusters(units, clusters) ? DecodeKernel::kClusters : DecodeKernel::kChunked;
+    if (T >= GDN_TC_MIN_T) return DecodeKernel::kTensorCore;
+    return DecodeKernel::kClusters;
+}
+
+cudaError_t decode_kernel_for(int B, int L, int T, DecodeKernel* out) {
+    int clusters = 0, sms = 0;
+    const cudaError_t e = device_setup(&clusters, &sms);
+    if (e != cudaSuccess) return e;
+    *out = choose_kernel(static_cast<long long>(B) * L * kKHeads, T, sms, clusters);
+    return cudaSuccess;
+}
+
 cudaError_t launch_decode_step(const StepArgs& a, cudaStream_t stream) {
     const long long units = static_cast<long long>(a.B) * a.L * kKHeads;
     int clusters = 0, sms = 0;
-    if (a.T == 1) {
-        cudaError_t e = device_setup(&clusters, &sms);
+    cudaError_t e = cudaSuccess;
+    if (a.T < GDN_TC_MIN_T) {
+        e = device_setup(&clusters, &sms);
         if (e != cudaSuccess) return e;
-        if (!single_token_on_clusters(units, sms, clusters)) return launch_decode_t1(a, stream);
-    } else if (a.T <= GDN_CHUNK_MAX_T) {
-        cudaError_t e = device_setup(&clusters, &sms);
-        if (e != cudaSuccess) return e;
-        if (!window_on_clusters(units, clusters)) return launch_decode_chunked(a, stream);
-    } else if (a.T >= GDN_TC_MIN_T) {
-        return launch_decode_window_tc(a, stream);
     }
-    cudaError_t e = device_setup(&clusters, &sms);
-    if (e != cudaSuccess) return e;
+    switch (choose_kernel(units, a.T, sms, clusters)) {
+        case DecodeKernel::kSingleToken: return launch_decode_t1(a, stream);
+        case DecodeKernel::kChunked: return launch_decode_chunked(a, stream);
+        case DecodeKernel::kTensorCore: return launch_decode_window_tc(a, stream);
+        case DecodeKernel::kClusters: break;
+    }
     Params p;
     p.qkv = a.qkv;
     p.z = a.z;

@@ -381,6 +381,16 @@ void gdn_host_pipeline_destroy(gdn_host_pipeline* p);
 const char* gdn_last_error(void);
 
 /*
+ * gdn_dispatch_kernel - the kernel gdn_decode_step (and the _varlen, _ex and
+ * verify calls) runs for a launch of B x L x T on the current device, by the
+ * dispatch rules described at gdn_decode_step: 1 the single-token kernel, 2
+ * the 3-CTA cluster kernel, 3 the kernel with the tiles resident in shared
+ * memory (8-token chunks), 4 the tensor-core chunk kernel. Launches nothing.
+ * Returns -1 on a bad shape or a CUDA error (gdn_last_error() says which).
+ */
+int gdn_dispatch_kernel(int B, int L, int T);
+
+/*
  * The compiled geometry: out[0..7] = head dim, k heads, v heads, conv channels,
  * value dim, d_conv, max T, CTA threads. Always GDN_OK for a non-NULL out.
  */

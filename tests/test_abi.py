@@ -32,7 +32,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*|size_t|void)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:gdn_status|const char\*|size_t|void|int)\s+(gdn_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -41,8 +41,21 @@ def test_header_declares_the_boundary():
                "gdn_decode_step_ex", "gdn_ab_gates", "gdn_in_proj", "gdn_in_proj_workspace_size",
                "gdn_in_proj_noalloc", "gdn_step_inputs", "gdn_proj_pack_bytes", "gdn_pack_proj_weights",
                "gdn_in_proj_packed", "gdn_step_inputs_packed",
-               "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error"):
+               "gdn_last_error", "gdn_get_geometry", "gdn_read_device_error", "gdn_dispatch_kernel"):
         assert fn in names
+
+
+def test_dispatch_query_refuses_bad_shapes_before_any_cuda_call(lib):
+    """gdn_dispatch_kernel checks its shape on the host: a bad one returns -1 with a message and
+    never reaches the CUDA runtime (so this runs without a GPU)."""
+    import ctypes
+
+    lib.gdn_dispatch_kernel.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.gdn_dispatch_kernel.restype = ctypes.c_int
+    lib.gdn_last_error.restype = ctypes.c_char_p
+    for B, L, T in [(0, 1, 1), (1, 0, 1), (1, 1, 0), (1, 1, 100000)]:
+        assert lib.gdn_dispatch_kernel(B, L, T) == -1
+        assert b"gdn_dispatch_kernel" in lib.gdn_last_error()
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -110,15 +110,20 @@ def test_kernel_sources_follow_the_library_dispatch():
     assert bench.kernel_name(8, 102, 152) == bench.kernel_name(8, 9216, 152) == "gdn_chunk_kernel"
     assert bench.kernel_name(24, 16, 152) == "gdn_window_tc_kernel"
     assert os.path.basename(bench.kernel_sources(8, 64, 152)[0]) == "gdn_step.cu"
+    # given the library's own answer, the sources follow it
+    for k, first in [("gdn_decode_t1_kernel", "gdn_decode_t1.cu"), ("gdn_window_kernel", "gdn_step.cu"),
+                     ("gdn_chunk_kernel", "gdn_chunk.cu"), ("gdn_window_tc_kernel", "gdn_window_tc.cu")]:
+        assert os.path.basename(bench.kernel_sources(1, kernel=k)[0]) == first
+        assert "void __launch_bounds__" in open(bench.kernel_sources(1, kernel=k)[0]).read()
     # the thresholds are the library's defaults
     src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                             "gated_deltanet_linear_step_gb300", "csrc", "gdn_step.cu")).read()
     assert f"#define GDN_CHUNK_MAX_T {bench.CHUNK_MAX_T}" in src
     assert f"#define GDN_TC_MIN_T {bench.TC_MIN_T}" in src
-    assert "if (!single_token_on_clusters(units, sms, clusters)) return launch_decode_t1(a, stream);" in src
+    assert "return single_token_on_clusters(units, sms, clusters) ? DecodeKernel::kClusters : DecodeKernel::kSingleToken;" in src
     assert "if (units > 6LL * sms || clusters <= 0) return false;" in src
     assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
-    assert "if (!window_on_clusters(units, clusters)) return launch_decode_chunked(a, stream);" in src
+    assert "return window_on_clusters(units, clusters) ? DecodeKernel::kClusters : DecodeKernel::kChunked;" in src
     assert "static bool window_on_clusters(long long units, int clusters) { return units <= clusters; }" in src
     assert "return 2 * ((units + c - 1) / c) <= 3 * ((units + sms - 1) / sms);" in src
 

@@ -329,3 +329,20 @@ def test_no_y_and_no_state_write_flags_match_the_full_call(g, B, L, T):
     assert torch.equal(yb, yf)
     assert torch.equal(b["state"], torch.from_numpy(h["state"]).to(dev))
     assert torch.equal(b["conv_state"], torch.from_numpy(h["conv_state"]).to(dev))
+
+
+def test_dispatch_query_names_the_kernel_of_each_size(g):
+    """gdn_dispatch_kernel gives the kernel the library runs; on unambiguous sizes it agrees with the
+    rules as bench.py states them (which the bench uses only without a GPU)."""
+    import bench
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cases = {(1, 1, 1): "gdn_window_kernel", (4, 1, 1): "gdn_window_kernel", (4, 2, 1): "gdn_decode_t1_kernel",
+             (64, 36, 1): "gdn_decode_t1_kernel", (2, 1, 8): "gdn_window_kernel", (16, 36, 8): "gdn_chunk_kernel",
+             (1, 36, 64): "gdn_window_tc_kernel", (2, 1, 24): "gdn_window_tc_kernel", (4, 2, 23): "gdn_chunk_kernel"}
+    for (B, L, T), want in cases.items():
+        got = g.gdn_dispatch_kernel(B, L, T)
+        assert got == want, (B, L, T, got)
+        assert got == bench.kernel_name(T, B * L * 16, sms), (B, L, T)
+    with pytest.raises(g.GdnError):
+        g.gdn_dispatch_kernel(0, 1, 1)
