@@ -19,6 +19,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 SOURCES = ["gdn_step.cu", "gdn_decode_t1.cu", "gdn_chunk.cu", "gdn_window_tc.cu", "gdn_ab.cu", "gdn_proj.cu", "gdn_proj_noalloc.cu", "gdn_host_pipeline.cpp", "gdn_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# A standalone measuring program, not linked into the library: the device's FP32 FMA rate.
+FMA_RATE_SRC = "fp32_fma_rate.cu"
+FMA_RATE_EXE = os.path.join(BUILD, "fp32_fma_rate")
 
 
 def nvcc() -> str:
@@ -29,7 +32,8 @@ def nvcc() -> str:
 
 
 def build(verbose: bool = False) -> str:
-    """Compiles every source in parallel and links ``libgdn.so``; returns its path."""
+    """Compiles every source in parallel and links ``libgdn.so``; returns its path. Also builds the
+    FP32 FMA-rate program (``_build/fp32_fma_rate``) from ``csrc/fp32_fma_rate.cu``."""
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -42,8 +46,16 @@ def build(verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         return obj, r.stderr
 
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
+    def compile_fma_rate():
+        cmd = [cc] + ARCH + ["-O3", "-std=c++17", "-lineinfo", os.path.join(CSRC, FMA_RATE_SRC), "-o", FMA_RATE_EXE]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {FMA_RATE_SRC}:\n{r.stdout}\n{r.stderr}")
+
+    with ThreadPoolExecutor(len(SOURCES) + 1) as ex:
+        fma_rate = ex.submit(compile_fma_rate)
         results = list(ex.map(compile_one, SOURCES))
+        fma_rate.result()
     if verbose:
         for _, log in results:
             for line in log.splitlines():
