@@ -248,12 +248,18 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
     cluster_sync();  // every rank's sums are in their owners' receive areas
 
     // ---- rank r finishes the tokens j = r mod 4 (four outputs per item) and applies the gate epilogue
-    constexpr int kChunks = kOut / 4;  // 24 float4 per token
+    //      The items run every token's alpha chunks first, then every token's beta chunks, so a warp
+    //      takes the softplus or the sigmoid branch, not both.
+    constexpr int kChunks = kOut / 4;   // 24 float4 per token
+    constexpr int kHalf = kChunks / 2;  // 12 of them alpha, 12 beta
     const int n_mine = (n_blk - rank + kSplit - 1) / kSplit;
+    const int n_half = n_mine * kHalf;
     if (!*abort_flag) {
-        for (int it = tid; it < n_mine * kChunks; it += kAbThreads) {
-            const int q = it % kChunks;
-            const int slot = it / kChunks;
+        for (int it = tid; it < 2 * n_half; it += kAbThreads) {
+            const bool is_beta = it >= n_half;
+            const int k = is_beta ? it - n_half : it;
+            const int slot = k / kHalf;
+            const int q = k % kHalf + (is_beta ? kHalf : 0);
             const int j = rank + kSplit * slot;
             const int b = b0 + j / p.Tb, t = t0 + j % p.Tb;
             if (j >= rows_box || b >= p.B || t >= p.T) continue;
@@ -270,20 +276,16 @@ __global__ void __launch_bounds__(kAbThreads, 1) gdn_ab_gates_kernel(const __gri
             const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
             float4 r;
             float* rr = &r.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = 4 * q + e;
-                if (row < kAbRows) {
-                    rr[e] = softplusf_(sv[e] + lw[row]) * lw[kVHeads + row];
-                } else {
-                    rr[e] = sigmoidf_(sv[e]);
-                }
-            }
             // chunks 0-11 are gate heads 0-47, chunks 12-23 beta heads 0-47
-            if (q < kChunks / 2)
+            if (!is_beta) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) rr[e] = softplusf_(sv[e] + lw[4 * q + e]) * lw[kVHeads + 4 * q + e];
                 *reinterpret_cast<float4*>(p.gate + orow + 4 * q) = r;
-            else
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) rr[e] = sigmoidf_(sv[e]);
                 *reinterpret_cast<float4*>(p.beta + orow + 4 * q - kAbRows) = r;
+            }
         }
     }
     // (no CTA reads another's shared memory after the barrier, so each may leave on its own)
